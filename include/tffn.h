@@ -1,0 +1,189 @@
+/*
+ * tffn.h -- C ABI of the GB300-native fused Transformer FFN library.
+ *
+ * All tensors are dense row-major arrays in DEVICE memory of the current CUDA
+ * device, owned by the caller; the library never frees them and keeps no
+ * pointer to them after a call returns.  bf16 means IEEE bfloat16 (the upper
+ * 16 bits of a binary32).  Calls are asynchronous on `stream` (a cudaStream_t;
+ * NULL = legacy default stream): the return value covers argument validation
+ * and launch errors only.  Errors found by a kernel while it runs (a wait that
+ * timed out) are kept in the workspace and returned by tffn_check().
+ *
+ * Shapes and pointer rules shared by every entry point:
+ *   - N, O, P are multiples of 8 and >= 8 (rows of every operand start on a
+ *     16-byte boundary, as the tensor-memory-accelerator copies require);
+ *   - every tensor pointer is 16-byte aligned;
+ *   - M, T >= 0 (0 rows is a valid, empty call);
+ *   - bias pointers may be NULL, meaning a zero bias.
+ * A violation returns TFFN_ERR_INVALID_ARG before anything is launched.
+ *
+ * Workspace: the fused path keeps the hidden tensor H, ready flags and a
+ * control block in a device workspace.  By default the library allocates it
+ * (cudaMalloc, once per device, grown on demand; never inside a call that is
+ * being captured into a CUDA graph if it has to grow).  A caller may instead
+ * hand in its own buffer with tffn_set_workspace().  Calls that share a
+ * workspace must be ordered on the GPU (same stream, or ordered by events).
+ */
+#ifndef TFFN_H
+#define TFFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+/* Elementwise activations.  GELU is the tanh form
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))). */
+typedef enum {
+    TFFN_ACT_NONE = 0,
+    TFFN_ACT_RELU = 1,
+    TFFN_ACT_GELU_TANH = 2
+} tffn_act;
+
+typedef enum {
+    TFFN_OK = 0,
+    TFFN_ERR_INVALID_ARG = -1,   /* bad pointer, size, alignment or code   */
+    TFFN_ERR_UNSUPPORTED = -2,   /* valid, but outside what is implemented */
+    TFFN_ERR_CUDA = -3,          /* a CUDA runtime call failed             */
+    TFFN_ERR_TIMEOUT = -4,       /* a device-side wait ran out of time     */
+    TFFN_ERR_NO_WORKSPACE = -5,  /* caller workspace too small             */
+    TFFN_ERR_DEVICE = -6         /* other device-detected error            */
+} tffn_status;
+
+/*
+ * ffn_forward -- Y = act2(act1(X W1 + b1) W2 + b2).
+ *
+ * Defined by "Kernel fusion and tensor parallelism" (brunomaga.github.io),
+ * section "Megatron-LM tensor parallelism", the FFN equation: H is
+ * act(X W1 + b1), Y is act(H W2 + b2), X in R^{MxN}, W1 in R^{NxO},
+ * b1 in R^O, W2 in R^{OxP}, b2 in R^P; the second activation is optional
+ * (TFFN_ACT_NONE), as Transformer FFNs omit it.  Section "Step 1" of the same
+ * page fixes how the work is fused: each tile of H is multiplied by its row of
+ * W2 tiles as soon as it is ready (Y_ik = sum_j H_ij (W2)_jk).
+ *
+ *   X  [M x N] bf16      W1 [N x O] bf16      b1 [O] bf16 (nullable)
+ *   W2 [O x P] bf16      b2 [P] bf16 (nullable)
+ *   Y  [M x P] bf16 (written; must not alias an input)
+ *   act1, act2: tffn_act codes.
+ *
+ * Numerics: products accumulate in fp32; H is rounded to bf16 (round to
+ * nearest even) after b1 and act1, as it is stored between the layers; Y is
+ * rounded to bf16 after b2 and act2.
+ * Paths: M <= 32 streams the weights (split-K, HBM-bound decode shapes);
+ * larger M runs the persistent tcgen05 engine (GEMM1 tiles publish ready
+ * flags that GEMM2 tiles consume in the same launch).
+ */
+int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, const void* b2,
+                int act1, int act2, int64_t M, int64_t N, int64_t O, int64_t P, void* Y,
+                struct CUstream_st* stream);
+
+/* Optional routing outputs of moe_ffn_forward (every member nullable; device
+ * pointers): topk_idx[T*k] int32 and topk_w[T*k] fp32, slot s of token t at
+ * t*k+s; perm[T*k] int32 maps the expert-grouped row r to t*k+s;
+ * expert_offsets[E+1] int32 are the first grouped row of each expert. */
+typedef struct {
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* perm;
+    int32_t* expert_offsets;
+} tffn_routing;
+
+/*
+ * moe_ffn_forward -- Mixture-of-Experts FFN: each token goes to its top_k
+ * experts by gate logit; the output is the gate-weighted sum of those experts'
+ * FFN outputs.
+ *
+ * Defined by "Fine-Grained Compute-Communication Overlap for MoE" (review of
+ * arXiv 2607.19539, zhongzhuzhou.org), section 2.1 (the router's distribution
+ * over E experts, top-k selection, gate-weighted sum) and section 2.2 steps 1,
+ * 3 and 5 (routing, expert computation, weighted reduction); section 4.2 (rows
+ * grouped contiguously per destination, each group zero-padded to a whole
+ * tile) gives the grouped row layout; the expert FFN is ffn_forward's
+ * ("Kernel fusion and tensor parallelism", section "Expert sharding").
+ *
+ *   X            [T x N] bf16
+ *   gate_logits  [T x E] fp32
+ *   W1, b1, W2, b2: HOST arrays of E DEVICE pointers; W1[e] [N x O],
+ *                b1[e] [O] (array or entries nullable), W2[e] [O x P],
+ *                b2[e] [P] (nullable) -- all bf16
+ *   Y            [T x P] bf16 (written)
+ *   1 <= top_k <= E <= 64.
+ *
+ * Routing: slot 0 holds the largest logit; equal logits go to the lower
+ * expert index; the gate weights are the softmax over the top_k kept logits
+ * (= softmax over E, keep top_k, renormalise to sum 1).  Each expert applies
+ * its own b2 and act2 before the gate weighting; the weighted sum is taken in
+ * fp32 in slot order and rounded to bf16 once.
+ */
+int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const void* const* W1,
+                    const void* const* b1, const void* const* W2, const void* const* b2, void* Y,
+                    int64_t T, int64_t N, int64_t O, int64_t P, int E, int act1, int act2,
+                    tffn_routing* routing, struct CUstream_st* stream);
+
+/* Bytes of workspace a call of this shape needs (E = 0 for ffn_forward). */
+size_t tffn_workspace_bytes(int64_t M, int64_t N, int64_t O, int64_t P, int E, int top_k);
+
+/* Use a caller-owned device buffer (>= 256-byte aligned) as the workspace of
+ * the current device from the next call on; NULL returns to the
+ * library-owned workspace.  The library initialises the buffer's control and
+ * flag region on the next call's stream. */
+int tffn_set_workspace(void* dev_ptr, size_t bytes);
+
+/* Synchronise `stream`, then read and clear the current device's device-side
+ * error record.  Returns TFFN_OK, TFFN_ERR_TIMEOUT or TFFN_ERR_DEVICE (or
+ * TFFN_ERR_CUDA if the synchronisation itself failed).  `detail` (nullable,
+ * 4 entries) receives {status, wait site, block, info}. */
+int tffn_check(struct CUstream_st* stream, int32_t* detail);
+
+/* Static description of a status code. */
+const char* tffn_status_string(int status);
+
+/* Tuning and test controls (process-wide):
+ *   TFFN_OPT_PATH         0 auto, 1 fused engine, 2 decode stream, 3 engine
+ *                         as two launches (layer 1, then layer 2)
+ *   TFFN_OPT_WAIT_LIMIT_MS  device wait limit in ms (default 4000)
+ *   TFFN_OPT_SKIP_FLAG    test fault injection: the engine never publishes
+ *                         the ready flag of this GEMM1 tile index (-1 = off);
+ *                         the waiting GEMM2 tile then times out and the call
+ *                         reports TFFN_ERR_TIMEOUT through tffn_check()
+ *   TFFN_OPT_GROUP_M      row bands per raster group of the engine (default 8)
+ * Returns the previous value. */
+enum {
+    TFFN_OPT_PATH = 1,
+    TFFN_OPT_WAIT_LIMIT_MS = 2,
+    TFFN_OPT_SKIP_FLAG = 3,
+    TFFN_OPT_GROUP_M = 4
+};
+int64_t tffn_set_option(int option, int64_t value);
+
+/* Kernels the most recent forward call on this thread launched. */
+int tffn_last_launch_count(void);
+
+/* Timing of the dominant kernel (the engine, or the decode stream): while
+ * enabled, each forward call records a CUDA event pair around its dominant
+ * kernel on the call's stream.  tffn_timing_end synchronises those events and
+ * returns the number of timed launches and their summed milliseconds. */
+int tffn_timing_begin(void);
+int tffn_timing_end(int* launches, double* total_ms);
+
+/* Host-side view of the engine's task order, for tests (no GPU needed):
+ * the task of `ticket` for a fused launch with m_blocks row bands, n1 GEMM1
+ * and n2 GEMM2 column tiles and raster groups of group_m bands.  out[0] =
+ * layer (0 or 1, -1 past the end), out[1] = row band, out[2] = column tile.
+ * Returns the total number of tickets. */
+int64_t tffn_debug_engine_task(int64_t m_blocks, int32_t n1, int32_t n2, int32_t group_m,
+                               int64_t ticket, int32_t out[3]);
+
+/* Tile sizes of the engine (rows, columns, k-step) and of the decode stream,
+ * for tests and tools: out[0..5] = {BM, BN, BK, stages, decode slice width,
+ * decode k chunk}. */
+void tffn_debug_tiles(int32_t out[6]);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TFFN_H */

@@ -1,0 +1,142 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports every
+symbol the public header declares, validates arguments before touching CUDA,
+and its host-side task order is dependency-safe."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from transformer_ffn_gb300 import build
+    build.build()
+    import transformer_ffn_gb300 as tffn
+    return tffn.load()
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "tffn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "sizeof")))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("ffn_forward", "moe_ffn_forward", "tffn_workspace_bytes", "tffn_set_workspace",
+              "tffn_check", "tffn_status_string", "tffn_set_option"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), f"missing export {n}"
+
+
+def test_status_strings(lib):
+    for code in range(-6, 1):
+        s = lib.tffn_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.tffn_status_string(-99) == b"unknown status"
+
+
+def _ffn(lib, X=16, W1=16, W2=16, Y=16, M=64, N=256, O=1024, P=256, act1=2, act2=0, b1=None, b2=None):
+    return lib.ffn_forward(X, W1, b1, W2, b2, act1, act2, M, N, O, P, Y, None)
+
+
+def test_ffn_validation_without_gpu(lib):
+    bad = -1
+    assert _ffn(lib, X=None) == bad
+    assert _ffn(lib, W1=None) == bad
+    assert _ffn(lib, W2=None) == bad
+    assert _ffn(lib, Y=None) == bad
+    assert _ffn(lib, N=12) == bad          # not a multiple of 8
+    assert _ffn(lib, O=0) == bad
+    assert _ffn(lib, P=4) == bad
+    assert _ffn(lib, M=-1) == bad
+    assert _ffn(lib, act1=7) == bad
+    assert _ffn(lib, act2=-1) == bad
+    assert _ffn(lib, X=24) == bad          # 8-byte aligned only
+    assert _ffn(lib, b1=40) == bad
+    assert _ffn(lib, M=0) == 0             # empty call: nothing to do, no launch
+    assert lib.tffn_last_launch_count() == 0
+
+
+def test_moe_validation_without_gpu(lib):
+    E = 4
+    arr = (ctypes.c_void_p * E)(*([16] * E))
+    p = ctypes.cast(arr, ctypes.c_void_p)
+
+    def call(top_k=2, E=E, T=32, N=64, w1=p, X=16, logits=16):
+        return lib.moe_ffn_forward(X, logits, top_k, w1, None, p, None, 16, T, N, 64, 64, E, 2, 0,
+                                   None, None)
+    assert call(top_k=0) == -1
+    assert call(top_k=5) == -1
+    assert call(E=0, top_k=1) == -1
+    assert call(E=65, top_k=1) == -1
+    assert call(N=20) == -1
+    assert call(X=None) == -1
+    assert call(logits=None) == -1
+    zeros = (ctypes.c_void_p * E)(*([16, 0, 16, 16]))
+    assert call(w1=ctypes.cast(zeros, ctypes.c_void_p)) == -1
+    assert call(T=0) == 0
+
+
+def test_workspace_bytes_holds_hidden_tensor(lib):
+    import json
+    with open(os.path.join(ROOT, "tests", "golden", "page1_llama3_70b_sizes.json")) as f:
+        g = json.load(f)
+    # one GPU's slice of the page's Llama 3 70B example: H^(g) is 56 MiB in bf16
+    tokens, cols = g["tokens"], g["hidden_cols_per_gpu"]
+    assert tokens * cols * 2 == g["hidden_slice_mib"] * 2**20
+    ws = lib.tffn_workspace_bytes(tokens, g["N"], cols, g["P"], 0, 0)
+    assert ws >= g["hidden_slice_mib"] * 2**20
+    assert ws < (g["hidden_slice_mib"] + 16) * 2**20
+    # invalid shapes report 0
+    assert lib.tffn_workspace_bytes(tokens, 12, cols, 8, 0, 0) == 0
+
+
+def test_engine_task_order_is_dependency_safe(lib):
+    import transformer_ffn_gb300 as tffn
+    for (mb, n1, n2, gm) in [(1, 4, 1, 8), (3, 5, 2, 1), (9, 7, 3, 4), (17, 3, 5, 8), (32, 64, 16, 8),
+                             (5, 1, 1, 16), (40, 2, 9, 3)]:
+        total, _ = tffn.debug_engine_task(mb, n1, n2, gm, 0)
+        assert total == mb * (n1 + n2)
+        seen = set()
+        done_l1 = {}
+        for t in range(total):
+            _, (layer, band, tile) = tffn.debug_engine_task(mb, n1, n2, gm, t)
+            assert layer in (0, 1)
+            assert 0 <= band < mb
+            assert (layer, band, tile) not in seen
+            seen.add((layer, band, tile))
+            if layer == 0:
+                assert 0 <= tile < n1
+                done_l1[band] = done_l1.get(band, 0) + 1
+            else:
+                assert 0 <= tile < n2
+                # every layer-1 tile of this band has a smaller ticket
+                assert done_l1.get(band, 0) == n1
+        assert len(seen) == total
+        _, (layer, _, _) = tffn.debug_engine_task(mb, n1, n2, gm, total)
+        assert layer == -1
+
+
+def test_debug_tiles(lib):
+    import transformer_ffn_gb300 as tffn
+    t = tffn.debug_tiles()
+    assert t["BM"] == 128 and t["BN"] % 64 == 0 and t["BK"] == 64
+    assert t["decode_slice"] == t["decode_kc"]
+
+
+def test_ops_fail_loudly_without_library(monkeypatch, tmp_path):
+    import transformer_ffn_gb300 as tffn
+    monkeypatch.setattr(tffn, "_lib", None)
+    monkeypatch.setattr(tffn, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        tffn.load()

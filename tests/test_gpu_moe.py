@@ -1,0 +1,113 @@
+"""Parity of moe_ffn_forward (through the C ABI) with the CPU oracle.
+
+Routing indices, the expert-grouped permutation and the expert offsets must
+match the oracle bit for bit; gate weights and outputs within the floating
+point tolerance |y - y_ref| <= 1e-2 + 1e-2 |y_ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from transformer_ffn_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+ACT = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "gelu_tanh": oracle.ACT_GELU_TANH}
+
+
+def _assert_close(got, want, what=""):
+    err = np.abs(got - want)
+    bound = 1e-2 + 1e-2 * np.abs(want)
+    bad = err > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} out of tolerance, max err {err.max():.3e}"
+
+
+def _inputs(T, N, O, P, E, seed, logits=None, device="cuda"):
+    return synth.moe_inputs(T, N, O, P, E, seed=seed, device=device, logits=logits)
+
+
+def _oracle_y(inp, k, act1, act2, tokens=None):
+    u = synth.to_u16
+    return oracle.moe_ffn(u(inp.X), inp.logits.cpu().numpy(), k, [u(w) for w in inp.W1],
+                          [u(b) for b in inp.b1], [u(w) for w in inp.W2], [u(b) for b in inp.b2],
+                          ACT[act1], ACT[act2], tokens=tokens)
+
+
+def _check_routing(r, logits, k, E):
+    lg = logits.cpu().numpy()
+    idx, w = oracle.moe_route(lg, k)
+    np.testing.assert_array_equal(r["topk_idx"].cpu().numpy(), idx)
+    np.testing.assert_allclose(r["topk_w"].cpu().numpy(), w, rtol=1e-5, atol=1e-6)
+    perm, offs = oracle.moe_permute(idx, E)
+    np.testing.assert_array_equal(r["perm"].cpu().numpy(), perm)
+    np.testing.assert_array_equal(r["expert_offsets"].cpu().numpy(), offs)
+
+
+@pytest.mark.parametrize("T,N,O,P,E,k,acts", [
+    (300, 64, 256, 128, 8, 2, ("gelu_tanh", "none")),
+    (77, 128, 136, 72, 4, 1, ("relu", "relu")),
+    (129, 64, 512, 264, 16, 4, ("gelu_tanh", "gelu_tanh")),
+    (1, 64, 128, 64, 8, 2, ("gelu_tanh", "none")),
+    (40, 64, 128, 64, 1, 1, ("relu", "none")),
+    (50, 64, 128, 64, 4, 4, ("gelu_tanh", "none")),      # top_k = E
+])
+def test_moe_small_full(cuda_lib, T, N, O, P, E, k, acts):
+    inp = _inputs(T, N, O, P, E, seed=T + E)
+    Y, r = cuda_lib.moe_ffn_forward(inp.X, inp.logits, k, inp.W1, inp.b1, inp.W2, inp.b2,
+                                    acts[0], acts[1], routing=True)
+    cuda_lib.check()
+    _check_routing(r, inp.logits, k, E)
+    _assert_close(Y.float().cpu().numpy(), _oracle_y(inp, k, *acts), "moe")
+
+
+def test_moe_skewed_routing(cuda_lib):
+    # one expert nobody picks, one expert every token picks, exact ties
+    T, N, O, P, E, k = 200, 64, 256, 128, 8, 2
+    g = torch.Generator(device="cpu").manual_seed(9)
+    logits = torch.randn((T, E), generator=g)
+    logits[:, 5] = -50.0
+    logits[:, 2] = 50.0
+    logits[::4, 0] = logits[::4, 1]
+    inp = _inputs(T, N, O, P, E, seed=4, logits=logits.cuda())
+    Y, r = cuda_lib.moe_ffn_forward(inp.X, inp.logits, k, inp.W1, inp.b1, inp.W2, inp.b2,
+                                    "gelu_tanh", "none", routing=True)
+    cuda_lib.check()
+    _check_routing(r, inp.logits, k, E)
+    offs = r["expert_offsets"].cpu().numpy()
+    assert offs[6] - offs[5] == 0 and offs[3] - offs[2] == T
+    _assert_close(Y.float().cpu().numpy(), _oracle_y(inp, k, "gelu_tanh", "none"), "skewed")
+
+
+def test_moe_equal_gates_top_all_is_mean_of_experts(cuda_lib):
+    T, N, O, P, E = 64, 64, 128, 64, 4
+    inp = _inputs(T, N, O, P, E, seed=8, logits=torch.zeros((T, E), device="cuda"))
+    Y = cuda_lib.moe_ffn_forward(inp.X, inp.logits, E, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh", "none")
+    cuda_lib.check()
+    dense = sum(cuda_lib.ffn_forward(inp.X, inp.W1[e], inp.b1[e], inp.W2[e], inp.b2[e], "gelu_tanh",
+                                     "none").float() for e in range(E)) / E
+    cuda_lib.check()
+    err = (Y.float() - dense).abs()
+    assert torch.all(err <= 2e-2 + 2e-2 * dense.abs())
+
+
+def test_moe_deterministic(cuda_lib):
+    inp = _inputs(500, 128, 512, 256, 8, seed=12)
+    a = cuda_lib.moe_ffn_forward(inp.X, inp.logits, 2, inp.W1, inp.b1, inp.W2, inp.b2)
+    b = cuda_lib.moe_ffn_forward(inp.X, inp.logits, 2, inp.W1, inp.b1, inp.W2, inp.b2)
+    cuda_lib.check()
+    assert torch.equal(a, b)
+
+
+def test_moe_full_size_sampled_tokens(cuda_lib):
+    # T 8192, N 4096, E 8 experts of O 14336, P 4096, softmax top-2, GELU-tanh
+    T, N, O, P, E, k = 8192, 4096, 14336, 4096, 8, 2
+    inp = _inputs(T, N, O, P, E, seed=0)
+    Y, r = cuda_lib.moe_ffn_forward(inp.X, inp.logits, k, inp.W1, inp.b1, inp.W2, inp.b2,
+                                    "gelu_tanh", "none", routing=True)
+    cuda_lib.check()
+    _check_routing(r, inp.logits, k, E)
+    tokens = [0, 1, 4095, 8191, 1234, 7000]
+    _assert_close(Y[tokens].float().cpu().numpy(), _oracle_y(inp, k, "gelu_tanh", "none", tokens=tokens),
+                  "moe full size")
+    assert torch.isfinite(Y.float()).all()

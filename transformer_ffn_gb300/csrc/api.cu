@@ -1,0 +1,660 @@
+// api.cu -- the C ABI (include/tffn.h): argument validation, the workspace,
+// tensor-map encoding and kernel launches.  No arithmetic of the FFN happens
+// here; every step of the path runs in the kernels of this directory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "../../include/tffn.h"
+#include "decode.cuh"
+#include "engine.cuh"
+#include "launch.h"
+#include "schedule.h"
+
+namespace {
+
+using namespace tffn;
+
+// ----------------------------------------------------------- workspace map
+// [0, 256)                 DevCtrl
+// [256, 256 + 4 MiB)       ready flags / counters (engine: one per layer-1 tile)
+// [.., + 256 KiB)          decode split-K arrival counters
+// [SYNC_BYTES, ...)        data: H, grouped rows, partial sums
+// The sync region is zeroed when a workspace is (re)initialised; after that,
+// flags are compared against a per-call epoch and counters are reset by the
+// kernels, so no per-call clearing is needed.
+constexpr size_t OFF_FLAGS = 256;
+constexpr size_t FLAG_WORDS = size_t(1) << 20;
+constexpr size_t OFF_DCOUNT = OFF_FLAGS + FLAG_WORDS * 4;
+constexpr size_t DCOUNT_WORDS = size_t(1) << 16;
+constexpr size_t SYNC_BYTES = size_t(5) << 20;
+static_assert(OFF_DCOUNT + DCOUNT_WORDS * 4 <= SYNC_BYTES, "sync region layout");
+constexpr uint32_t EPOCH_LIMIT = 0xFFFFFFF0u;      // flag words hold the epoch of their last write
+
+constexpr int64_t DECODE_MAX_M = 32;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct DeviceState {
+    bool init = false;
+    int sms = 0;
+    void* owned = nullptr;
+    size_t owned_bytes = 0;
+    void* user = nullptr;
+    size_t user_bytes = 0;
+    bool user_set = false;
+    bool needs_reset = true;
+    uint32_t epoch = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[64];
+
+std::atomic<int64_t> g_opt_path{0};
+std::atomic<int64_t> g_opt_wait_ms{4000};
+std::atomic<int64_t> g_opt_skip{-1};
+std::atomic<int64_t> g_opt_group{8};
+
+thread_local int g_last_launches = 0;
+thread_local bool g_timing = false;
+thread_local std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_events;
+thread_local size_t g_events_used = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int get_encode()
+{
+    if (g_encode)
+        return 0;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return -1;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return 0;
+}
+
+// Row-major bf16 matrix [outer x inner], box [box_outer x box_inner], 128-byte
+// swizzle, zero fill outside the matrix.
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+             uint32_t box_outer)
+{
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool act_ok(int a) { return a == TFFN_ACT_NONE || a == TFFN_ACT_RELU || a == TFFN_ACT_GELU_TANH; }
+bool dim_ok(int64_t d) { return d >= 8 && d % 8 == 0 && d < (int64_t(1) << 31); }
+
+// Current device's state, initialised on first use.
+int device_state(DeviceState** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return TFFN_ERR_CUDA;
+    DeviceState& d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TFFN_ERR_CUDA;
+        if (get_encode() != 0)
+            return TFFN_ERR_CUDA;
+        d.init = true;
+    }
+    *out = &d;
+    return TFFN_OK;
+}
+
+// Workspace of at least `need` bytes, initialised; returns its base.
+int workspace(DeviceState& d, size_t need, cudaStream_t s, uint8_t** base)
+{
+    void* b = nullptr;
+    if (d.user_set) {
+        if (d.user_bytes < need)
+            return TFFN_ERR_NO_WORKSPACE;
+        b = d.user;
+    } else {
+        if (d.owned_bytes < need) {
+            if (d.owned) {
+                if (cudaFree(d.owned) != cudaSuccess)
+                    return TFFN_ERR_CUDA;
+                d.owned = nullptr;
+                d.owned_bytes = 0;
+            }
+            const size_t bytes = align_up(need, size_t(64) << 20);
+            if (cudaMalloc(&d.owned, bytes) != cudaSuccess) {
+                d.owned = nullptr;
+                return TFFN_ERR_CUDA;
+            }
+            d.owned_bytes = bytes;
+            d.needs_reset = true;
+        }
+        b = d.owned;
+    }
+    if (d.needs_reset) {
+        if (cudaMemsetAsync(b, 0, SYNC_BYTES, s) != cudaSuccess)
+            return TFFN_ERR_CUDA;
+        d.epoch = 0;
+        d.needs_reset = false;
+    }
+    *base = static_cast<uint8_t*>(b);
+    return TFFN_OK;
+}
+
+// Epoch for the next launch that uses ready flags.
+int next_epoch(DeviceState& d, uint8_t* base, cudaStream_t s, uint32_t* epoch)
+{
+    if (d.epoch >= EPOCH_LIMIT) {
+        if (cudaMemsetAsync(base + OFF_FLAGS, 0, FLAG_WORDS * 4, s) != cudaSuccess)
+            return TFFN_ERR_CUDA;
+        d.epoch = 0;
+    }
+    *epoch = ++d.epoch;
+    return TFFN_OK;
+}
+
+void timing_start(cudaStream_t s)
+{
+    if (!g_timing)
+        return;
+    if (g_events_used == g_events.size()) {
+        cudaEvent_t a, b;
+        cudaEventCreate(&a);
+        cudaEventCreate(&b);
+        g_events.emplace_back(a, b);
+    }
+    cudaEventRecord(g_events[g_events_used].first, s);
+}
+
+void timing_stop(cudaStream_t s)
+{
+    if (!g_timing)
+        return;
+    cudaEventRecord(g_events[g_events_used].second, s);
+    ++g_events_used;
+}
+
+uint64_t wait_limit_ns()
+{
+    int64_t ms = g_opt_wait_ms.load();
+    if (ms < 1)
+        ms = 1;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+}
+
+// ------------------------------------------------------------------ layouts
+struct DenseLayout {
+    int path = 0;          // 1 engine fused, 2 decode, 3 engine two launches
+    int64_t m_blocks = 0;
+    int32_t n1 = 0, n2 = 0;
+    size_t off_h = 0;      // engine: H [m_blocks*BM x O]; decode: H [M x O]
+    size_t off_part = 0;   // decode: split-K partial sums
+    size_t total = 0;
+};
+
+DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P)
+{
+    DenseLayout L;
+    int64_t path = g_opt_path.load();
+    if (path == 0)
+        path = (M <= DECODE_MAX_M) ? 2 : 1;
+    if (path == 2 && M > DECODE_MAX_M)
+        path = 1;
+    L.path = static_cast<int>(path);
+    L.off_h = SYNC_BYTES;
+    if (L.path == 2) {
+        const decode::Plan pl = decode::make_plan(M, N, O, P, 1);
+        L.off_part = align_up(L.off_h + static_cast<size_t>(M) * O * 2, 256);
+        L.total = L.off_part + pl.partial_bytes;
+        return L;
+    }
+    L.m_blocks = (M + engine::BM - 1) / engine::BM;
+    L.n1 = static_cast<int32_t>((O + engine::BN - 1) / engine::BN);
+    L.n2 = static_cast<int32_t>((P + engine::BN - 1) / engine::BN);
+    if (L.path == 1 && static_cast<size_t>(L.m_blocks) * L.n1 * 4 > FLAG_WORDS)
+        L.path = 3;   // more layer-1 tiles than flags: run the layers as two launches
+    L.total = align_up(L.off_h + static_cast<size_t>(L.m_blocks) * engine::BM * O * 2, 256);
+    return L;
+}
+
+struct MoeLayout {
+    int64_t R = 0, Rmax = 0, mbmax = 0;
+    int32_t n1 = 0, n2 = 0;
+    size_t off_idx, off_w, off_pos, off_src, off_band, off_nb, off_xp, off_h, off_yp, total;
+};
+
+MoeLayout moe_layout(int64_t T, int64_t N, int64_t O, int64_t P, int E, int k)
+{
+    MoeLayout L;
+    L.R = T * k;
+    L.Rmax = static_cast<int64_t>(align_up(static_cast<size_t>(L.R + static_cast<int64_t>(E) * (engine::BM - 1)),
+                                           engine::BM));
+    L.mbmax = L.Rmax / engine::BM;
+    L.n1 = static_cast<int32_t>((O + engine::BN - 1) / engine::BN);
+    L.n2 = static_cast<int32_t>((P + engine::BN - 1) / engine::BN);
+    size_t o = SYNC_BYTES;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.off_idx = take(static_cast<size_t>(L.R) * 4);
+    L.off_w = take(static_cast<size_t>(L.R) * 4);
+    L.off_pos = take(static_cast<size_t>(L.R) * 4);
+    L.off_src = take(static_cast<size_t>(L.Rmax) * 4);
+    L.off_band = take(static_cast<size_t>(L.mbmax) * 4);
+    L.off_nb = take(4);
+    L.off_xp = take(static_cast<size_t>(L.Rmax) * N * 2);
+    L.off_h = take(static_cast<size_t>(L.Rmax) * O * 2);
+    L.off_yp = take(static_cast<size_t>(L.Rmax) * P * 4);
+    L.total = o;
+    return L;
+}
+
+template <int MAX_E>
+void fill_layer(engine::LayerArgs& la, int64_t K, int64_t ncols, int act, int out_f32, int64_t rows, void* out)
+{
+    la.K = static_cast<int32_t>(K);
+    la.ncols = static_cast<int32_t>(ncols);
+    la.n_tiles = static_cast<int32_t>((ncols + engine::BN - 1) / engine::BN);
+    la.act = act;
+    la.out_f32 = out_f32;
+    la.pad_ = 0;
+    la.ld_out = ncols;
+    la.rows = rows;
+    la.out = out;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+
+extern "C" {
+
+int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, const void* b2, int act1,
+                int act2, int64_t M, int64_t N, int64_t O, int64_t P, void* Y, struct CUstream_st* stream)
+{
+    g_last_launches = 0;
+    if (!X || !W1 || !W2 || !Y)
+        return TFFN_ERR_INVALID_ARG;
+    if (M < 0 || M >= (int64_t(1) << 31) || !dim_ok(N) || !dim_ok(O) || !dim_ok(P))
+        return TFFN_ERR_INVALID_ARG;
+    if (!act_ok(act1) || !act_ok(act2))
+        return TFFN_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W2) || !aligned16(Y) || (b1 && !aligned16(b1)) ||
+        (b2 && !aligned16(b2)))
+        return TFFN_ERR_INVALID_ARG;
+    if (M == 0)
+        return TFFN_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != TFFN_OK)
+        return rc;
+    const DenseLayout L = dense_layout(M, N, O, P);
+    uint8_t* base = nullptr;
+    rc = workspace(*d, L.total, s, &base);
+    if (rc != TFFN_OK)
+        return rc;
+    DevCtrl* ctrl = reinterpret_cast<DevCtrl*>(base);
+    uint32_t* flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+
+    if (L.path == 2) {
+        uint32_t epoch = 0;
+        if ((rc = next_epoch(*d, base, s, &epoch)) != TFFN_OK)
+            return rc;
+        decode::Params p{};
+        p.X = static_cast<const __nv_bfloat16*>(X);
+        p.W1 = static_cast<const __nv_bfloat16*>(W1);
+        p.b1 = static_cast<const __nv_bfloat16*>(b1);
+        p.W2 = static_cast<const __nv_bfloat16*>(W2);
+        p.b2 = static_cast<const __nv_bfloat16*>(b2);
+        p.Y = static_cast<__nv_bfloat16*>(Y);
+        p.H = reinterpret_cast<__nv_bfloat16*>(base + L.off_h);
+        p.partial = reinterpret_cast<float*>(base + L.off_part);
+        p.counters = reinterpret_cast<uint32_t*>(base + OFF_DCOUNT);
+        p.flags = flags;
+        p.ctrl = ctrl;
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.O = static_cast<int32_t>(O);
+        p.P = static_cast<int32_t>(P);
+        p.act1 = act1;
+        p.act2 = act2;
+        p.epoch = epoch;
+        p.wait_limit_ns = wait_limit_ns();
+        p.plan = decode::make_plan(M, N, O, P, d->sms);
+        if (static_cast<size_t>(p.plan.slices[0]) * 4 > FLAG_WORDS ||
+            (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * 4 > DCOUNT_WORDS)
+            return TFFN_ERR_UNSUPPORTED;
+        const uint32_t arows = M <= 16 ? 16u : 32u;
+        if (make_map(&p.map_w[0], W1, O, N, 64, decode::KC) || make_map(&p.map_w[1], W2, P, O, 64, decode::KC) ||
+            make_map(&p.map_a[0], X, N, M, 64, arows) || make_map(&p.map_a[1], p.H, O, M, 64, arows))
+            return TFFN_ERR_INVALID_ARG;
+        timing_start(s);
+        if (launch_decode(p, p.plan.grid, s) != 0)
+            return TFFN_ERR_CUDA;
+        timing_stop(s);
+        g_last_launches = 1;
+        return TFFN_OK;
+    }
+
+    engine::Params<1> p;
+    std::memset(&p, 0, sizeof(p));
+    void* H = base + L.off_h;
+    const int64_t rows_h = L.m_blocks * engine::BM;
+    if (make_map(&p.map_a[0], X, N, M, 64, engine::BM) || make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM) ||
+        make_map(&p.map_b[0][0], W1, O, N, 64, engine::BK) || make_map(&p.map_b[1][0], W2, P, O, 64, engine::BK))
+        return TFFN_ERR_INVALID_ARG;
+    p.bias[0][0] = static_cast<const __nv_bfloat16*>(b1);
+    p.bias[1][0] = static_cast<const __nv_bfloat16*>(b2);
+    fill_layer<1>(p.layer[0], N, O, act1, 0, rows_h, H);
+    fill_layer<1>(p.layer[1], O, P, act2, 0, M, Y);
+    p.m_blocks = L.m_blocks;
+    p.m_blocks_dev = nullptr;
+    p.band_expert = nullptr;
+    p.flags = flags;
+    p.ctrl = ctrl;
+    p.wait_limit_ns = wait_limit_ns();
+    p.group_m = static_cast<int32_t>(g_opt_group.load() < 1 ? 1 : g_opt_group.load());
+    p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
+
+    if (L.path == 1) {
+        uint32_t epoch = 0;
+        if ((rc = next_epoch(*d, base, s, &epoch)) != TFFN_OK)
+            return rc;
+        p.epoch = epoch;
+        p.mode = MODE_FUSED;
+        const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, MODE_FUSED);
+        const int grid = static_cast<int>(total < d->sms ? total : d->sms);
+        timing_start(s);
+        if (launch_engine_dense(p, grid, s) != 0)
+            return TFFN_ERR_CUDA;
+        timing_stop(s);
+        g_last_launches = 1;
+        return TFFN_OK;
+    }
+    // two launches: layer 1, then layer 2
+    for (int mode = MODE_LAYER1; mode <= MODE_LAYER2; ++mode) {
+        p.mode = mode;
+        p.epoch = 0;
+        const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, mode);
+        const int grid = static_cast<int>(total < d->sms ? total : d->sms);
+        if (mode == MODE_LAYER1)
+            timing_start(s);
+        if (launch_engine_dense(p, grid, s) != 0)
+            return TFFN_ERR_CUDA;
+        ++g_last_launches;
+    }
+    timing_stop(s);
+    return TFFN_OK;
+}
+
+int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const void* const* W1,
+                    const void* const* b1, const void* const* W2, const void* const* b2, void* Y, int64_t T,
+                    int64_t N, int64_t O, int64_t P, int E, int act1, int act2, tffn_routing* routing,
+                    struct CUstream_st* stream)
+{
+    g_last_launches = 0;
+    if (!X || !gate_logits || !W1 || !W2 || !Y)
+        return TFFN_ERR_INVALID_ARG;
+    if (E < 1 || E > MOE_MAX_E || top_k < 1 || top_k > E)
+        return TFFN_ERR_INVALID_ARG;
+    if (T < 0 || T * top_k >= (int64_t(1) << 30) || !dim_ok(N) || !dim_ok(O) || !dim_ok(P))
+        return TFFN_ERR_INVALID_ARG;
+    if (!act_ok(act1) || !act_ok(act2))
+        return TFFN_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(gate_logits) & 3u))
+        return TFFN_ERR_INVALID_ARG;
+    for (int e = 0; e < E; ++e) {
+        if (!W1[e] || !W2[e] || !aligned16(W1[e]) || !aligned16(W2[e]))
+            return TFFN_ERR_INVALID_ARG;
+        if (b1 && b1[e] && !aligned16(b1[e]))
+            return TFFN_ERR_INVALID_ARG;
+        if (b2 && b2[e] && !aligned16(b2[e]))
+            return TFFN_ERR_INVALID_ARG;
+    }
+    if (T == 0)
+        return TFFN_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != TFFN_OK)
+        return rc;
+    const MoeLayout L = moe_layout(T, N, O, P, E, top_k);
+    if (static_cast<size_t>(L.mbmax) * L.n1 * 4 > FLAG_WORDS)
+        return TFFN_ERR_UNSUPPORTED;
+    uint8_t* base = nullptr;
+    rc = workspace(*d, L.total, s, &base);
+    if (rc != TFFN_OK)
+        return rc;
+    uint32_t epoch = 0;
+    if ((rc = next_epoch(*d, base, s, &epoch)) != TFFN_OK)
+        return rc;
+
+    int32_t* idx = reinterpret_cast<int32_t*>(base + L.off_idx);
+    float* w = reinterpret_cast<float*>(base + L.off_w);
+    int32_t* pos = reinterpret_cast<int32_t*>(base + L.off_pos);
+    int32_t* src = reinterpret_cast<int32_t*>(base + L.off_src);
+    int32_t* band = reinterpret_cast<int32_t*>(base + L.off_band);
+    int32_t* nb = reinterpret_cast<int32_t*>(base + L.off_nb);
+    void* Xp = base + L.off_xp;
+    void* H = base + L.off_h;
+    float* Yp = reinterpret_cast<float*>(base + L.off_yp);
+
+    engine::Params<MOE_MAX_E>* pp = new engine::Params<MOE_MAX_E>;
+    std::memset(pp, 0, sizeof(*pp));
+    engine::Params<MOE_MAX_E>& p = *pp;
+    int bad = make_map(&p.map_a[0], Xp, N, L.Rmax, 64, engine::BM) |
+              make_map(&p.map_a[1], H, O, L.Rmax, 64, engine::BM);
+    for (int e = 0; e < E && !bad; ++e) {
+        bad |= make_map(&p.map_b[0][e], W1[e], O, N, 64, engine::BK);
+        bad |= make_map(&p.map_b[1][e], W2[e], P, O, 64, engine::BK);
+        p.bias[0][e] = b1 ? static_cast<const __nv_bfloat16*>(b1[e]) : nullptr;
+        p.bias[1][e] = b2 ? static_cast<const __nv_bfloat16*>(b2[e]) : nullptr;
+    }
+    if (bad) {
+        delete pp;
+        return TFFN_ERR_INVALID_ARG;
+    }
+    fill_layer<MOE_MAX_E>(p.layer[0], N, O, act1, 0, L.Rmax, H);
+    fill_layer<MOE_MAX_E>(p.layer[1], O, P, act2, 1, L.Rmax, Yp);
+    p.m_blocks = -1;
+    p.m_blocks_dev = nb;
+    p.band_expert = band;
+    p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+    p.ctrl = reinterpret_cast<DevCtrl*>(base);
+    p.wait_limit_ns = wait_limit_ns();
+    p.epoch = epoch;
+    p.mode = MODE_FUSED;
+    p.group_m = static_cast<int32_t>(g_opt_group.load() < 1 ? 1 : g_opt_group.load());
+    p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
+
+    int fail = 0;
+    fail |= launch_moe_route(gate_logits, T, E, top_k, idx, w, s);
+    fail |= launch_moe_plan(idx, T, E, top_k, engine::BM, pos, src, band, nb, routing ? routing->perm : nullptr,
+                            routing ? routing->expert_offsets : nullptr, s);
+    fail |= launch_moe_gather(X, src, nb, engine::BM, N, Xp, d->sms * 4, s);
+    if (!fail) {
+        timing_start(s);
+        fail |= launch_engine_grouped(p, d->sms, s);
+        timing_stop(s);
+    }
+    fail |= launch_moe_combine(Yp, pos, w, T, top_k, P, Y, d->sms * 4, s);
+    delete pp;
+    if (fail)
+        return TFFN_ERR_CUDA;
+    g_last_launches = 5;
+    if (routing && routing->topk_idx &&
+        cudaMemcpyAsync(routing->topk_idx, idx, static_cast<size_t>(L.R) * 4, cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+        return TFFN_ERR_CUDA;
+    if (routing && routing->topk_w &&
+        cudaMemcpyAsync(routing->topk_w, w, static_cast<size_t>(L.R) * 4, cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+        return TFFN_ERR_CUDA;
+    return TFFN_OK;
+}
+
+size_t tffn_workspace_bytes(int64_t M, int64_t N, int64_t O, int64_t P, int E, int top_k)
+{
+    if (M < 0 || !dim_ok(N) || !dim_ok(O) || !dim_ok(P))
+        return 0;
+    if (E <= 0)
+        return dense_layout(M, N, O, P).total;
+    if (top_k < 1 || top_k > E)
+        return 0;
+    return moe_layout(M, N, O, P, E, top_k).total;
+}
+
+int tffn_set_workspace(void* dev_ptr, size_t bytes)
+{
+    if (dev_ptr && ((reinterpret_cast<uintptr_t>(dev_ptr) & 255u) || bytes < SYNC_BYTES))
+        return TFFN_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return TFFN_ERR_CUDA;
+    DeviceState& d = g_dev[dev];
+    d.user = dev_ptr;
+    d.user_bytes = dev_ptr ? bytes : 0;
+    d.user_set = dev_ptr != nullptr;
+    d.needs_reset = true;
+    return TFFN_OK;
+}
+
+int tffn_check(struct CUstream_st* stream, int32_t* detail)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TFFN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return TFFN_ERR_CUDA;
+    DeviceState& d = g_dev[dev];
+    void* base = d.user_set ? d.user : d.owned;
+    if (detail)
+        detail[0] = detail[1] = detail[2] = detail[3] = 0;
+    if (!base)
+        return TFFN_OK;
+    uint32_t rec[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(rec, base, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TFFN_ERR_CUDA;
+    if (detail)
+        for (int i = 0; i < 4; ++i)
+            detail[i] = static_cast<int32_t>(rec[i]);
+    if (rec[0] == 0)
+        return TFFN_OK;
+    // The failed launch may have left flags and counters inconsistent: the
+    // whole sync region is re-zeroed before the next call.
+    if (cudaMemset(base, 0, sizeof(rec)) != cudaSuccess)
+        return TFFN_ERR_CUDA;
+    d.needs_reset = true;
+    const int32_t code = static_cast<int32_t>(rec[0]);
+    return (code == TFFN_ERR_TIMEOUT) ? TFFN_ERR_TIMEOUT : TFFN_ERR_DEVICE;
+}
+
+const char* tffn_status_string(int status)
+{
+    switch (status) {
+    case TFFN_OK: return "ok";
+    case TFFN_ERR_INVALID_ARG: return "invalid argument";
+    case TFFN_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case TFFN_ERR_CUDA: return "CUDA runtime error";
+    case TFFN_ERR_TIMEOUT: return "device wait timed out";
+    case TFFN_ERR_NO_WORKSPACE: return "workspace too small";
+    case TFFN_ERR_DEVICE: return "device-side error";
+    default: return "unknown status";
+    }
+}
+
+int64_t tffn_set_option(int option, int64_t value)
+{
+    switch (option) {
+    case TFFN_OPT_PATH: return g_opt_path.exchange(value);
+    case TFFN_OPT_WAIT_LIMIT_MS: return g_opt_wait_ms.exchange(value);
+    case TFFN_OPT_SKIP_FLAG: return g_opt_skip.exchange(value);
+    case TFFN_OPT_GROUP_M: return g_opt_group.exchange(value);
+    default: return -1;
+    }
+}
+
+int tffn_last_launch_count(void) { return g_last_launches; }
+
+int tffn_timing_begin(void)
+{
+    g_timing = true;
+    g_events_used = 0;
+    return TFFN_OK;
+}
+
+int tffn_timing_end(int* launches, double* total_ms)
+{
+    double sum = 0.0;
+    for (size_t i = 0; i < g_events_used; ++i) {
+        if (cudaEventSynchronize(g_events[i].second) != cudaSuccess)
+            return TFFN_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, g_events[i].first, g_events[i].second) != cudaSuccess)
+            return TFFN_ERR_CUDA;
+        sum += ms;
+    }
+    if (launches)
+        *launches = static_cast<int>(g_events_used);
+    if (total_ms)
+        *total_ms = sum;
+    g_timing = false;
+    g_events_used = 0;
+    return TFFN_OK;
+}
+
+int64_t tffn_debug_engine_task(int64_t m_blocks, int32_t n1, int32_t n2, int32_t group_m, int64_t ticket,
+                               int32_t out[3])
+{
+    if (group_m < 1)
+        group_m = 1;
+    const int64_t total = engine_total_tickets(m_blocks, n1, n2, MODE_FUSED);
+    EngineTask t = engine_task(ticket, m_blocks, n1, n2, group_m, MODE_FUSED);
+    if (ticket >= total)
+        t.layer = -1;
+    if (out) {
+        out[0] = t.layer;
+        out[1] = t.band;
+        out[2] = t.tile;
+    }
+    return total;
+}
+
+void tffn_debug_tiles(int32_t out[6])
+{
+    out[0] = engine::BM;
+    out[1] = engine::BN;
+    out[2] = engine::BK;
+    out[3] = engine::STAGES;
+    out[4] = decode::SLICE;
+    out[5] = decode::KC;
+}
+
+}  // extern "C"

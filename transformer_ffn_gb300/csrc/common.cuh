@@ -1,0 +1,134 @@
+// common.cuh -- device-side control block, error reporting and bounded waits.
+//
+// Every wait in the library's kernels goes through wait_mbar / wait_flag: each
+// has a time limit (globaltimer, nanoseconds) after which the kernel records an
+// error in the workspace's control block, raises the CTA's abort flag and
+// returns, so the host can read the error from tffn_check() and the context
+// stays usable.  Nothing traps.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "../../include/tffn.h"
+#include "ptx.cuh"
+
+namespace tffn {
+
+// Where a wait gave up (stored in DevCtrl::where).
+enum WaitSite : uint32_t {
+    SITE_SMEM_EMPTY = 1,     // producer waiting for a free shared-memory stage
+    SITE_SMEM_FULL = 2,      // MMA waiting for a loaded stage
+    SITE_TMEM_EMPTY = 3,     // MMA waiting for a drained accumulator
+    SITE_TMEM_FULL = 4,      // epilogue waiting for a finished accumulator
+    SITE_TASK_FULL = 5,      // consumer waiting for the next task
+    SITE_TASK_EMPTY = 6,     // producer waiting for a free task slot
+    SITE_H_FLAG = 7,         // layer-2 producer waiting for a hidden tile
+    SITE_DRAIN = 8,          // exit path waiting for its own copies / MMAs
+    SITE_SLICE_FLAG = 9,     // decode layer 2 waiting for a hidden slice
+    SITE_STAGE = 10,         // decode consumer waiting for a stage
+};
+
+// Control block at the start of the workspace (256 bytes).
+struct DevCtrl {
+    uint32_t status;      // 0 or a negative tffn_status, stored as uint32
+    uint32_t where;       // WaitSite of the first failure
+    uint32_t block;       // blockIdx.x of the first failure
+    uint32_t info;        // site-specific detail (tile / slice index)
+    uint32_t ticket;      // engine: next task ticket
+    uint32_t done;        // engine: CTAs that have exited
+    uint32_t dticket;     // decode: unused for now
+    uint32_t ddone;       // decode: CTAs that have exited
+    uint32_t pad[56];
+};
+static_assert(sizeof(DevCtrl) == 256, "control block is 256 bytes");
+
+struct WaitCtx {
+    volatile uint32_t* abort;   // CTA-wide abort flag in shared memory
+    DevCtrl* ctrl;
+    uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void raise_error(const WaitCtx& w, uint32_t code, uint32_t where,
+                                            uint32_t info)
+{
+    *w.abort = 1u;
+    if (atomicCAS(&w.ctrl->status, 0u, code) == 0u) {
+        w.ctrl->where = where;
+        w.ctrl->block = blockIdx.x;
+        w.ctrl->info = info;
+    }
+}
+
+// Wait for the phase of `bar` with this parity; false on abort or timeout.
+static __device__ __noinline__ bool wait_mbar(const WaitCtx& w, uint32_t bar, uint32_t parity,
+                                       uint32_t where)
+{
+    if (ptx::mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        if (*w.abort)
+            return false;
+        if (ptx::globaltimer() - t0 > w.limit_ns) {
+            raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), where, parity);
+            return false;
+        }
+    }
+}
+
+// Wait (acquire, gpu scope) until *flag == epoch; false on abort or timeout.
+static __device__ __noinline__ bool wait_flag(const WaitCtx& w, const uint32_t* flag, uint32_t epoch,
+                                       uint32_t where, uint32_t info)
+{
+    if (ptx::ld_acquire_gpu(flag) == epoch)
+        return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        __nanosleep(100);
+        if (ptx::ld_acquire_gpu(flag) == epoch)
+            return true;
+        if (*w.abort)
+            return false;
+        if (ptx::globaltimer() - t0 > w.limit_ns) {
+            raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), where, info);
+            return false;
+        }
+    }
+}
+
+// Activations (fp32).  GELU uses the tanh form written through the identity
+// 0.5 x (1 + tanh(u)) = x / (1 + exp(-2u)), which keeps full relative accuracy
+// for negative x where 1 + tanh(u) would cancel.
+__device__ __forceinline__ float act_apply(int act, float x)
+{
+    if (act == TFFN_ACT_RELU)
+        return fmaxf(x, 0.0f);
+    if (act == TFFN_ACT_GELU_TANH) {
+        const float k0 = 0.7978845608028654f;   // sqrt(2/pi)
+        const float k1 = 0.044715f;
+        const float u = k0 * fmaf(k1 * x, x * x, x);
+        return __fdividef(x, 1.0f + __expf(-2.0f * u));
+    }
+    return x;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v)
+{
+    return __uint_as_float(v << 16);
+}
+
+__device__ __forceinline__ float bf16_hi(uint32_t v)
+{
+    return __uint_as_float(v & 0xFFFF0000u);
+}
+
+}  // namespace tffn

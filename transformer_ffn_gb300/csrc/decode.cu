@@ -1,0 +1,351 @@
+// decode.cu -- the weight-streaming small-M FFN kernel (see decode.cuh).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "decode.cuh"
+#include "launch.h"
+
+namespace tffn {
+namespace decode {
+
+static_assert(SLICE == KC, "layer 2 reads exactly one layer-1 slice of H per unit");
+
+struct Aux {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint32_t abort;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled
+// box (rows of 128 bytes; chunk index XOR row mod 8).
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk)
+{
+    return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+template <int MT>
+struct Acc {
+    float c[MT][4][4];   // [m tile][n8 tile][fragment]
+};
+
+template <int MT>
+__device__ __forceinline__ void zero(Acc<MT>& a)
+{
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                a.c[m][n][i] = 0.0f;
+}
+
+// One KC x SLICE unit: this warp's 32 columns, all K rows of the stage.
+template <int MT>
+__device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uint32_t a_base, int cw, int lane)
+{
+    const uint32_t wbox = w_base + static_cast<uint32_t>(cw >> 1) * W_BOX_BYTES;
+    const uint32_t cb_chunk = static_cast<uint32_t>(cw & 1) * 4;   // 32 columns = 4 chunks
+    const uint32_t j = static_cast<uint32_t>(lane >> 3);
+    const uint32_t r = static_cast<uint32_t>(lane & 7);
+#pragma unroll
+    for (int ks = 0; ks < KC / 16; ++ks) {
+        uint32_t a[MT][4];
+        const uint32_t abox = a_base + static_cast<uint32_t>(ks >> 2) * A_BOX_BYTES;
+        const uint32_t kchunk = static_cast<uint32_t>((ks & 3) * 2) + (j >> 1);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const uint32_t row = static_cast<uint32_t>(m * 16) + (j & 1u) * 8u + r;
+            ldsm_x4(abox + sw128(row, kchunk), a[m][0], a[m][1], a[m][2], a[m][3]);
+        }
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+            const uint32_t krow = static_cast<uint32_t>(ks * 16) + (j & 1u) * 8u + r;
+            const uint32_t nchunk = cb_chunk + static_cast<uint32_t>(pr * 2) + (j >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(wbox + sw128(krow, nchunk), b0, b1, b2, b3);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                mma_bf16_16816(acc.c[m][pr * 2 + 0], a[m][0], a[m][1], a[m][2], a[m][3], b0, b1);
+                mma_bf16_16816(acc.c[m][pr * 2 + 1], a[m][0], a[m][1], a[m][2], a[m][3], b2, b3);
+            }
+        }
+    }
+}
+
+// Finish this warp's 32 columns of one slice: direct epilogue when one CTA
+// owns the whole K range, else store the partial and let the last arriver sum
+// the parts in part order.
+template <int MT>
+__device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, int cw, int lane)
+{
+    const Plan& pl = p.plan;
+    const int64_t U = pl.units[layer], G = pl.grid, kch = pl.kch[layer];
+    const int64_t first = owner_of(slice * kch, U, G);
+    const int64_t last = owner_of((slice + 1) * kch - 1, U, G);
+    const int nparts = static_cast<int>(last - first + 1);
+    const int part = static_cast<int>(blockIdx.x - first);
+    const int g = lane >> 2, q = lane & 3;
+    const int M = p.M;
+
+    if (nparts > 1) {
+        float* base = p.partial + pl.part_off[layer] +
+                      (static_cast<int64_t>(slice) * pl.maxp[layer]) * MAX_ROWS * SLICE;
+        float* mine = base + static_cast<int64_t>(part) * MAX_ROWS * SLICE;
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const int col = cw * 32 + n * 8 + 2 * q;
+                const int r0 = m * 16 + g, r1 = r0 + 8;
+                if (r0 < M)
+                    *reinterpret_cast<float2*>(mine + r0 * SLICE + col) = make_float2(acc.c[m][n][0], acc.c[m][n][1]);
+                if (r1 < M)
+                    *reinterpret_cast<float2*>(mine + r1 * SLICE + col) = make_float2(acc.c[m][n][2], acc.c[m][n][3]);
+            }
+        __threadfence();
+        __syncwarp();
+        uint32_t* cnt = p.counters + (layer == 0 ? 0 : pl.slices[0] * 4) + slice * 4 + cw;
+        uint32_t old = 0;
+        if (lane == 0)
+            old = atomicAdd(cnt, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old != static_cast<uint32_t>(nparts - 1))
+            return;
+        __threadfence();
+        zero(acc);
+        for (int pp = 0; pp < nparts; ++pp) {
+            const float* src = base + static_cast<int64_t>(pp) * MAX_ROWS * SLICE;
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    const int col = cw * 32 + n * 8 + 2 * q;
+                    const int r0 = m * 16 + g, r1 = r0 + 8;
+                    if (r0 < M) {
+                        const float2 v = __ldcg(reinterpret_cast<const float2*>(src + r0 * SLICE + col));
+                        acc.c[m][n][0] += v.x;
+                        acc.c[m][n][1] += v.y;
+                    }
+                    if (r1 < M) {
+                        const float2 v = __ldcg(reinterpret_cast<const float2*>(src + r1 * SLICE + col));
+                        acc.c[m][n][2] += v.x;
+                        acc.c[m][n][3] += v.y;
+                    }
+                }
+        }
+        if (lane == 0)
+            *cnt = 0u;   // every part has arrived: ready for the next call
+    }
+
+    // Epilogue: bias, activation, bf16.
+    const __nv_bfloat16* bias = layer == 0 ? p.b1 : p.b2;
+    const int act = layer == 0 ? p.act1 : p.act2;
+    const int ncols = layer == 0 ? p.O : p.P;
+    __nv_bfloat16* out = layer == 0 ? p.H : p.Y;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+        const int col = static_cast<int>(slice) * SLICE + cw * 32 + n * 8 + 2 * q;
+        if (col >= ncols)
+            continue;
+        float b0 = 0.f, b1 = 0.f;
+        if (bias) {
+            const uint32_t bb = *reinterpret_cast<const uint32_t*>(bias + col);
+            b0 = bf16_lo(bb);
+            b1 = bf16_hi(bb);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const int r0 = m * 16 + g, r1 = r0 + 8;
+            if (r0 < M)
+                *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(r0) * ncols + col) =
+                    pack_bf16x2(act_apply(act, acc.c[m][n][0] + b0), act_apply(act, acc.c[m][n][1] + b1));
+            if (r1 < M)
+                *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(r1) * ncols + col) =
+                    pack_bf16x2(act_apply(act, acc.c[m][n][2] + b0), act_apply(act, acc.c[m][n][3] + b1));
+        }
+    }
+    if (layer == 0) {
+        // Publish this warp's quarter of the H slice: stamp its flag word with
+        // the call's epoch (release, gpu scope).
+        ptx::fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();
+            ptx::st_release_gpu(p.flags + slice * CONSUMER_WARPS + cw, p.epoch);
+        }
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_constant__ Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* stages = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Aux& aux = *reinterpret_cast<Aux*>(stages + STAGES * STAGE_BYTES);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    constexpr uint32_t A_BYTES = 2u * (16u * MT) * 64u * 2u;
+    const Plan& pl = p.plan;
+    const int64_t G = pl.grid;
+    const int64_t c = blockIdx.x;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&aux.full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&aux.empty[s]), CONSUMER_WARPS);
+        }
+        aux.abort = 0u;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    const WaitCtx w{&aux.abort, p.ctrl, p.wait_limit_ns};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t evict_first = ptx::policy_evict_first();
+            uint32_t stage = 0, phase = 0;
+            int32_t last_phase[STAGES];
+            for (int s = 0; s < STAGES; ++s)
+                last_phase[s] = -1;
+            bool ok = true;
+            for (int layer = 0; layer < 2 && ok; ++layer) {
+                const int64_t U = pl.units[layer], kch = pl.kch[layer];
+                const int64_t u0 = range_start(c, U, G), u1 = range_start(c + 1, U, G);
+                const CUtensorMap* mw = &p.map_w[layer];
+                const CUtensorMap* ma = &p.map_a[layer];
+                int64_t last_h = -1;
+                for (int64_t u = u0; u < u1; ++u) {
+                    const int64_t slice = u / kch, kc = u % kch;
+                    ok = wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY);
+                    if (!ok)
+                        break;
+                    const uint32_t fb = ptx::smem_u32(&aux.full[stage]);
+                    const uint32_t sw = ptx::smem_u32(stages + stage * STAGE_BYTES);
+                    const uint32_t sa = sw + W_STAGE_BYTES;
+                    ptx::mbar_arrive_expect_tx(fb, W_STAGE_BYTES + A_BYTES);
+                    ptx::tma_load_2d_hint(sw, mw, fb, static_cast<int32_t>(slice * SLICE),
+                                          static_cast<int32_t>(kc * KC), evict_first);
+                    ptx::tma_load_2d_hint(sw + W_BOX_BYTES, mw, fb, static_cast<int32_t>(slice * SLICE + 64),
+                                          static_cast<int32_t>(kc * KC), evict_first);
+                    if (layer == 1 && kc != last_h) {
+                        for (int q = 0; q < CONSUMER_WARPS && ok; ++q)
+                            ok = wait_flag(w, p.flags + kc * CONSUMER_WARPS + q, p.epoch, SITE_SLICE_FLAG,
+                                           static_cast<uint32_t>(kc));
+                        if (!ok) {
+                            // the W copies above are in flight: still drain them
+                            ptx::tma_load_2d(sa, ma, fb, static_cast<int32_t>(kc * KC), 0);
+                            ptx::tma_load_2d(sa + A_BOX_BYTES, ma, fb, static_cast<int32_t>(kc * KC + 64), 0);
+                            last_phase[stage] = static_cast<int32_t>(phase);
+                            break;
+                        }
+                        ptx::fence_proxy_async_global();
+                        last_h = kc;
+                    }
+                    ptx::tma_load_2d(sa, ma, fb, static_cast<int32_t>(kc * KC), 0);
+                    ptx::tma_load_2d(sa + A_BOX_BYTES, ma, fb, static_cast<int32_t>(kc * KC + 64), 0);
+                    last_phase[stage] = static_cast<int32_t>(phase);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Exit: every copy issued by this thread has landed before the CTA leaves.
+            for (int s = 0; s < STAGES; ++s) {
+                if (last_phase[s] < 0)
+                    continue;
+                const uint64_t t0 = ptx::globaltimer();
+                while (!ptx::mbar_try_wait(ptx::smem_u32(&aux.full[s]), static_cast<uint32_t>(last_phase[s]))) {
+                    if (ptx::globaltimer() - t0 > p.wait_limit_ns) {
+                        raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), SITE_DRAIN, s);
+                        break;
+                    }
+                }
+            }
+        }
+    } else {
+        const int cw = warp - 1;
+        uint32_t stage = 0, phase = 0;
+        Acc<MT> acc;
+        bool ok = true;
+        for (int layer = 0; layer < 2 && ok; ++layer) {
+            const int64_t U = pl.units[layer], kch = pl.kch[layer];
+            const int64_t u0 = range_start(c, U, G), u1 = range_start(c + 1, U, G);
+            int64_t cur = -1;
+            for (int64_t u = u0; u < u1; ++u) {
+                const int64_t slice = u / kch;
+                if (slice != cur) {
+                    if (cur >= 0)
+                        flush<MT>(p, layer, cur, acc, cw, lane);
+                    zero(acc);
+                    cur = slice;
+                }
+                ok = wait_mbar(w, ptx::smem_u32(&aux.full[stage]), phase, SITE_STAGE);
+                if (!ok)
+                    break;
+                const uint32_t sw = ptx::smem_u32(stages + stage * STAGE_BYTES);
+                compute_stage<MT>(acc, sw, sw + W_STAGE_BYTES, cw, lane);
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(ptx::smem_u32(&aux.empty[stage]));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (ok && cur >= 0)
+                flush<MT>(p, layer, cur, acc, cw, lane);
+        }
+    }
+    __syncwarp();
+    __syncthreads();
+}
+
+}  // namespace decode
+
+int launch_decode(const decode::Params& p, int grid, cudaStream_t s)
+{
+    (void)grid;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(decode::decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 decode::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(decode::decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 decode::SMEM_BYTES) != cudaSuccess)
+            return -1;
+        attr_set = true;
+    }
+    if (p.M <= 16)
+        decode::decode_kernel<1><<<p.plan.grid, decode::NUM_THREADS, decode::SMEM_BYTES, s>>>(p);
+    else
+        decode::decode_kernel<2><<<p.plan.grid, decode::NUM_THREADS, decode::SMEM_BYTES, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace tffn

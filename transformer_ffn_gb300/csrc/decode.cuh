@@ -1,0 +1,127 @@
+// decode.cuh -- the small-M (decode) path: both layers of the FFN as one
+// persistent launch that streams the weights from HBM exactly once.
+//
+// At M <= 32 rows the FFN is bound by reading W1 and W2 ("kernel fusion"
+// page, section "Complexity and constants": a memory-bound kernel takes the
+// bytes it moves divided by the achievable HBM bandwidth, and needs 16-byte
+// accesses to get there).  Work is cut into units of SLICE output columns x KC
+// rows of K; CTA c of G owns the contiguous unit range [c*U/G, (c+1)*U/G) of
+// each layer (Stream-K style: every CTA gets the same amount of weight bytes).
+// A slice whose K range is split across CTAs is finished by the last CTA to
+// arrive on the slice's counter, which sums the parts in part order, so the
+// result does not depend on arrival order ("Kernel fusion and tensor
+// parallelism", section "Step 1": a per-tile counter, the last contributor
+// marks the tile ready; the accumulation of partial tiles with completion
+// flags that Stream-K uses).  A finished layer-1 slice of H publishes a ready
+// flag; layer-2 units wait on the flag of the H slice they read.
+//
+// Layout per CTA: warp 0 issues TMA copies (W tile [KC x SLICE] as two
+// 128-byte-swizzled boxes, plus the [rows x KC] tile of X or H); warps 1..4
+// each own 32 of the SLICE columns and run mma.sync m16n8k16 (bf16, fp32
+// accumulation) on fragments read with ldmatrix from the swizzled tiles.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace tffn {
+namespace decode {
+
+constexpr int SLICE = 128;              // output columns per unit
+constexpr int KC = 128;                 // K rows per unit
+constexpr int MAX_ROWS = 32;            // rows handled by this path
+constexpr int STAGES = 5;
+constexpr int CONSUMER_WARPS = 4;       // 32 columns each
+constexpr int NUM_THREADS = 32 * (1 + CONSUMER_WARPS);
+constexpr int W_BOX_BYTES = KC * 64 * 2;                 // 16 KiB: KC rows x 64 cols
+constexpr int W_STAGE_BYTES = 2 * W_BOX_BYTES;           // 32 KiB
+constexpr int A_BOX_BYTES = MAX_ROWS * 64 * 2;           // 4 KiB: 32 rows x 64 k
+constexpr int A_STAGE_BYTES = 2 * A_BOX_BYTES;           // 8 KiB
+constexpr int STAGE_BYTES = W_STAGE_BYTES + A_STAGE_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+
+struct Plan {
+    int32_t grid;
+    int32_t slices[2];      // output slices per layer
+    int32_t kch[2];         // K chunks per slice
+    int64_t units[2];       // slices * kch
+    int32_t maxp[2];        // most CTAs sharing one slice
+    int64_t part_off[2];    // float offset of each layer's partial area
+    size_t partial_bytes;
+};
+
+// CTA that owns unit u when U units are spread over G CTAs (U >= G).
+__host__ __device__ inline int64_t owner_of(int64_t u, int64_t U, int64_t G)
+{
+    return ((u + 1) * G + U - 1) / U - 1;
+}
+
+__host__ __device__ inline int64_t range_start(int64_t c, int64_t U, int64_t G)
+{
+    return c * U / G;
+}
+
+// grid is the CTA count the caller wants; it is lowered so that every CTA
+// owns at least one unit of each layer.
+inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid)
+{
+    (void)M;
+    Plan pl{};
+    pl.slices[0] = static_cast<int32_t>((O + SLICE - 1) / SLICE);
+    pl.kch[0] = static_cast<int32_t>((N + KC - 1) / KC);
+    pl.slices[1] = static_cast<int32_t>((P + SLICE - 1) / SLICE);
+    pl.kch[1] = static_cast<int32_t>((O + KC - 1) / KC);
+    int64_t g = grid;
+    for (int l = 0; l < 2; ++l) {
+        pl.units[l] = static_cast<int64_t>(pl.slices[l]) * pl.kch[l];
+        if (pl.units[l] < g)
+            g = pl.units[l];
+    }
+    if (g < 1)
+        g = 1;
+    pl.grid = static_cast<int32_t>(g);
+    size_t off = 0;
+    for (int l = 0; l < 2; ++l) {
+        int32_t maxp = 1;
+        for (int64_t s = 0; s < pl.slices[l]; ++s) {
+            const int64_t a = owner_of(s * pl.kch[l], pl.units[l], g);
+            const int64_t b = owner_of((s + 1) * pl.kch[l] - 1, pl.units[l], g);
+            if (b - a + 1 > maxp)
+                maxp = static_cast<int32_t>(b - a + 1);
+        }
+        pl.maxp[l] = maxp;
+        pl.part_off[l] = static_cast<int64_t>(off / 4);
+        off += static_cast<size_t>(pl.slices[l]) * maxp * MAX_ROWS * SLICE * 4;
+    }
+    pl.partial_bytes = off;
+    return pl;
+}
+
+struct Params {
+    CUtensorMap map_w[2];      // W1 {O, N}, W2 {P, O}; box {64, KC}
+    CUtensorMap map_a[2];      // X {N, M}, H {O, M}; box {64, 16 * m_tiles}
+    const __nv_bfloat16* X;
+    const __nv_bfloat16* W1;
+    const __nv_bfloat16* b1;
+    const __nv_bfloat16* W2;
+    const __nv_bfloat16* b2;
+    __nv_bfloat16* Y;
+    __nv_bfloat16* H;          // [M x O]
+    float* partial;
+    uint32_t* counters;        // [slices0 * 4] then [slices1 * 4]
+    uint32_t* flags;           // [slices0 * 4]: one word per consumer warp, = epoch when ready
+    DevCtrl* ctrl;
+    int32_t M, N, O, P;
+    int32_t act1, act2;
+    uint32_t epoch;
+    uint64_t wait_limit_ns;
+    Plan plan;
+};
+
+}  // namespace decode
+}  // namespace tffn

@@ -1,0 +1,455 @@
+// engine.cuh -- the persistent, warp-specialised tcgen05 engine that runs the
+// two GEMMs of the FFN (and of every expert of the MoE form) in one launch.
+//
+// What it computes ("Kernel fusion and tensor parallelism", section
+// "Megatron-LM tensor parallelism", FFN equation; section "Step 1"):
+//   layer 1 tile (band i, tile j):  H[i, j] = bf16(act1(X[i, :] W1[:, j] + b1[j]))
+//   layer 2 tile (band i, tile k):  Y[i, k] = act2(H[i, :] W2[:, k] + b2[k])
+// with fp32 accumulation in tensor memory.  A layer-1 tile publishes a ready
+// flag once its H tile is in global memory; a layer-2 tile of the same band
+// waits on those flags chunk by chunk before its TMA loads read H, so H is
+// consumed while the rest of H is still being produced (the page's per-tile
+// flag, used here between the SMs of one GPU).
+//
+// CTA layout (192 threads, one CTA per SM):
+//   warp 0      TMA producer: takes tickets, publishes tasks, streams A/B
+//               k-slices into a STAGES-deep shared-memory ring
+//   warp 1      owns the tensor memory (512 columns = two 128x256 fp32
+//               accumulators) and issues tcgen05.mma from one thread
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane quadrant
+//               per warp, one row per thread), add bias, activation, round,
+//               store; the accumulator is double-buffered so the epilogue of
+//               one tile overlaps the main loop of the next.
+//
+// Operands: A (X or H) is row-major [rows x K]: K-major, 128-byte swizzle,
+// boxes of 64 (K) x 128 (rows).  B (W1 or W2) is row-major [K x cols]: the
+// columns are contiguous, so B is MN-major: four boxes of 64 (cols) x 64 (K)
+// per stage, 128-byte swizzle.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "schedule.h"
+
+namespace tffn {
+namespace engine {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;              // 16 KiB
+constexpr int B_BOX_BYTES = 64 * BK * 2;                // 8 KiB: 64 cols x 64 k
+constexpr int B_STAGE_BYTES = BK * BN * 2;              // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TASK_SLOTS = 4;
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int AUX_BYTES = 1024;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + 1024;   // + alignment slack
+
+// Per-layer arguments.
+struct LayerArgs {
+    int32_t K;          // reduction length (N for layer 1, O for layer 2)
+    int32_t ncols;      // output columns (O, P)
+    int32_t n_tiles;    // ceil(ncols / BN)
+    int32_t act;        // tffn_act
+    int32_t out_f32;    // 1: fp32 output, 0: bf16
+    int32_t pad_;
+    int64_t ld_out;     // output row stride in elements
+    int64_t rows;       // rows of the output that are stored (later rows are skipped)
+    void* out;
+};
+
+template <int MAX_E>
+struct Params {
+    CUtensorMap map_a[2];                      // layer-1 A (X), layer-2 A (H)
+    CUtensorMap map_b[2][MAX_E];               // W1[e], W2[e]
+    const __nv_bfloat16* bias[2][MAX_E];       // b1[e], b2[e] (nullable)
+    LayerArgs layer[2];
+    int64_t m_blocks;                          // row bands; < 0: read *m_blocks_dev
+    const int32_t* m_blocks_dev;
+    const int32_t* band_expert;                // expert of each band (NULL: expert 0)
+    uint32_t* flags;                           // [m_blocks * n1 * 4] ready words
+    DevCtrl* ctrl;
+    uint64_t wait_limit_ns;
+    uint32_t epoch;                            // value of a ready flag word in this call
+    int32_t mode;                              // EngineMode
+    int32_t group_m;
+    int32_t skip_flag;                         // test fault injection, -1 = off
+};
+
+// Everything in shared memory besides the stage ring.
+struct Aux {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t task_full[TASK_SLOTS];
+    uint64_t task_empty[TASK_SLOTS];
+    uint64_t drain;
+    int4 task[TASK_SLOTS];
+    uint32_t tmem_base;
+    uint32_t abort;
+};
+static_assert(sizeof(Aux) <= AUX_BYTES, "aux block fits");
+
+// Bounded wait that ignores the abort flag: used on the exit path to wait for
+// this CTA's own copies and MMAs, which always complete.
+__device__ __forceinline__ void wait_own(const WaitCtx& w, uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer() - t0 > w.limit_ns) {
+            raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), SITE_DRAIN, parity);
+            return;
+        }
+    }
+}
+
+template <int MAX_E>
+__device__ __forceinline__ int expert_of(const Params<MAX_E>& p, int band)
+{
+    if (MAX_E == 1 || p.band_expert == nullptr)
+        return 0;
+    return p.band_expert[band];
+}
+
+// ----------------------------------------------------------------- producer
+template <int MAX_E>
+__device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const WaitCtx& w,
+                             int64_t m_blocks, int64_t total)
+{
+    const int32_t n1 = p.layer[0].n_tiles;
+    const int32_t n2 = p.layer[1].n_tiles;
+    uint32_t stage = 0, phase = 0, slot = 0, slot_phase = 0;
+    int32_t last_phase[STAGES];
+    for (int s = 0; s < STAGES; ++s)
+        last_phase[s] = -1;
+
+    for (;;) {
+        const uint32_t t = atomicAdd(&p.ctrl->ticket, 1u);
+        EngineTask task = engine_task(static_cast<int64_t>(t), m_blocks, n1, n2, p.group_m, p.mode);
+        if (static_cast<int64_t>(t) >= total)
+            task.layer = -1;
+        if (!wait_mbar(w, ptx::smem_u32(&aux.task_empty[slot]), slot_phase ^ 1u, SITE_TASK_EMPTY))
+            break;
+        aux.task[slot] = make_int4(task.layer, task.band, task.tile, 0);
+        ptx::mbar_arrive(ptx::smem_u32(&aux.task_full[slot]));
+        if (++slot == TASK_SLOTS) {
+            slot = 0;
+            slot_phase ^= 1u;
+        }
+        if (task.layer < 0)
+            break;
+
+        const int L = task.layer;
+        const LayerArgs& la = p.layer[L];
+        const int e = expert_of(p, task.band);
+        const CUtensorMap* ma = &p.map_a[L];
+        const CUtensorMap* mb = &p.map_b[L][e];
+        const int nk = (la.K + BK - 1) / BK;
+        const int32_t row0 = task.band * BM;
+        const int32_t col0 = task.tile * BN;
+        const bool wait_h = (L == 1 && p.mode == MODE_FUSED);
+        int last_h = -1;
+        bool ok = true;
+        for (int kb = 0; kb < nk && ok; ++kb) {
+            if (wait_h) {
+                const int j = (kb * BK) / BN;   // layer-1 tile holding this H chunk
+                if (j != last_h) {
+                    // the tile is ready once each of its four epilogue warps
+                    // has stamped its word with this call's epoch
+                    const uint32_t fi = static_cast<uint32_t>(task.band * n1 + j);
+                    for (int q = 0; q < EPI_WARPS && ok; ++q)
+                        ok = wait_flag(w, &p.flags[fi * EPI_WARPS + q], p.epoch, SITE_H_FLAG, fi);
+                    if (!ok)
+                        break;
+                    ptx::fence_proxy_async_global();
+                    last_h = j;
+                }
+            }
+            ok = wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY);
+            if (!ok)
+                break;
+            const uint32_t fb = ptx::smem_u32(&aux.full[stage]);
+            ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const uint32_t sa = ptx::smem_u32(stages + stage * STAGE_BYTES);
+            const uint32_t sb = sa + A_STAGE_BYTES;
+            ptx::tma_load_2d(sa, ma, fb, kb * BK, row0);
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+                ptx::tma_load_2d(sb + i * B_BOX_BYTES, mb, fb, col0 + i * 64, kb * BK);
+            last_phase[stage] = static_cast<int32_t>(phase);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok)
+            break;
+    }
+    // Exit: wait until every copy this thread issued has landed.
+    for (int s = 0; s < STAGES; ++s)
+        if (last_phase[s] >= 0)
+            wait_own(w, ptx::smem_u32(&aux.full[s]), static_cast<uint32_t>(last_phase[s]));
+}
+
+// ---------------------------------------------------------------------- MMA
+template <int MAX_E>
+__device__ void run_mma(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const WaitCtx& w,
+                        uint32_t tmem_base)
+{
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, 0, 1);
+    uint32_t stage = 0, phase = 0, slot = 0, slot_phase = 0, iter = 0;
+    for (;;) {
+        if (!wait_mbar(w, ptx::smem_u32(&aux.task_full[slot]), slot_phase, SITE_TASK_FULL))
+            break;
+        const int4 task = aux.task[slot];
+        ptx::mbar_arrive(ptx::smem_u32(&aux.task_empty[slot]));
+        if (++slot == TASK_SLOTS) {
+            slot = 0;
+            slot_phase ^= 1u;
+        }
+        if (task.x < 0)
+            break;
+        const int nk = (p.layer[task.x].K + BK - 1) / BK;
+        const uint32_t acc = iter & 1u;
+        const uint32_t acc_phase = (iter >> 1) & 1u;
+        if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_empty[acc]), acc_phase ^ 1u, SITE_TMEM_EMPTY))
+            break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+            ok = wait_mbar(w, ptx::smem_u32(&aux.full[stage]), phase, SITE_SMEM_FULL);
+            if (!ok)
+                break;
+            ptx::tc_fence_after();
+            const uint32_t sa = ptx::smem_u32(stages + stage * STAGE_BYTES);
+            const uint32_t sb = sa + A_STAGE_BYTES;
+            // A: K-major, rows of 128 B, 8-row groups 1 KiB apart; a 16-wide
+            // k step advances 32 B inside the swizzle atom.
+            const uint64_t adesc = ptx::sdesc_sw128(sa, 16, 1024);
+            // B: MN-major, 64-column blocks 8 KiB apart (LBO), 8-row k groups
+            // 1 KiB apart (SBO); a 16-deep k step advances 2 KiB.
+            const uint64_t bdesc = ptx::sdesc_sw128(sb, B_BOX_BYTES, 1024);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+                ptx::umma_bf16(d_tmem, adesc + static_cast<uint64_t>((k * 32) >> 4),
+                               bdesc + static_cast<uint64_t>((k * 2048) >> 4), idesc,
+                               (kb > 0 || k > 0) ? 1u : 0u);
+            ptx::umma_commit(ptx::smem_u32(&aux.empty[stage]));
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok)
+            break;
+        ptx::umma_commit(ptx::smem_u32(&aux.tmem_full[acc]));
+        ++iter;
+    }
+    // Exit: wait until every MMA this thread issued has completed.
+    ptx::umma_commit(ptx::smem_u32(&aux.drain));
+    wait_own(w, ptx::smem_u32(&aux.drain), 0u);
+}
+
+// ----------------------------------------------------------------- epilogue
+__device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int32_t col, int32_t ncols,
+                                            float (&b)[32])
+{
+    if (bias == nullptr) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            b[i] = 0.0f;
+        return;
+    }
+    if (col + 32 <= ncols) {
+        const uint4* src = reinterpret_cast<const uint4*>(bias + col);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldg(src + q);
+            b[q * 8 + 0] = bf16_lo(v.x);
+            b[q * 8 + 1] = bf16_hi(v.x);
+            b[q * 8 + 2] = bf16_lo(v.y);
+            b[q * 8 + 3] = bf16_hi(v.y);
+            b[q * 8 + 4] = bf16_lo(v.z);
+            b[q * 8 + 5] = bf16_hi(v.z);
+            b[q * 8 + 6] = bf16_lo(v.w);
+            b[q * 8 + 7] = bf16_hi(v.w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            b[i] = (col + i < ncols) ? __bfloat162float(bias[col + i]) : 0.0f;
+    }
+}
+
+template <int MAX_E>
+__device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
+                             uint32_t tmem_base, int warp, int lane)
+{
+    const uint32_t quad = static_cast<uint32_t>(warp & 3);   // TMEM lanes [32*quad, 32*quad+32)
+    const int32_t n1 = p.layer[0].n_tiles;
+    uint32_t slot = 0, slot_phase = 0, iter = 0;
+    for (;;) {
+        if (!wait_mbar(w, ptx::smem_u32(&aux.task_full[slot]), slot_phase, SITE_TASK_FULL))
+            break;
+        const int4 task = aux.task[slot];
+        __syncwarp();
+        if (lane == 0)
+            ptx::mbar_arrive(ptx::smem_u32(&aux.task_empty[slot]));
+        if (++slot == TASK_SLOTS) {
+            slot = 0;
+            slot_phase ^= 1u;
+        }
+        if (task.x < 0)
+            break;
+        const int L = task.x;
+        const LayerArgs& la = p.layer[L];
+        const uint32_t acc = iter & 1u;
+        const uint32_t acc_phase = (iter >> 1) & 1u;
+        if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_full[acc]), acc_phase, SITE_TMEM_FULL))
+            break;
+        ptx::tc_fence_after();
+
+        const __nv_bfloat16* bias = p.bias[L][expert_of(p, task.y)];
+        const int64_t row = static_cast<int64_t>(task.y) * BM + quad * 32 + lane;
+        const bool row_ok = row < la.rows;
+        const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            const int32_t col = task.z * BN + c * 32;
+            if (col >= la.ncols)
+                break;
+            uint32_t r[32];
+            __syncwarp();
+            ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+            ptx::tmem_ld_wait();
+            float b[32];
+            load_bias32(bias, col, la.ncols, b);
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                v[i] = act_apply(la.act, __uint_as_float(r[i]) + b[i]);
+            if (row_ok) {
+                const int nvalid = la.ncols - col < 32 ? la.ncols - col : 32;   // multiple of 8
+                if (la.out_f32) {
+                    float* dst = static_cast<float*>(la.out) + row * la.ld_out + col;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (q * 4 < nvalid)
+                            reinterpret_cast<float4*>(dst)[q] =
+                                make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+                } else {
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(la.out) + row * la.ld_out + col;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q * 8 < nvalid)
+                            reinterpret_cast<uint4*>(dst)[q] = make_uint4(
+                                pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                                pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+                }
+            }
+        }
+        // Accumulator drained: hand it back to the MMA warp.
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            ptx::mbar_arrive(ptx::smem_u32(&aux.tmem_empty[acc]));
+        ++iter;
+
+        // Layer-1 tile: publish this warp's quarter of the H tile by stamping
+        // the warp's flag word with the call's epoch (release, gpu scope).
+        if (L == 0 && p.mode == MODE_FUSED) {
+            ptx::fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) {
+                const int32_t fi = task.y * n1 + task.z;
+                if (fi != p.skip_flag) {
+                    __threadfence();
+                    ptx::st_release_gpu(&p.flags[fi * EPI_WARPS + quad], p.epoch);
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------- kernel
+template <int MAX_E>
+__global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_constant__ Params<MAX_E> p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* stages = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Aux& aux = *reinterpret_cast<Aux*>(stages + STAGES * STAGE_BYTES);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&aux.full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&aux.empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(ptx::smem_u32(&aux.tmem_full[a]), 1);
+            ptx::mbar_init(ptx::smem_u32(&aux.tmem_empty[a]), EPI_WARPS);
+        }
+        for (int s = 0; s < TASK_SLOTS; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&aux.task_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&aux.task_empty[s]), 1 + EPI_WARPS);
+        }
+        ptx::mbar_init(ptx::smem_u32(&aux.drain), 1);
+        aux.abort = 0u;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&p.map_a[0]);
+        ptx::prefetch_tmap(&p.map_a[1]);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&aux.tmem_base), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = aux.tmem_base;
+
+    const WaitCtx w{&aux.abort, p.ctrl, p.wait_limit_ns};
+    const int64_t m_blocks = p.m_blocks >= 0 ? p.m_blocks : static_cast<int64_t>(*p.m_blocks_dev);
+    const int64_t total = engine_total_tickets(m_blocks, p.layer[0].n_tiles, p.layer[1].n_tiles, p.mode);
+
+    if (warp == 0) {
+        if (lane == 0)
+            run_producer(p, aux, stages, w, m_blocks, total);
+    } else if (warp == 1) {
+        if (lane == 0)
+            run_mma(p, aux, stages, w, tmem_base);
+    } else {
+        run_epilogue(p, aux, w, tmem_base, warp, lane);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0) {
+        // The last CTA out resets the ticket counter for the next launch.
+        __threadfence();
+        if (atomicAdd(&p.ctrl->done, 1u) == gridDim.x - 1) {
+            p.ctrl->ticket = 0u;
+            p.ctrl->done = 0u;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace engine
+}  // namespace tffn

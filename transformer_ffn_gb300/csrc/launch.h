@@ -1,0 +1,34 @@
+// launch.h -- host-side launchers of the library's kernels (one per
+// translation unit), called by api.cu.  Every launcher returns 0 or -1 (launch
+// error; the CUDA error is left for the caller to read).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tffn {
+namespace engine {
+template <int MAX_E>
+struct Params;
+}
+namespace decode {
+struct Params;
+}
+
+constexpr int MOE_MAX_E = 64;
+
+int launch_engine_dense(const engine::Params<1>& p, int grid, cudaStream_t s);
+int launch_engine_grouped(const engine::Params<MOE_MAX_E>& p, int grid, cudaStream_t s);
+int launch_decode(const decode::Params& p, int grid, cudaStream_t s);
+
+int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w,
+                     cudaStream_t s);
+int launch_moe_plan(const int32_t* idx, int64_t T, int E, int k, int bm, int32_t* pos, int32_t* row_src,
+                    int32_t* band_expert, int32_t* nbands, int32_t* perm_out, int32_t* offs_out,
+                    cudaStream_t s);
+int launch_moe_gather(const void* X, const int32_t* row_src, const int32_t* nbands, int bm, int64_t N,
+                      void* Xp, int grid, cudaStream_t s);
+int launch_moe_combine(const float* Yp, const int32_t* pos, const float* w, int64_t T, int k, int64_t P,
+                       void* Y, int grid, cudaStream_t s);
+
+}  // namespace tffn
