@@ -1,0 +1,463 @@
+"""Benchmark of the fused FFN (and its decode / large / MoE workloads).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+A step is one ffn_forward (or moe_ffn_forward) call over one batch of
+synthetic input resident in HBM.  Timing: W untimed warm-up steps, then K
+steps, each bracketed by CUDA events on the launching stream, with a 256 MiB
+write between steps so that L2 (129 MB) holds nothing of the previous step;
+a barrier + device synchronisation on both sides of the timed block; the max
+over ranks.  Under torchrun every rank runs its own replica of the workload
+(the FFN has no data-path exchange: weak scaling, no collective but the
+timing barrier and max).
+
+Printed (rank 0): one JSON line with the metric, the roofline of the dominant
+kernel (its own CUDA-event time inside the timed steps), the end-to-end
+number through the public API with pinned host buffers (inputs copied in,
+result copied out inside the timed region), the clocks sampled during the
+timed region, and the CPU oracle timed on a bounded sample of the workload
+(rank 0, N = 1).  --impl reference times that oracle as the reference arm.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+# ----------------------------------------------------------------- workloads
+CONFIGS = {
+    "tiny": dict(kind="ffn", M=64, N=256, O=1024, P=256, act1="gelu_tanh", act2="none",
+                 label="tiny dense FFN M=64 N=256 O=1024 P=256, GELU-tanh"),
+    "prefill": dict(kind="ffn", M=4096, N=4096, O=16384, P=4096, act1="gelu_tanh", act2="none",
+                    label="prefill FFN M=4096 N=4096 O=16384 P=4096, GELU-tanh"),
+    "decode": dict(kind="ffn", M=16, N=8192, O=28672, P=8192, act1="relu", act2="none",
+                   label="decode FFN M=16 N=8192 O=28672 P=8192, ReLU"),
+    "large": dict(kind="ffn", M=16384, N=8192, O=28672, P=8192, act1="gelu_tanh", act2="relu",
+                  label="large prefill FFN M=16384 N=8192 O=28672 P=8192, GELU-tanh + ReLU"),
+    "moe": dict(kind="moe", M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="gelu_tanh", act2="none",
+                label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh"),
+}
+DEFAULT = "prefill"
+FLUSH_BYTES = 256 << 20
+
+# Dominant kernel of each workload (for the ncu traffic record).
+KERNEL = {"tiny": "engine_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
+          "moe": "engine_kernel", "decode": "decode_kernel"}
+KERNEL_SOURCES = {
+    "engine_kernel": ["engine.cuh", "common.cuh", "ptx.cuh", "schedule.h", "engine_dense.cu",
+                      "engine_grouped.cu"],
+    "decode_kernel": ["decode.cu", "decode.cuh", "common.cuh", "ptx.cuh"],
+}
+
+
+def flops(cfg):
+    """Algorithmic FLOPs of one step: 2*rows*O*(N+P), routed rows for MoE."""
+    rows = cfg["M"] * cfg.get("k", 1)
+    return 2.0 * rows * cfg["O"] * (cfg["N"] + cfg["P"])
+
+
+def weight_bytes(cfg):
+    """Bytes the decode step must move: W1, W2, X, Y, b1, b2 (bf16)."""
+    M, N, O, P = cfg["M"], cfg["N"], cfg["O"], cfg["P"]
+    return 2.0 * (N * O + O * P + M * N + M * P + O + P)
+
+
+def is_hbm_bound(cfg):
+    return cfg["kind"] == "ffn" and cfg["M"] <= 32
+
+
+def metric_of(cfg):
+    if is_hbm_bound(cfg):
+        return "fused FFN weight-stream bandwidth (small M)", "GB/s"
+    return "fused FFN throughput (large M)", "TFLOP/s"
+
+
+def rate(cfg, seconds):
+    if is_hbm_bound(cfg):
+        return weight_bytes(cfg) / seconds / 1e9
+    return flops(cfg) / seconds / 1e12
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], d["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+def kernel_sha(kernel):
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "transformer_ffn_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config):
+    """DRAM bytes per launch from the committed ncu record, if it was taken
+    on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_sha(KERNEL[config])
+    for line in open(path):
+        if line.startswith("#") or "=" not in line:
+            continue
+        kv = dict(p.split("=", 1) for p in line.split())
+        if kv.get("config") == config and kv.get("src_sha") == want:
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+# -------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------- helpers
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def make_inputs(cfg, device, seed=0):
+    from transformer_ffn_gb300 import synth
+    if cfg["kind"] == "moe":
+        return synth.moe_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], cfg["E"], seed=seed, device=device)
+    return synth.ffn_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], seed=seed, device=device)
+
+
+def step_fn(cfg, inp, out, X=None):
+    import transformer_ffn_gb300 as tffn
+    X = inp.X if X is None else X
+    if cfg["kind"] == "moe":
+        return lambda: tffn.moe_ffn_forward(X, inp.logits, cfg["k"], inp.W1, inp.b1, inp.W2, inp.b2,
+                                            cfg["act1"], cfg["act2"], out=out)
+    return lambda: tffn.ffn_forward(X, inp.W1, inp.b1, inp.W2, inp.b2, cfg["act1"], cfg["act2"], out=out)
+
+
+# ----------------------------------------------------------------- GPU arm
+def time_steps(step, steps, flush_buf, stream):
+    """Per-step device time (s) of `steps` steps, L2 flushed between them."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush_buf.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) / 1e3 for a, b in evs]
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    import transformer_ffn_gb300 as tffn
+
+    tffn.load()
+    cfg = CONFIGS[args.config]
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    inp = make_inputs(cfg, dev)
+    out = torch.empty((cfg["M"], cfg["P"]), dtype=torch.bfloat16, device=dev)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    step = step_fn(cfg, inp, out)
+
+    for _ in range(args.warmup):
+        flush_buf.zero_()
+        step()
+    tffn.check()
+    launches_per_step = tffn.last_launch_count()
+
+    # ---- timed region (device time, inputs resident)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    tffn.timing_begin()
+    t0 = time.perf_counter()
+    per_step = time_steps(step, args.steps, flush_buf, stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    n_dom, dom_ms = tffn.timing_end()
+    clocks = sampler.stop()
+    tffn.check()
+
+    mean_s = sum(per_step) / len(per_step)
+    mean_s = max_over_ranks(mean_s, world)
+    metric, unit = metric_of(cfg)
+    value = rate(cfg, mean_s) * world
+
+    # ---- dominant kernel roofline (its own events, same steps)
+    peak_tf, peak_gbs, peak_kind = measured_peaks()
+    dom_s = dom_ms / 1e3 / max(n_dom, 1)
+    if is_hbm_bound(cfg):
+        roof = {"bound": "hbm", "achieved": weight_bytes(cfg) / dom_s / 1e9, "peak": peak_gbs,
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops(cfg) / dom_s / 1e12, "peak": peak_tf, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json {'hbm_gbs' if is_hbm_bound(cfg) else 'bf16_tflops'})"
+    roof["kernel"] = KERNEL[args.config]
+    roof["kernel_ms"] = dom_s * 1e3
+    roof["traffic"] = recorded_traffic(args.config)
+
+    # ---- end to end through the public API: pinned host input in, result out
+    X_host = inp.X.cpu().pin_memory()
+    Y_host = torch.empty((cfg["M"], cfg["P"]), dtype=torch.bfloat16).pin_memory()
+    X_dev = torch.empty_like(inp.X)
+    logits_host = inp.logits.cpu().pin_memory() if cfg["kind"] == "moe" else None
+    e2e_step = step_fn(cfg, inp, out, X=X_dev)
+
+    def full_step():
+        X_dev.copy_(X_host, non_blocking=True)
+        if logits_host is not None:
+            inp.logits.copy_(logits_host, non_blocking=True)
+        e2e_step()
+        Y_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        full_step()
+    torch.cuda.synchronize()
+    e2e_s = time_steps(full_step, args.steps, flush_buf, stream)
+    tffn.check()
+    e2e_mean = max_over_ranks(sum(e2e_s) / len(e2e_s), world)
+    h2d = X_host.numel() * 2 + (logits_host.numel() * 4 if logits_host is not None else 0)
+    d2h = Y_host.numel() * 2
+
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; X~N(0,1), W~N(0,1/fan_in), b~U(-0.1,0.1), bf16)",
+        "config": {"workload": cfg["label"], "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between steps (256 MiB write outside the step events)",
+                   "global_batch": cfg["M"] * world, "flops_per_step": flops(cfg)},
+        "roofline": roof,
+        "e2e": {"value": rate(cfg, e2e_mean) * world, "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean * 1e3},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_block": wall,
+    }
+    if cfg["kind"] == "moe":
+        line["config"]["routed_rows"] = cfg["M"] * cfg["k"]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        Y_dev = out.clone()
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, Y_dev, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------- oracle (CPU) arms
+def _oracle_inputs(cfg, inp):
+    from transformer_ffn_gb300 import synth
+    u = synth.to_u16
+    if cfg["kind"] == "moe":
+        return (u(inp.X), inp.logits.cpu().numpy(), [u(w) for w in inp.W1], [u(b) for b in inp.b1],
+                [u(w) for w in inp.W2], [u(b) for b in inp.b2])
+    return (u(inp.X), u(inp.W1), u(inp.b1), u(inp.W2), u(inp.b2))
+
+
+def _oracle_rows(cfg, host, rows):
+    import oracle
+    acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "gelu_tanh": oracle.ACT_GELU_TANH}
+    if cfg["kind"] == "moe":
+        X, lg, W1, b1, W2, b2 = host
+        return oracle.moe_ffn(X, lg, cfg["k"], W1, b1, W2, b2, acts[cfg["act1"]], acts[cfg["act2"]],
+                              tokens=rows)
+    X, W1, b1, W2, b2 = host
+    return oracle.ffn(X, W1, b1, W2, b2, acts[cfg["act1"]], acts[cfg["act2"]], rows=rows)
+
+
+def _sample_work(cfg, nrows):
+    """Algorithmic work of nrows of the workload, in the metric's unit base."""
+    if is_hbm_bound(cfg):
+        return weight_bytes(cfg) * nrows / cfg["M"]     # share of the step's bytes
+    return flops(cfg) * nrows / cfg["M"]
+
+
+def cpu_baseline(cfg, inp, Y_dev=None, budget_s=15.0):
+    """The oracle, as it stands, on rows of the same workload: one row at a
+    time until about budget_s seconds of single-threaded work."""
+    import numpy as np
+    host = _oracle_inputs(cfg, inp)
+    rng = np.random.default_rng(0)
+    order = rng.permutation(cfg["M"])
+    done, t_total = [], 0.0
+    results = []
+    while t_total < budget_s and len(done) < cfg["M"]:
+        r = int(order[len(done)])
+        t0 = time.perf_counter()
+        y = _oracle_rows(cfg, host, [r])
+        t_total += time.perf_counter() - t0
+        done.append(r)
+        results.append(y[0])
+    metric, unit = metric_of(cfg)
+    out = {"value": (_sample_work(cfg, len(done)) / t_total) / (1e9 if unit == "GB/s" else 1e12),
+           "unit": unit, "cores": 1, "kind": "oracle",
+           "sample": f"{len(done)} of {cfg['M']} {'tokens' if cfg['kind'] == 'moe' else 'rows'} "
+                     f"({cfg['label']}), single-threaded C oracle, fp64 accumulation",
+           "seconds": t_total}
+    if Y_dev is not None:
+        got = Y_dev[done].float().cpu().numpy()
+        want = np.stack(results)
+        err = np.abs(got - want)
+        out["parity_on_sample"] = bool(np.all(err <= 1e-2 + 1e-2 * np.abs(want)))
+        out["max_abs_err_on_sample"] = float(err.max())
+    return out
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle timed on host cores, same metric."""
+    if rank != 0:
+        return
+    cfg = CONFIGS[args.config]
+    inp = make_inputs(cfg, "cpu")
+    import numpy as np
+    host = _oracle_inputs(cfg, inp)
+    rows_per_step = max(1, int(args.ref_rows))
+    rng = np.random.default_rng(1)
+    for _ in range(args.warmup):
+        _oracle_rows(cfg, host, [int(x) for x in rng.choice(cfg["M"], size=1)])
+    times = []
+    for _ in range(args.steps):
+        rows = [int(x) for x in rng.choice(cfg["M"], size=rows_per_step, replace=False)]
+        t0 = time.perf_counter()
+        _oracle_rows(cfg, host, rows)
+        times.append(time.perf_counter() - t0)
+    mean_s = sum(times) / len(times)
+    metric, unit = metric_of(cfg)
+    val = (_sample_work(cfg, rows_per_step) / mean_s) / (1e9 if unit == "GB/s" else 1e12)
+    sample = (f"{rows_per_step} random rows of {cfg['M']} per step ({cfg['label']}), "
+              f"single-threaded C oracle, fp64 accumulation")
+    line = {"impl": "reference", "metric": metric, "value": val, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, same recipe as the GPU arm)",
+            "config": {"workload": cfg["label"], "rows_per_step": rows_per_step},
+            "cpu_baseline": {"value": val, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT, choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="tffn", choices=["tffn", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_gpu(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -64,6 +64,7 @@ def test_ffn_validation_without_gpu(lib):
     assert _ffn(lib, X=24) == bad          # 8-byte aligned only
     assert _ffn(lib, b1=40) == bad
     assert _ffn(lib, M=0) == 0             # empty call: nothing to do, no launch
+    assert _ffn(lib, M=0, X=None, Y=None) == 0
     assert lib.tffn_last_launch_count() == 0
 
 
@@ -85,6 +86,7 @@ def test_moe_validation_without_gpu(lib):
     zeros = (ctypes.c_void_p * E)(*([16, 0, 16, 16]))
     assert call(w1=ctypes.cast(zeros, ctypes.c_void_p)) == -1
     assert call(T=0) == 0
+    assert call(T=0, X=None, logits=None) == 0
 
 
 def test_workspace_bytes_holds_hidden_tensor(lib):

@@ -293,17 +293,17 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
                 int act2, int64_t M, int64_t N, int64_t O, int64_t P, void* Y, struct CUstream_st* stream)
 {
     g_last_launches = 0;
-    if (!X || !W1 || !W2 || !Y)
-        return TFFN_ERR_INVALID_ARG;
     if (M < 0 || M >= (int64_t(1) << 31) || !dim_ok(N) || !dim_ok(O) || !dim_ok(P))
         return TFFN_ERR_INVALID_ARG;
     if (!act_ok(act1) || !act_ok(act2))
         return TFFN_ERR_INVALID_ARG;
+    if (M == 0)
+        return TFFN_OK;   // empty call: X and Y may be NULL
+    if (!X || !W1 || !W2 || !Y)
+        return TFFN_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W1) || !aligned16(W2) || !aligned16(Y) || (b1 && !aligned16(b1)) ||
         (b2 && !aligned16(b2)))
         return TFFN_ERR_INVALID_ARG;
-    if (M == 0)
-        return TFFN_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     std::lock_guard<std::mutex> lock(g_mu);
@@ -416,13 +416,15 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
                     struct CUstream_st* stream)
 {
     g_last_launches = 0;
-    if (!X || !gate_logits || !W1 || !W2 || !Y)
-        return TFFN_ERR_INVALID_ARG;
     if (E < 1 || E > MOE_MAX_E || top_k < 1 || top_k > E)
         return TFFN_ERR_INVALID_ARG;
     if (T < 0 || T * top_k >= (int64_t(1) << 30) || !dim_ok(N) || !dim_ok(O) || !dim_ok(P))
         return TFFN_ERR_INVALID_ARG;
     if (!act_ok(act1) || !act_ok(act2))
+        return TFFN_ERR_INVALID_ARG;
+    if (T == 0)
+        return TFFN_OK;   // empty call: X, gate_logits and Y may be NULL
+    if (!X || !gate_logits || !W1 || !W2 || !Y)
         return TFFN_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(gate_logits) & 3u))
         return TFFN_ERR_INVALID_ARG;
@@ -434,8 +436,6 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
         if (b2 && b2[e] && !aligned16(b2[e]))
             return TFFN_ERR_INVALID_ARG;
     }
-    if (T == 0)
-        return TFFN_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     std::lock_guard<std::mutex> lock(g_mu);
