@@ -124,6 +124,35 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
                     int64_t T, int64_t N, int64_t O, int64_t P, int E, int act1, int act2,
                     tffn_routing* routing, struct CUstream_st* stream);
 
+/*
+ * ffn_forward_decode_noalloc -- ffn_forward for M <= 32 rows (the decode
+ * shapes) that allocates nothing.  The paper has no counterpart: this entry
+ * point exists for callers that cannot allocate device memory -- plugins
+ * whose host framework owns every byte of HBM, code that must not trigger the
+ * device-wide synchronisation of cudaMalloc/cudaFree, and callers without
+ * access to any allocator, torch's included.
+ *
+ * Same arguments, layouts, numerics and validation as ffn_forward (M <= 32,
+ * else TFFN_ERR_INVALID_ARG).  The caller passes inputs and outputs; all
+ * scratch (control word, ready flags, split-K counters, H, partial sums) lives
+ * in one static 16 MiB device array in the library, held by every GPU that
+ * loads it until the process exits.  A shape whose scratch does not fit
+ * returns TFFN_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on each device fetches the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and clears its flags and counters
+ *     (cudaMemsetAsync) on `stream` before its kernel: calls that overlap on
+ *     the GPU (different streams, not ordered) race and corrupt each other.
+ *   - It calls no cudaMalloc, cudaFree or allocating routine, and does not use
+ *     or need the workspace of the other entry points.  A device wait that ran
+ *     out of time leaves Y incomplete; the record stays in the array (not read
+ *     by tffn_check) until the next call clears it.
+ */
+int ffn_forward_decode_noalloc(const void* X, const void* W1, const void* b1, const void* W2,
+                               const void* b2, int act1, int act2, int64_t M, int64_t N, int64_t O,
+                               int64_t P, void* Y, struct CUstream_st* stream);
+
 /* Bytes of workspace a call of this shape needs (E = 0 for ffn_forward). */
 size_t tffn_workspace_bytes(int64_t M, int64_t N, int64_t O, int64_t P, int E, int top_k);
 
