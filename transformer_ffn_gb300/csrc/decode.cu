@@ -33,8 +33,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1)
 {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -64,7 +63,10 @@ __device__ __forceinline__ void zero(Acc<MT>& a)
                 a.c[m][n][i] = 0.0f;
 }
 
-// One KC x SLICE unit: this warp's 32 columns, all K rows of the stage.
+// One KC x SLICE unit: this warp's 32 columns, all K rows of the stage.  The
+// fragments of four k-steps are loaded first and the MMAs issued after, so the
+// shared-memory latency of the loads overlaps instead of sitting in front of
+// every MMA.
 template <int MT>
 __device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uint32_t a_base, int cw, int lane)
 {
@@ -73,27 +75,37 @@ __device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uin
     const uint32_t j = static_cast<uint32_t>(lane >> 3);
     const uint32_t r = static_cast<uint32_t>(lane & 7);
 #pragma unroll
-    for (int ks = 0; ks < KC / 16; ++ks) {
-        uint32_t a[MT][4];
-        const uint32_t abox = a_base + static_cast<uint32_t>(ks >> 2) * A_BOX_BYTES;
-        const uint32_t kchunk = static_cast<uint32_t>((ks & 3) * 2) + (j >> 1);
+    for (int half = 0; half < KC / 64; ++half) {
+        uint32_t a[4][MT][4];
+        uint32_t b[4][2][4];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const uint32_t row = static_cast<uint32_t>(m * 16) + (j & 1u) * 8u + r;
-            ldsm_x4(abox + sw128(row, kchunk), a[m][0], a[m][1], a[m][2], a[m][3]);
-        }
-#pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-            const uint32_t krow = static_cast<uint32_t>(ks * 16) + (j & 1u) * 8u + r;
-            const uint32_t nchunk = cb_chunk + static_cast<uint32_t>(pr * 2) + (j >> 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(wbox + sw128(krow, nchunk), b0, b1, b2, b3);
+        for (int kk = 0; kk < 4; ++kk) {
+            const int ks = half * 4 + kk;
+            const uint32_t abox = a_base + static_cast<uint32_t>(ks >> 2) * A_BOX_BYTES;
+            const uint32_t kchunk = static_cast<uint32_t>((ks & 3) * 2) + (j >> 1);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                mma_bf16_16816(acc.c[m][pr * 2 + 0], a[m][0], a[m][1], a[m][2], a[m][3], b0, b1);
-                mma_bf16_16816(acc.c[m][pr * 2 + 1], a[m][0], a[m][1], a[m][2], a[m][3], b2, b3);
+                const uint32_t row = static_cast<uint32_t>(m * 16) + (j & 1u) * 8u + r;
+                ldsm_x4(abox + sw128(row, kchunk), a[kk][m][0], a[kk][m][1], a[kk][m][2], a[kk][m][3]);
+            }
+            const uint32_t krow = static_cast<uint32_t>(ks * 16) + (j & 1u) * 8u + r;
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const uint32_t nchunk = cb_chunk + static_cast<uint32_t>(pr * 2) + (j >> 1);
+                ldsm_x4_t(wbox + sw128(krow, nchunk), b[kk][pr][0], b[kk][pr][1], b[kk][pr][2], b[kk][pr][3]);
             }
         }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    mma_bf16_16816(acc.c[m][pr * 2 + 0], a[kk][m][0], a[kk][m][1], a[kk][m][2], a[kk][m][3],
+                                   b[kk][pr][0], b[kk][pr][1]);
+                    mma_bf16_16816(acc.c[m][pr * 2 + 1], a[kk][m][0], a[kk][m][1], a[kk][m][2], a[kk][m][3],
+                                   b[kk][pr][2], b[kk][pr][3]);
+                }
     }
 }
 
@@ -201,6 +213,160 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
     }
 }
 
+// Wait, with the whole warp, until every layer-1 slice of H in the cyclic
+// window [k0, k0 + count) of kch slices is ready (all four words equal the
+// epoch).  Relaxed loads spread over the lanes, then an acquire fence in every
+// lane: one pass over many flags instead of one serialised acquire per unit.
+__device__ bool wait_h_window(const WaitCtx& w, const uint32_t* flags, uint32_t epoch, int64_t k0, int64_t count,
+                              int64_t kch, int lane)
+{
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        bool mine = true;
+        for (int64_t i = lane; i < count && mine; i += 32) {
+            const uint32_t* f = flags + ((k0 + i) % kch) * CONSUMER_WARPS;
+            uint32_t v[CONSUMER_WARPS];
+#pragma unroll
+            for (int q = 0; q < CONSUMER_WARPS; ++q)
+                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v[q]) : "l"(f + q) : "memory");
+#pragma unroll
+            for (int q = 0; q < CONSUMER_WARPS; ++q)
+                mine = mine && (v[q] == epoch);
+        }
+        if (__all_sync(0xffffffffu, mine))
+            break;
+        if (__any_sync(0xffffffffu, *w.abort != 0u))
+            return false;
+        bool late = lane == 0 && ptx::globaltimer() - t0 > w.limit_ns;
+        late = __shfl_sync(0xffffffffu, late, 0);
+        if (late) {
+            if (lane == 0)
+                raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), SITE_SLICE_FLAG, static_cast<uint32_t>(k0));
+            return false;
+        }
+        __nanosleep(256);
+    }
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    __syncwarp();
+    return true;
+}
+
+// Warp 0.  Layer 1 streams W1 and X; layer 2 first prefetches the W2 part of
+// its first stages (W2 does not depend on H), then waits once for every H
+// slice its unit range reads, then streams W2 and H.
+template <int MT>
+__device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const WaitCtx& w, int lane)
+{
+    constexpr uint32_t A_BYTES = 2u * (16u * MT) * 64u * 2u;
+    const Plan& pl = p.plan;
+    const int64_t G = pl.grid, c = blockIdx.x;
+    uint32_t stage = 0, phase = 0;
+    int32_t last_phase[STAGES];
+    for (int s = 0; s < STAGES; ++s)
+        last_phase[s] = -1;
+    uint64_t evict_first = 0;
+    if (lane == 0)
+        evict_first = ptx::policy_evict_first();
+    bool ok = true;
+
+    auto issue_w = [&](int layer, int64_t slice, int64_t kc, uint32_t st) {
+        const uint32_t fb = ptx::smem_u32(&aux.full[st]);
+        const uint32_t sw = ptx::smem_u32(stages + st * STAGE_BYTES);
+        ptx::tma_load_2d_hint(sw, &p.map_w[layer], fb, static_cast<int32_t>(slice * SLICE),
+                              static_cast<int32_t>(kc * KC), evict_first);
+        ptx::tma_load_2d_hint(sw + W_BOX_BYTES, &p.map_w[layer], fb, static_cast<int32_t>(slice * SLICE + 64),
+                              static_cast<int32_t>(kc * KC), evict_first);
+    };
+    auto issue_a = [&](int layer, int64_t kc, uint32_t st) {
+        const uint32_t fb = ptx::smem_u32(&aux.full[st]);
+        const uint32_t sa = ptx::smem_u32(stages + st * STAGE_BYTES) + W_STAGE_BYTES;
+        ptx::tma_load_2d(sa, &p.map_a[layer], fb, static_cast<int32_t>(kc * KC), 0);
+        ptx::tma_load_2d(sa + A_BOX_BYTES, &p.map_a[layer], fb, static_cast<int32_t>(kc * KC + 64), 0);
+    };
+    auto advance = [&]() {
+        if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    };
+
+    // ---- layer 1
+    if (lane == 0) {
+        const int64_t U = pl.units[0], kch = pl.kch[0];
+        const int64_t u0 = range_start(c, U, G), u1 = range_start(c + 1, U, G);
+        for (int64_t u = u0; u < u1; ++u) {
+            ok = wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY);
+            if (!ok)
+                break;
+            ptx::mbar_arrive_expect_tx(ptx::smem_u32(&aux.full[stage]), W_STAGE_BYTES + A_BYTES);
+            issue_w(0, u / kch, u % kch, stage);
+            issue_a(0, u % kch, stage);
+            last_phase[stage] = static_cast<int32_t>(phase);
+            advance();
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+
+    // ---- layer 2
+    if (ok) {
+        const int64_t U = pl.units[1], kch = pl.kch[1];
+        const int64_t u0 = range_start(c, U, G), u1 = range_start(c + 1, U, G);
+        const int64_t npre = (u1 - u0) < STAGES ? (u1 - u0) : STAGES;
+        uint32_t pre_stage[STAGES];
+        if (lane == 0) {
+            for (int64_t i = 0; i < npre; ++i) {
+                const int64_t u = u0 + i;
+                ok = wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY);
+                if (!ok)
+                    break;
+                ptx::mbar_arrive_expect_tx(ptx::smem_u32(&aux.full[stage]), W_STAGE_BYTES + A_BYTES);
+                issue_w(1, u / kch, u % kch, stage);
+                pre_stage[i] = stage;
+                last_phase[stage] = static_cast<int32_t>(phase);
+                advance();
+            }
+        }
+        const int npre_done = __shfl_sync(0xffffffffu, ok ? static_cast<int>(npre) : -1, 0);
+        if (npre_done >= 0) {
+            const int64_t count = (u1 - u0) < kch ? (u1 - u0) : kch;
+            const bool ready = wait_h_window(w, p.flags, p.epoch, u0 % kch, count, kch, lane);
+            if (lane == 0) {
+                ptx::fence_proxy_async_global();
+                // the prefetched stages expect their H bytes: issue them even
+                // after a failed wait so that every barrier completes
+                for (int64_t i = 0; i < npre; ++i)
+                    issue_a(1, (u0 + i) % kch, pre_stage[i]);
+                if (ready) {
+                    for (int64_t u = u0 + npre; u < u1; ++u) {
+                        if (!wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY))
+                            break;
+                        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&aux.full[stage]), W_STAGE_BYTES + A_BYTES);
+                        issue_w(1, u / kch, u % kch, stage);
+                        issue_a(1, u % kch, stage);
+                        last_phase[stage] = static_cast<int32_t>(phase);
+                        advance();
+                    }
+                }
+            }
+        }
+    }
+
+    // Exit: every copy issued by this warp has landed before the CTA leaves.
+    if (lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            if (last_phase[s] < 0)
+                continue;
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(ptx::smem_u32(&aux.full[s]), static_cast<uint32_t>(last_phase[s]))) {
+                if (ptx::globaltimer() - t0 > p.wait_limit_ns) {
+                    raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), SITE_DRAIN, s);
+                    break;
+                }
+            }
+        }
+    }
+}
+
 template <int MT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_constant__ Params p)
 {
@@ -210,7 +376,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
     Aux& aux = *reinterpret_cast<Aux*>(stages + STAGES * STAGE_BYTES);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    constexpr uint32_t A_BYTES = 2u * (16u * MT) * 64u * 2u;
     const Plan& pl = p.plan;
     const int64_t G = pl.grid;
     const int64_t c = blockIdx.x;
@@ -227,68 +392,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
     const WaitCtx w{&aux.abort, p.ctrl, p.wait_limit_ns};
 
     if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t evict_first = ptx::policy_evict_first();
-            uint32_t stage = 0, phase = 0;
-            int32_t last_phase[STAGES];
-            for (int s = 0; s < STAGES; ++s)
-                last_phase[s] = -1;
-            bool ok = true;
-            for (int layer = 0; layer < 2 && ok; ++layer) {
-                const int64_t U = pl.units[layer], kch = pl.kch[layer];
-                const int64_t u0 = range_start(c, U, G), u1 = range_start(c + 1, U, G);
-                const CUtensorMap* mw = &p.map_w[layer];
-                const CUtensorMap* ma = &p.map_a[layer];
-                int64_t last_h = -1;
-                for (int64_t u = u0; u < u1; ++u) {
-                    const int64_t slice = u / kch, kc = u % kch;
-                    ok = wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY);
-                    if (!ok)
-                        break;
-                    const uint32_t fb = ptx::smem_u32(&aux.full[stage]);
-                    const uint32_t sw = ptx::smem_u32(stages + stage * STAGE_BYTES);
-                    const uint32_t sa = sw + W_STAGE_BYTES;
-                    ptx::mbar_arrive_expect_tx(fb, W_STAGE_BYTES + A_BYTES);
-                    ptx::tma_load_2d_hint(sw, mw, fb, static_cast<int32_t>(slice * SLICE),
-                                          static_cast<int32_t>(kc * KC), evict_first);
-                    ptx::tma_load_2d_hint(sw + W_BOX_BYTES, mw, fb, static_cast<int32_t>(slice * SLICE + 64),
-                                          static_cast<int32_t>(kc * KC), evict_first);
-                    if (layer == 1 && kc != last_h) {
-                        for (int q = 0; q < CONSUMER_WARPS && ok; ++q)
-                            ok = wait_flag(w, p.flags + kc * CONSUMER_WARPS + q, p.epoch, SITE_SLICE_FLAG,
-                                           static_cast<uint32_t>(kc));
-                        if (!ok) {
-                            // the W copies above are in flight: still drain them
-                            ptx::tma_load_2d(sa, ma, fb, static_cast<int32_t>(kc * KC), 0);
-                            ptx::tma_load_2d(sa + A_BOX_BYTES, ma, fb, static_cast<int32_t>(kc * KC + 64), 0);
-                            last_phase[stage] = static_cast<int32_t>(phase);
-                            break;
-                        }
-                        ptx::fence_proxy_async_global();
-                        last_h = kc;
-                    }
-                    ptx::tma_load_2d(sa, ma, fb, static_cast<int32_t>(kc * KC), 0);
-                    ptx::tma_load_2d(sa + A_BOX_BYTES, ma, fb, static_cast<int32_t>(kc * KC + 64), 0);
-                    last_phase[stage] = static_cast<int32_t>(phase);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            // Exit: every copy issued by this thread has landed before the CTA leaves.
-            for (int s = 0; s < STAGES; ++s) {
-                if (last_phase[s] < 0)
-                    continue;
-                const uint64_t t0 = ptx::globaltimer();
-                while (!ptx::mbar_try_wait(ptx::smem_u32(&aux.full[s]), static_cast<uint32_t>(last_phase[s]))) {
-                    if (ptx::globaltimer() - t0 > p.wait_limit_ns) {
-                        raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), SITE_DRAIN, s);
-                        break;
-                    }
-                }
-            }
-        }
+        run_producer<MT>(p, aux, stages, w, lane);
     } else {
         const int cw = warp - 1;
         uint32_t stage = 0, phase = 0;
