@@ -132,7 +132,7 @@ def test_engine_task_order_is_dependency_safe(lib):
 def test_debug_tiles(lib):
     import transformer_ffn_gb300 as tffn
     t = tffn.debug_tiles()
-    assert t["BM"] == 128 and t["BN"] % 64 == 0 and t["BK"] == 64
+    assert t["BM"] in (128, 256) and t["BN"] % 64 == 0 and t["BK"] == 64
     assert t["decode_slice"] == t["decode_kc"]
 
 

@@ -229,7 +229,7 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P)
     L.m_blocks = (M + engine::BM - 1) / engine::BM;
     L.n1 = static_cast<int32_t>((O + engine::BN - 1) / engine::BN);
     L.n2 = static_cast<int32_t>((P + engine::BN - 1) / engine::BN);
-    if (L.path == 1 && static_cast<size_t>(L.m_blocks) * L.n1 * 4 > FLAG_WORDS)
+    if (L.path == 1 && static_cast<size_t>(L.m_blocks) * L.n1 * engine::FLAG_WORDS_PER_TILE > FLAG_WORDS)
         L.path = 3;   // more layer-1 tiles than flags: run the layers as two launches
     L.total = align_up(L.off_h + static_cast<size_t>(L.m_blocks) * engine::BM * O * 2, 256);
     return L;
@@ -363,7 +363,7 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
     std::memset(&p, 0, sizeof(p));
     void* H = base + L.off_h;
     const int64_t rows_h = L.m_blocks * engine::BM;
-    if (make_map(&p.map_a[0], X, N, M, 64, engine::BM) || make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM) ||
+    if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) || make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) ||
         make_map(&p.map_b[0][0], W1, O, N, 64, engine::BK) || make_map(&p.map_b[1][0], W2, P, O, 64, engine::BK))
         return TFFN_ERR_INVALID_ARG;
     p.bias[0][0] = static_cast<const __nv_bfloat16*>(b1);
@@ -386,9 +386,9 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
         p.epoch = epoch;
         p.mode = MODE_FUSED;
         const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, MODE_FUSED);
-        const int grid = static_cast<int>(total < d->sms ? total : d->sms);
+        const int pairs = static_cast<int>(total < d->sms ? total : d->sms);
         timing_start(s);
-        if (launch_engine_dense(p, grid, s) != 0)
+        if (launch_engine_dense(p, pairs, s) != 0)
             return TFFN_ERR_CUDA;
         timing_stop(s);
         g_last_launches = 1;
@@ -399,10 +399,10 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
         p.mode = mode;
         p.epoch = 0;
         const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, mode);
-        const int grid = static_cast<int>(total < d->sms ? total : d->sms);
+        const int pairs = static_cast<int>(total < d->sms ? total : d->sms);
         if (mode == MODE_LAYER1)
             timing_start(s);
-        if (launch_engine_dense(p, grid, s) != 0)
+        if (launch_engine_dense(p, pairs, s) != 0)
             return TFFN_ERR_CUDA;
         ++g_last_launches;
     }
@@ -444,7 +444,7 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     if (rc != TFFN_OK)
         return rc;
     const MoeLayout L = moe_layout(T, N, O, P, E, top_k);
-    if (static_cast<size_t>(L.mbmax) * L.n1 * 4 > FLAG_WORDS)
+    if (static_cast<size_t>(L.mbmax) * L.n1 * engine::FLAG_WORDS_PER_TILE > FLAG_WORDS)
         return TFFN_ERR_UNSUPPORTED;
     uint8_t* base = nullptr;
     rc = workspace(*d, L.total, s, &base);
@@ -467,8 +467,8 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     engine::Params<MOE_MAX_E>* pp = new engine::Params<MOE_MAX_E>;
     std::memset(pp, 0, sizeof(*pp));
     engine::Params<MOE_MAX_E>& p = *pp;
-    int bad = make_map(&p.map_a[0], Xp, N, L.Rmax, 64, engine::BM) |
-              make_map(&p.map_a[1], H, O, L.Rmax, 64, engine::BM);
+    int bad = make_map(&p.map_a[0], Xp, N, L.Rmax, 64, engine::BM_CTA) |
+              make_map(&p.map_a[1], H, O, L.Rmax, 64, engine::BM_CTA);
     for (int e = 0; e < E && !bad; ++e) {
         bad |= make_map(&p.map_b[0][e], W1[e], O, N, 64, engine::BK);
         bad |= make_map(&p.map_b[1][e], W2[e], P, O, 64, engine::BK);
@@ -499,7 +499,7 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     fail |= launch_moe_gather(X, src, nb, engine::BM, N, Xp, d->sms * 4, s);
     if (!fail) {
         timing_start(s);
-        fail |= launch_engine_grouped(p, d->sms, s);
+        fail |= launch_engine_grouped(p, d->sms / 2, s);
         timing_stop(s);
     }
     fail |= launch_moe_combine(Yp, pos, w, T, top_k, P, Y, d->sms * 4, s);

@@ -47,12 +47,15 @@ struct WaitCtx {
     volatile uint32_t* abort;   // CTA-wide abort flag in shared memory
     DevCtrl* ctrl;
     uint64_t limit_ns;
+    uint32_t peer_abort;        // shared::cluster address of the peer CTA's abort flag (0: none)
 };
 
 __device__ __forceinline__ void raise_error(const WaitCtx& w, uint32_t code, uint32_t where,
                                             uint32_t info)
 {
     *w.abort = 1u;
+    if (w.peer_abort != 0u)
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(w.peer_abort), "r"(1u) : "memory");
     if (atomicCAS(&w.ctrl->status, 0u, code) == 0u) {
         w.ctrl->where = where;
         w.ctrl->block = blockIdx.x;
@@ -69,6 +72,26 @@ static __device__ __noinline__ bool wait_mbar(const WaitCtx& w, uint32_t bar, ui
     const uint64_t t0 = ptx::globaltimer();
     for (;;) {
         if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        if (*w.abort)
+            return false;
+        if (ptx::globaltimer() - t0 > w.limit_ns) {
+            raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), where, parity);
+            return false;
+        }
+    }
+}
+
+// Same, acquiring at cluster scope: for barriers that receive arrivals from the
+// peer CTA of a cluster (or from its tensor-core commits).
+static __device__ __noinline__ bool wait_mbar_cl(const WaitCtx& w, uint32_t bar, uint32_t parity,
+                                                 uint32_t where)
+{
+    if (ptx::mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        if (ptx::mbar_try_wait_cluster(bar, parity))
             return true;
         if (*w.abort)
             return false;

@@ -1,30 +1,42 @@
-// engine.cuh -- the persistent, warp-specialised tcgen05 engine that runs the
-// two GEMMs of the FFN (and of every expert of the MoE form) in one launch.
+// engine.cuh -- the persistent, warp-specialised 2-SM tcgen05 engine that runs
+// the two GEMMs of the FFN (and of every expert of the MoE form) in one launch.
 //
 // What it computes ("Kernel fusion and tensor parallelism", section
 // "Megatron-LM tensor parallelism", FFN equation; section "Step 1"):
 //   layer 1 tile (band i, tile j):  H[i, j] = bf16(act1(X[i, :] W1[:, j] + b1[j]))
 //   layer 2 tile (band i, tile k):  Y[i, k] = act2(H[i, :] W2[:, k] + b2[k])
-// with fp32 accumulation in tensor memory.  A layer-1 tile publishes a ready
-// flag once its H tile is in global memory; a layer-2 tile of the same band
+// with fp32 accumulation in tensor memory.  A layer-1 tile publishes ready
+// flags once its H tile is in global memory; a layer-2 tile of the same band
 // waits on those flags chunk by chunk before its TMA loads read H, so H is
 // consumed while the rest of H is still being produced (the page's per-tile
 // flag, used here between the SMs of one GPU).
 //
-// CTA layout (192 threads, one CTA per SM):
-//   warp 0      TMA producer: takes tickets, publishes tasks, streams A/B
-//               k-slices into a STAGES-deep shared-memory ring
-//   warp 1      owns the tensor memory (512 columns = two 128x256 fp32
-//               accumulators) and issues tcgen05.mma from one thread
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane quadrant
-//               per warp, one row per thread), add bias, activation, round,
-//               store; the accumulator is double-buffered so the epilogue of
-//               one tile overlaps the main loop of the next.
+// Tiles are 256 x 256 and belong to a cluster of two CTAs on two SMs (a CTA
+// pair): tcgen05.mma.cta_group::2 with M = 256 reads A's rows split between
+// the pair (128 each) and B's columns split between the pair (128 each), and
+// writes each CTA's tensor memory with its 128 rows x 256 columns.  Each CTA
+// therefore streams only half of the B tile: 32 KiB per 64-deep k-stage per
+// SM, six stages deep.
+//
+// CTA layout (192 threads, one CTA per SM, two CTAs per cluster):
+//   warp 0      TMA producer.  The leader (cluster rank 0) takes tickets and
+//               publishes each task to both CTAs' task rings; both producers
+//               stream their own A rows and B columns into their own ring and
+//               count the bytes on the leader's stage barrier (cta_group::2
+//               copies), so the leader sees one barrier per stage for the pair.
+//   warp 1      leader: issues the pair MMAs from one thread and commits
+//               them to both CTAs' barriers (multicast).  Both CTAs: own the
+//               CTA's tensor memory (512 columns = two accumulators of 128
+//               lanes x 256 fp32 columns).
+//   warps 2..5  epilogue: tcgen05.ld the CTA's accumulator (one TMEM lane
+//               quadrant per warp, one row per thread), bias, activation,
+//               round, store; the accumulator is double-buffered so the
+//               epilogue of one tile overlaps the main loop of the next.
 //
 // Operands: A (X or H) is row-major [rows x K]: K-major, 128-byte swizzle,
 // boxes of 64 (K) x 128 (rows).  B (W1 or W2) is row-major [K x cols]: the
-// columns are contiguous, so B is MN-major: four boxes of 64 (cols) x 64 (K)
-// per stage, 128-byte swizzle.
+// columns are contiguous, so B is MN-major: two boxes of 64 (cols) x 64 (K)
+// per CTA per stage, 128-byte swizzle.
 #pragma once
 
 #include <cuda.h>
@@ -36,20 +48,26 @@
 namespace tffn {
 namespace engine {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 256;                                   // rows of a pair tile (a band)
+constexpr int BM_CTA = 128;                               // rows per CTA
+constexpr int BN = 256;                                   // columns of a tile
+constexpr int BN_CTA = 128;                               // B columns loaded per CTA
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;              // 16 KiB
-constexpr int B_BOX_BYTES = 64 * BK * 2;                // 8 KiB: 64 cols x 64 k
-constexpr int B_STAGE_BYTES = BK * BN * 2;              // 32 KiB
+constexpr int STAGES = 6;
+constexpr int A_STAGE_BYTES = BM_CTA * BK * 2;            // 16 KiB
+constexpr int B_BOX_BYTES = 64 * BK * 2;                  // 8 KiB: 64 cols x 64 k
+constexpr int B_STAGE_BYTES = BK * BN_CTA * 2;            // 16 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TASK_SLOTS = 4;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARPS = 4;
+constexpr int FLAG_WORDS_PER_TILE = 2 * EPI_WARPS;        // one per epilogue warp of the pair
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int AUX_BYTES = 1024;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + 1024;   // + alignment slack
+// Arrivals that free a task slot (counted on the leader): leader MMA thread,
+// leader epilogue warps, peer producer, peer epilogue warps.
+constexpr uint32_t TASK_CONSUMERS = 1 + EPI_WARPS + 1 + EPI_WARPS;
 
 // Per-layer arguments.
 struct LayerArgs {
@@ -66,14 +84,14 @@ struct LayerArgs {
 
 template <int MAX_E>
 struct Params {
-    CUtensorMap map_a[2];                      // layer-1 A (X), layer-2 A (H)
-    CUtensorMap map_b[2][MAX_E];               // W1[e], W2[e]
+    CUtensorMap map_a[2];                      // layer-1 A (X), layer-2 A (H); box {64, 128}
+    CUtensorMap map_b[2][MAX_E];               // W1[e], W2[e]; box {64, 64}
     const __nv_bfloat16* bias[2][MAX_E];       // b1[e], b2[e] (nullable)
     LayerArgs layer[2];
-    int64_t m_blocks;                          // row bands; < 0: read *m_blocks_dev
+    int64_t m_blocks;                          // 256-row bands; < 0: read *m_blocks_dev
     const int32_t* m_blocks_dev;
     const int32_t* band_expert;                // expert of each band (NULL: expert 0)
-    uint32_t* flags;                           // [m_blocks * n1 * 4] ready words
+    uint32_t* flags;                           // [m_blocks * n1 * 8] ready words
     DevCtrl* ctrl;
     uint64_t wait_limit_ns;
     uint32_t epoch;                            // value of a ready flag word in this call
@@ -82,15 +100,16 @@ struct Params {
     int32_t skip_flag;                         // test fault injection, -1 = off
 };
 
-// Everything in shared memory besides the stage ring.
+// Everything in shared memory besides the stage ring (same offsets in both
+// CTAs of a pair, which the cross-CTA addressing relies on).
 struct Aux {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t tmem_full[2];
-    uint64_t tmem_empty[2];
+    uint64_t full[STAGES];          // leader: the TMA bytes of both CTAs (peer's copy unused)
+    uint64_t empty[STAGES];         // MMA done with the stage (multicast commit)
+    uint64_t tmem_full[2];          // accumulator ready (multicast commit)
+    uint64_t tmem_empty[2];         // leader: eight epilogue warps of the pair drained it
     uint64_t task_full[TASK_SLOTS];
-    uint64_t task_empty[TASK_SLOTS];
-    uint64_t drain;
+    uint64_t task_empty[TASK_SLOTS];    // leader only
+    uint64_t drain;                 // leader: every MMA issued has completed
     int4 task[TASK_SLOTS];
     uint32_t tmem_base;
     uint32_t abort;
@@ -102,7 +121,7 @@ static_assert(sizeof(Aux) <= AUX_BYTES, "aux block fits");
 __device__ __forceinline__ void wait_own(const WaitCtx& w, uint32_t bar, uint32_t parity)
 {
     const uint64_t t0 = ptx::globaltimer();
-    while (!ptx::mbar_try_wait(bar, parity)) {
+    while (!ptx::mbar_try_wait_cluster(bar, parity)) {
         if (ptx::globaltimer() - t0 > w.limit_ns) {
             raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), SITE_DRAIN, parity);
             return;
@@ -118,42 +137,85 @@ __device__ __forceinline__ int expert_of(const Params<MAX_E>& p, int band)
     return p.band_expert[band];
 }
 
+// Arrive on the leader's copy of a barrier (a local arrive on the leader).
+__device__ __forceinline__ void arrive_on_leader(uint32_t bar, uint32_t rank)
+{
+    if (rank == 0)
+        ptx::mbar_arrive(bar);
+    else
+        ptx::mbar_arrive_cluster(ptx::mapa(bar, 0));
+}
+
+// Position in the task ring.
+struct Ring {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void advance()
+    {
+        if (++slot == TASK_SLOTS) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Read the next task from this CTA's ring and free the slot on the leader
+// (warp_wide: the whole warp waits, lane 0 arrives).  False on abort/timeout.
+__device__ __forceinline__ bool read_task(Aux& aux, const WaitCtx& w, Ring& r, uint32_t rank, bool warp_wide,
+                                          int lane, int4& task)
+{
+    if (!wait_mbar_cl(w, ptx::smem_u32(&aux.task_full[r.slot]), r.phase, SITE_TASK_FULL))
+        return false;
+    task = aux.task[r.slot];
+    if (warp_wide)
+        __syncwarp();
+    if (!warp_wide || lane == 0)
+        arrive_on_leader(ptx::smem_u32(&aux.task_empty[r.slot]), rank);
+    r.advance();
+    return true;
+}
+
 // ----------------------------------------------------------------- producer
 template <int MAX_E>
 __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const WaitCtx& w,
-                             int64_t m_blocks, int64_t total)
+                             int64_t m_blocks, int64_t total, uint32_t rank)
 {
     const int32_t n1 = p.layer[0].n_tiles;
     const int32_t n2 = p.layer[1].n_tiles;
-    uint32_t stage = 0, phase = 0, slot = 0, slot_phase = 0;
+    uint32_t stage = 0, phase = 0;
+    Ring ring;
     int32_t last_phase[STAGES];
     for (int s = 0; s < STAGES; ++s)
         last_phase[s] = -1;
 
     for (;;) {
-        const uint32_t t = atomicAdd(&p.ctrl->ticket, 1u);
-        EngineTask task = engine_task(static_cast<int64_t>(t), m_blocks, n1, n2, p.group_m, p.mode);
-        if (static_cast<int64_t>(t) >= total)
-            task.layer = -1;
-        if (!wait_mbar(w, ptx::smem_u32(&aux.task_empty[slot]), slot_phase ^ 1u, SITE_TASK_EMPTY))
+        int4 task;
+        if (rank == 0) {
+            const uint32_t t = atomicAdd(&p.ctrl->ticket, 1u);
+            EngineTask et = engine_task(static_cast<int64_t>(t), m_blocks, n1, n2, p.group_m, p.mode);
+            if (static_cast<int64_t>(t) >= total)
+                et.layer = -1;
+            task = make_int4(et.layer, et.band, et.tile, 0);
+            if (!wait_mbar_cl(w, ptx::smem_u32(&aux.task_empty[ring.slot]), ring.phase ^ 1u, SITE_TASK_EMPTY))
+                break;
+            aux.task[ring.slot] = task;
+            ptx::st_cluster_v4(ptx::mapa(ptx::smem_u32(&aux.task[ring.slot]), 1), task);
+            ptx::mbar_arrive(ptx::smem_u32(&aux.task_full[ring.slot]));
+            ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&aux.task_full[ring.slot]), 1));
+            ring.advance();
+        } else if (!read_task(aux, w, ring, rank, false, 0, task)) {
             break;
-        aux.task[slot] = make_int4(task.layer, task.band, task.tile, 0);
-        ptx::mbar_arrive(ptx::smem_u32(&aux.task_full[slot]));
-        if (++slot == TASK_SLOTS) {
-            slot = 0;
-            slot_phase ^= 1u;
         }
-        if (task.layer < 0)
+        if (task.x < 0)
             break;
 
-        const int L = task.layer;
+        const int L = task.x;
         const LayerArgs& la = p.layer[L];
-        const int e = expert_of(p, task.band);
+        const int e = expert_of(p, task.y);
         const CUtensorMap* ma = &p.map_a[L];
         const CUtensorMap* mb = &p.map_b[L][e];
         const int nk = (la.K + BK - 1) / BK;
-        const int32_t row0 = task.band * BM;
-        const int32_t col0 = task.tile * BN;
+        const int32_t row0 = task.y * BM + static_cast<int32_t>(rank) * BM_CTA;
+        const int32_t col0 = task.z * BN + static_cast<int32_t>(rank) * BN_CTA;
         const bool wait_h = (L == 1 && p.mode == MODE_FUSED);
         int last_h = -1;
         bool ok = true;
@@ -161,11 +223,12 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
             if (wait_h) {
                 const int j = (kb * BK) / BN;   // layer-1 tile holding this H chunk
                 if (j != last_h) {
-                    // the tile is ready once each of its four epilogue warps
-                    // has stamped its word with this call's epoch
-                    const uint32_t fi = static_cast<uint32_t>(task.band * n1 + j);
+                    // this CTA's 128 rows of the H tile were written by the
+                    // same-rank CTA of the producing pair: its four words
+                    const uint32_t fi = static_cast<uint32_t>(task.y * n1 + j);
+                    const uint32_t* f = p.flags + fi * FLAG_WORDS_PER_TILE + rank * EPI_WARPS;
                     for (int q = 0; q < EPI_WARPS && ok; ++q)
-                        ok = wait_flag(w, &p.flags[fi * EPI_WARPS + q], p.epoch, SITE_H_FLAG, fi);
+                        ok = wait_flag(w, f + q, p.epoch, SITE_H_FLAG, fi);
                     if (!ok)
                         break;
                     ptx::fence_proxy_async_global();
@@ -175,14 +238,16 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
             ok = wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY);
             if (!ok)
                 break;
-            const uint32_t fb = ptx::smem_u32(&aux.full[stage]);
-            ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const uint32_t fb_local = ptx::smem_u32(&aux.full[stage]);
+            const uint32_t fb = ptx::mapa(fb_local, 0);     // the leader's stage barrier
+            if (rank == 0)
+                ptx::mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
             const uint32_t sa = ptx::smem_u32(stages + stage * STAGE_BYTES);
             const uint32_t sb = sa + A_STAGE_BYTES;
-            ptx::tma_load_2d(sa, ma, fb, kb * BK, row0);
+            ptx::tma_load_2d_pair(sa, ma, fb, kb * BK, row0);
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-                ptx::tma_load_2d(sb + i * B_BOX_BYTES, mb, fb, col0 + i * 64, kb * BK);
+            for (int i = 0; i < BN_CTA / 64; ++i)
+                ptx::tma_load_2d_pair(sb + i * B_BOX_BYTES, mb, fb, col0 + i * 64, kb * BK);
             last_phase[stage] = static_cast<int32_t>(phase);
             if (++stage == STAGES) {
                 stage = 0;
@@ -192,34 +257,33 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
         if (!ok)
             break;
     }
-    // Exit: wait until every copy this thread issued has landed.
-    for (int s = 0; s < STAGES; ++s)
-        if (last_phase[s] >= 0)
-            wait_own(w, ptx::smem_u32(&aux.full[s]), static_cast<uint32_t>(last_phase[s]));
+    // Exit: every copy of the pair has landed (the leader's stage barriers
+    // count both CTAs' bytes; the peer cannot leave before the leader passes
+    // the final cluster barrier).
+    if (rank == 0)
+        for (int s = 0; s < STAGES; ++s)
+            if (last_phase[s] >= 0)
+                wait_own(w, ptx::smem_u32(&aux.full[s]), static_cast<uint32_t>(last_phase[s]));
 }
 
-// ---------------------------------------------------------------------- MMA
+// ------------------------------------------------------------- leader: MMA
 template <int MAX_E>
 __device__ void run_mma(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const WaitCtx& w,
                         uint32_t tmem_base)
 {
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, 0, 1);
-    uint32_t stage = 0, phase = 0, slot = 0, slot_phase = 0, iter = 0;
+    uint32_t stage = 0, phase = 0, iter = 0;
+    Ring ring;
     for (;;) {
-        if (!wait_mbar(w, ptx::smem_u32(&aux.task_full[slot]), slot_phase, SITE_TASK_FULL))
+        int4 task;
+        if (!read_task(aux, w, ring, 0, false, 0, task))
             break;
-        const int4 task = aux.task[slot];
-        ptx::mbar_arrive(ptx::smem_u32(&aux.task_empty[slot]));
-        if (++slot == TASK_SLOTS) {
-            slot = 0;
-            slot_phase ^= 1u;
-        }
         if (task.x < 0)
             break;
         const int nk = (p.layer[task.x].K + BK - 1) / BK;
         const uint32_t acc = iter & 1u;
         const uint32_t acc_phase = (iter >> 1) & 1u;
-        if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_empty[acc]), acc_phase ^ 1u, SITE_TMEM_EMPTY))
+        if (!wait_mbar_cl(w, ptx::smem_u32(&aux.tmem_empty[acc]), acc_phase ^ 1u, SITE_TMEM_EMPTY))
             break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -239,10 +303,10 @@ __device__ void run_mma(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const
             const uint64_t bdesc = ptx::sdesc_sw128(sb, B_BOX_BYTES, 1024);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
-                ptx::umma_bf16(d_tmem, adesc + static_cast<uint64_t>((k * 32) >> 4),
-                               bdesc + static_cast<uint64_t>((k * 2048) >> 4), idesc,
-                               (kb > 0 || k > 0) ? 1u : 0u);
-            ptx::umma_commit(ptx::smem_u32(&aux.empty[stage]));
+                ptx::umma_bf16_pair(d_tmem, adesc + static_cast<uint64_t>((k * 32) >> 4),
+                                    bdesc + static_cast<uint64_t>((k * 2048) >> 4), idesc,
+                                    (kb > 0 || k > 0) ? 1u : 0u);
+            ptx::umma_commit_pair_mc(ptx::smem_u32(&aux.empty[stage]), 0x3);
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -250,11 +314,11 @@ __device__ void run_mma(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const
         }
         if (!ok)
             break;
-        ptx::umma_commit(ptx::smem_u32(&aux.tmem_full[acc]));
+        ptx::umma_commit_pair_mc(ptx::smem_u32(&aux.tmem_full[acc]), 0x3);
         ++iter;
     }
     // Exit: wait until every MMA this thread issued has completed.
-    ptx::umma_commit(ptx::smem_u32(&aux.drain));
+    ptx::umma_commit_pair_mc(ptx::smem_u32(&aux.drain), 0x1);
     wait_own(w, ptx::smem_u32(&aux.drain), 0u);
 }
 
@@ -290,23 +354,17 @@ __device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int32_t c
 }
 
 template <int MAX_E>
-__device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
-                             uint32_t tmem_base, int warp, int lane)
+__device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w, uint32_t tmem_base,
+                             uint32_t rank, int warp, int lane)
 {
     const uint32_t quad = static_cast<uint32_t>(warp & 3);   // TMEM lanes [32*quad, 32*quad+32)
     const int32_t n1 = p.layer[0].n_tiles;
-    uint32_t slot = 0, slot_phase = 0, iter = 0;
+    uint32_t iter = 0;
+    Ring ring;
     for (;;) {
-        if (!wait_mbar(w, ptx::smem_u32(&aux.task_full[slot]), slot_phase, SITE_TASK_FULL))
+        int4 task;
+        if (!read_task(aux, w, ring, rank, true, lane, task))
             break;
-        const int4 task = aux.task[slot];
-        __syncwarp();
-        if (lane == 0)
-            ptx::mbar_arrive(ptx::smem_u32(&aux.task_empty[slot]));
-        if (++slot == TASK_SLOTS) {
-            slot = 0;
-            slot_phase ^= 1u;
-        }
         if (task.x < 0)
             break;
         const int L = task.x;
@@ -318,7 +376,7 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         ptx::tc_fence_after();
 
         const __nv_bfloat16* bias = p.bias[L][expert_of(p, task.y)];
-        const int64_t row = static_cast<int64_t>(task.y) * BM + quad * 32 + lane;
+        const int64_t row = static_cast<int64_t>(task.y) * BM + rank * BM_CTA + quad * 32 + lane;
         const bool row_ok = row < la.rows;
         const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * BN;
 #pragma unroll 1
@@ -356,14 +414,14 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
                 }
             }
         }
-        // Accumulator drained: hand it back to the MMA warp.
+        // Accumulator drained: hand it back to the leader's MMA thread.
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0)
-            ptx::mbar_arrive(ptx::smem_u32(&aux.tmem_empty[acc]));
+            arrive_on_leader(ptx::smem_u32(&aux.tmem_empty[acc]), rank);
         ++iter;
 
-        // Layer-1 tile: publish this warp's quarter of the H tile by stamping
+        // Layer-1 tile: publish this warp's 32 rows of the H tile by stamping
         // the warp's flag word with the call's epoch (release, gpu scope).
         if (L == 0 && p.mode == MODE_FUSED) {
             ptx::fence_proxy_async_global();
@@ -372,7 +430,7 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
                 const int32_t fi = task.y * n1 + task.z;
                 if (fi != p.skip_flag) {
                     __threadfence();
-                    ptx::st_release_gpu(&p.flags[fi * EPI_WARPS + quad], p.epoch);
+                    ptx::st_release_gpu(&p.flags[fi * FLAG_WORDS_PER_TILE + rank * EPI_WARPS + quad], p.epoch);
                 }
             }
         }
@@ -389,6 +447,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
     Aux& aux = *reinterpret_cast<Aux*>(stages + STAGES * STAGE_BYTES);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    const uint32_t rank = ptx::cluster_ctarank();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -397,11 +456,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_u32(&aux.tmem_full[a]), 1);
-            ptx::mbar_init(ptx::smem_u32(&aux.tmem_empty[a]), EPI_WARPS);
+            ptx::mbar_init(ptx::smem_u32(&aux.tmem_empty[a]), 2 * EPI_WARPS);
         }
         for (int s = 0; s < TASK_SLOTS; ++s) {
             ptx::mbar_init(ptx::smem_u32(&aux.task_full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&aux.task_empty[s]), 1 + EPI_WARPS);
+            ptx::mbar_init(ptx::smem_u32(&aux.task_empty[s]), TASK_CONSUMERS);
         }
         ptx::mbar_init(ptx::smem_u32(&aux.drain), 1);
         aux.abort = 0u;
@@ -412,33 +471,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
         ptx::prefetch_tmap(&p.map_a[1]);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(&aux.tmem_base), TMEM_COLS);
-        ptx::tmem_relinquish();
+        // one collective allocation per CTA pair: both CTAs' warp 1 take part
+        ptx::tmem_alloc_pair(ptx::smem_u32(&aux.tmem_base), TMEM_COLS);
+        ptx::tmem_relinquish_pair();
     }
     ptx::tc_fence_before();
     __syncthreads();
+    ptx::cluster_sync();   // both CTAs' barriers exist before any remote arrive
     ptx::tc_fence_after();
     const uint32_t tmem_base = aux.tmem_base;
 
-    const WaitCtx w{&aux.abort, p.ctrl, p.wait_limit_ns};
+    const WaitCtx w{&aux.abort, p.ctrl, p.wait_limit_ns, ptx::mapa(ptx::smem_u32(&aux.abort), rank ^ 1u)};
     const int64_t m_blocks = p.m_blocks >= 0 ? p.m_blocks : static_cast<int64_t>(*p.m_blocks_dev);
     const int64_t total = engine_total_tickets(m_blocks, p.layer[0].n_tiles, p.layer[1].n_tiles, p.mode);
 
     if (warp == 0) {
         if (lane == 0)
-            run_producer(p, aux, stages, w, m_blocks, total);
+            run_producer(p, aux, stages, w, m_blocks, total, rank);
     } else if (warp == 1) {
-        if (lane == 0)
+        if (lane == 0 && rank == 0)
             run_mma(p, aux, stages, w, tmem_base);
     } else {
-        run_epilogue(p, aux, w, tmem_base, warp, lane);
+        run_epilogue(p, aux, w, tmem_base, rank, warp, lane);
     }
     __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
+    // The leader's MMAs read the peer's shared memory: neither CTA leaves (or
+    // frees its tensor memory) before both are done.
+    ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
     if (threadIdx.x == 0) {
         // The last CTA out resets the ticket counter for the next launch.

@@ -17,8 +17,10 @@ struct Params;
 
 constexpr int MOE_MAX_E = 64;
 
-int launch_engine_dense(const engine::Params<1>& p, int grid, cudaStream_t s);
-int launch_engine_grouped(const engine::Params<MOE_MAX_E>& p, int grid, cudaStream_t s);
+// The engine launches clusters of two CTAs; max_pairs caps the number of CTA
+// pairs (further capped by how many pairs can be resident at once).
+int launch_engine_dense(const engine::Params<1>& p, int max_pairs, cudaStream_t s);
+int launch_engine_grouped(const engine::Params<MOE_MAX_E>& p, int max_pairs, cudaStream_t s);
 int launch_decode(const decode::Params& p, int grid, cudaStream_t s);
 
 int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w,
