@@ -174,6 +174,51 @@ __device__ __forceinline__ bool read_task(Aux& aux, const WaitCtx& w, Ring& r, u
     return true;
 }
 
+// Layer-2 producer: make sure H chunk j of the band is published, polling a
+// window of up to H_WINDOW chunks at once (relaxed loads of this CTA's four
+// words per chunk, independent so they overlap), then one acquire fence and
+// one proxy fence.  Advances ready_upto past every chunk found ready.
+constexpr int H_WINDOW = 8;
+
+static __device__ __noinline__ bool wait_h_chunks(const WaitCtx& w, const uint32_t* band_flags, uint32_t epoch, int j,
+                                           int n1, int& ready_upto, uint32_t info)
+{
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        const int end = j + H_WINDOW < n1 ? j + H_WINDOW : n1;
+        int upto = j;
+        bool gap = false;
+        for (int c = j; c < end; ++c) {
+            const uint32_t* f = band_flags + c * FLAG_WORDS_PER_TILE;
+            uint32_t v[EPI_WARPS];
+#pragma unroll
+            for (int q = 0; q < EPI_WARPS; ++q)
+                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v[q]) : "l"(f + q) : "memory");
+            bool all = true;
+#pragma unroll
+            for (int q = 0; q < EPI_WARPS; ++q)
+                all = all && (v[q] == epoch);
+            if (!gap && all)
+                upto = c + 1;
+            else
+                gap = true;
+        }
+        if (upto > j) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            ptx::fence_proxy_async_global();
+            ready_upto = upto;
+            return true;
+        }
+        if (*w.abort)
+            return false;
+        if (ptx::globaltimer() - t0 > w.limit_ns) {
+            raise_error(w, static_cast<uint32_t>(TFFN_ERR_TIMEOUT), SITE_H_FLAG, info);
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
 // ----------------------------------------------------------------- producer
 template <int MAX_E>
 __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const WaitCtx& w,
@@ -217,23 +262,18 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
         const int32_t row0 = task.y * BM + static_cast<int32_t>(rank) * BM_CTA;
         const int32_t col0 = task.z * BN + static_cast<int32_t>(rank) * BN_CTA;
         const bool wait_h = (L == 1 && p.mode == MODE_FUSED);
-        int last_h = -1;
+        // H chunks [0, ready_upto) of this band are known to be published
+        int ready_upto = wait_h ? 0 : n1;
+        const uint32_t* band_flags =
+            p.flags + static_cast<uint32_t>(task.y * n1) * FLAG_WORDS_PER_TILE + rank * EPI_WARPS;
         bool ok = true;
         for (int kb = 0; kb < nk && ok; ++kb) {
-            if (wait_h) {
-                const int j = (kb * BK) / BN;   // layer-1 tile holding this H chunk
-                if (j != last_h) {
-                    // this CTA's 128 rows of the H tile were written by the
-                    // same-rank CTA of the producing pair: its four words
-                    const uint32_t fi = static_cast<uint32_t>(task.y * n1 + j);
-                    const uint32_t* f = p.flags + fi * FLAG_WORDS_PER_TILE + rank * EPI_WARPS;
-                    for (int q = 0; q < EPI_WARPS && ok; ++q)
-                        ok = wait_flag(w, f + q, p.epoch, SITE_H_FLAG, fi);
-                    if (!ok)
-                        break;
-                    ptx::fence_proxy_async_global();
-                    last_h = j;
-                }
+            const int j = (kb * BK) / BN;   // layer-1 tile holding this H chunk
+            if (j >= ready_upto) {
+                ok = wait_h_chunks(w, band_flags, p.epoch, j, n1, ready_upto,
+                                   static_cast<uint32_t>(task.y * n1 + j));
+                if (!ok)
+                    break;
             }
             ok = wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY);
             if (!ok)
