@@ -179,7 +179,7 @@ const char* tffn_status_string(int status);
  *                         the ready flag of this GEMM1 tile index (-1 = off);
  *                         the waiting GEMM2 tile then times out and the call
  *                         reports TFFN_ERR_TIMEOUT through tffn_check()
- *   TFFN_OPT_GROUP_M      row bands per raster group of the engine (default 8)
+ *   TFFN_OPT_GROUP_M      row bands per raster group of the engine (default 4)
  * Returns the previous value. */
 enum {
     TFFN_OPT_PATH = 1,

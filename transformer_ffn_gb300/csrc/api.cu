@@ -59,7 +59,7 @@ DeviceState g_dev[64];
 std::atomic<int64_t> g_opt_path{0};
 std::atomic<int64_t> g_opt_wait_ms{4000};
 std::atomic<int64_t> g_opt_skip{-1};
-std::atomic<int64_t> g_opt_group{8};
+std::atomic<int64_t> g_opt_group{4};
 
 thread_local int g_last_launches = 0;
 thread_local bool g_timing = false;
@@ -99,6 +99,28 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+// W [K x ncols] row-major bf16 seen as {64 columns, K rows, ncols/64 column
+// blocks}, box {64, 64, 2}: one copy brings a 64-deep, 128-column slab in the
+// same shared-memory layout as two 2-D {64, 64} boxes.  Only for ncols % 64 == 0
+// (a partial last block would reach past the end of the matrix).
+int make_map_b3(CUtensorMap* m, const void* base, uint64_t ncols, uint64_t K)
+{
+    cuuint64_t dims[3] = {64, K, ncols / 64};
+    cuuint64_t strides[2] = {ncols * 2, 128};
+    cuuint32_t box[3] = {64, 64, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+int make_map_b(CUtensorMap* m, const void* base, int64_t ncols, int64_t K, bool b3d)
+{
+    return b3d ? make_map_b3(m, base, static_cast<uint64_t>(ncols), static_cast<uint64_t>(K))
+               : make_map(m, base, static_cast<uint64_t>(ncols), static_cast<uint64_t>(K), 64, 64);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -363,9 +385,11 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
     std::memset(&p, 0, sizeof(p));
     void* H = base + L.off_h;
     const int64_t rows_h = L.m_blocks * engine::BM;
+    const bool b3d = (O % 64 == 0) && (P % 64 == 0);
     if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) || make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) ||
-        make_map(&p.map_b[0][0], W1, O, N, 64, engine::BK) || make_map(&p.map_b[1][0], W2, P, O, 64, engine::BK))
+        make_map_b(&p.map_b[0][0], W1, O, N, b3d) || make_map_b(&p.map_b[1][0], W2, P, O, b3d))
         return TFFN_ERR_INVALID_ARG;
+    p.b3d = b3d ? 1 : 0;
     p.bias[0][0] = static_cast<const __nv_bfloat16*>(b1);
     p.bias[1][0] = static_cast<const __nv_bfloat16*>(b2);
     fill_layer<1>(p.layer[0], N, O, act1, 0, rows_h, H);
@@ -469,9 +493,11 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     engine::Params<MOE_MAX_E>& p = *pp;
     int bad = make_map(&p.map_a[0], Xp, N, L.Rmax, 64, engine::BM_CTA) |
               make_map(&p.map_a[1], H, O, L.Rmax, 64, engine::BM_CTA);
+    const bool b3d = (O % 64 == 0) && (P % 64 == 0);
+    p.b3d = b3d ? 1 : 0;
     for (int e = 0; e < E && !bad; ++e) {
-        bad |= make_map(&p.map_b[0][e], W1[e], O, N, 64, engine::BK);
-        bad |= make_map(&p.map_b[1][e], W2[e], P, O, 64, engine::BK);
+        bad |= make_map_b(&p.map_b[0][e], W1[e], O, N, b3d);
+        bad |= make_map_b(&p.map_b[1][e], W2[e], P, O, b3d);
         p.bias[0][e] = b1 ? static_cast<const __nv_bfloat16*>(b1[e]) : nullptr;
         p.bias[1][e] = b2 ? static_cast<const __nv_bfloat16*>(b2[e]) : nullptr;
     }

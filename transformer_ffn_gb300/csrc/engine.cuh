@@ -18,12 +18,17 @@
 // therefore streams only half of the B tile: 32 KiB per 64-deep k-stage per
 // SM, six stages deep.
 //
-// CTA layout (192 threads, one CTA per SM, two CTAs per cluster):
-//   warp 0      TMA producer.  The leader (cluster rank 0) takes tickets and
-//               publishes each task to both CTAs' task rings; both producers
-//               stream their own A rows and B columns into their own ring and
-//               count the bytes on the leader's stage barrier (cta_group::2
-//               copies), so the leader sees one barrier per stage for the pair.
+// CTA layout (224 threads, one CTA per SM, two CTAs per cluster):
+//   warp 0      A loader.  The leader (cluster rank 0) takes tickets and
+//               publishes each task to both CTAs' task rings; each A loader
+//               streams its CTA's A rows (and, for layer 2, waits on the H
+//               flags first).
+//   warp 6      B loader: streams the CTA's B columns, one TMA copy per stage
+//               (a 3-D map covers both 64-column halves).  A and B copies are
+//               issued by different warps because one warp issues bulk copies
+//               one after the other; the B loader needs no flags and runs
+//               ahead freely.  Every copy of the pair counts its bytes on the
+//               leader's stage barrier (cta_group::2 copies).
 //   warp 1      leader: issues the pair MMAs from one thread and commits
 //               them to both CTAs' barriers (multicast).  Both CTAs: own the
 //               CTA's tensor memory (512 columns = two accumulators of 128
@@ -59,15 +64,17 @@ constexpr int B_BOX_BYTES = 64 * BK * 2;                  // 8 KiB: 64 cols x 64
 constexpr int B_STAGE_BYTES = BK * BN_CTA * 2;            // 16 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TASK_SLOTS = 4;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;
+constexpr int B_LOADER_WARP = 6;
 constexpr int EPI_WARPS = 4;
 constexpr int FLAG_WORDS_PER_TILE = 2 * EPI_WARPS;        // one per epilogue warp of the pair
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int AUX_BYTES = 1024;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + 1024;   // + alignment slack
 // Arrivals that free a task slot (counted on the leader): leader MMA thread,
-// leader epilogue warps, peer producer, peer epilogue warps.
-constexpr uint32_t TASK_CONSUMERS = 1 + EPI_WARPS + 1 + EPI_WARPS;
+// leader B loader, leader epilogue warps, peer A loader, peer B loader, peer
+// epilogue warps.
+constexpr uint32_t TASK_CONSUMERS = 1 + 1 + EPI_WARPS + 1 + 1 + EPI_WARPS;
 
 // Per-layer arguments.
 struct LayerArgs {
@@ -85,7 +92,7 @@ struct LayerArgs {
 template <int MAX_E>
 struct Params {
     CUtensorMap map_a[2];                      // layer-1 A (X), layer-2 A (H); box {64, 128}
-    CUtensorMap map_b[2][MAX_E];               // W1[e], W2[e]; box {64, 64}
+    CUtensorMap map_b[2][MAX_E];               // W1[e], W2[e]; b3d: {64, 64, 2} else {64, 64}
     const __nv_bfloat16* bias[2][MAX_E];       // b1[e], b2[e] (nullable)
     LayerArgs layer[2];
     int64_t m_blocks;                          // 256-row bands; < 0: read *m_blocks_dev
@@ -98,6 +105,7 @@ struct Params {
     int32_t mode;                              // EngineMode
     int32_t group_m;
     int32_t skip_flag;                         // test fault injection, -1 = off
+    int32_t b3d;                               // 1: map_b are 3-D {64 cols, K, cols/64} maps
 };
 
 // Everything in shared memory besides the stage ring (same offsets in both
@@ -255,12 +263,9 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
 
         const int L = task.x;
         const LayerArgs& la = p.layer[L];
-        const int e = expert_of(p, task.y);
         const CUtensorMap* ma = &p.map_a[L];
-        const CUtensorMap* mb = &p.map_b[L][e];
         const int nk = (la.K + BK - 1) / BK;
         const int32_t row0 = task.y * BM + static_cast<int32_t>(rank) * BM_CTA;
-        const int32_t col0 = task.z * BN + static_cast<int32_t>(rank) * BN_CTA;
         const bool wait_h = (L == 1 && p.mode == MODE_FUSED);
         // H chunks [0, ready_upto) of this band are known to be published
         int ready_upto = wait_h ? 0 : n1;
@@ -283,11 +288,7 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
             if (rank == 0)
                 ptx::mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
             const uint32_t sa = ptx::smem_u32(stages + stage * STAGE_BYTES);
-            const uint32_t sb = sa + A_STAGE_BYTES;
             ptx::tma_load_2d_pair(sa, ma, fb, kb * BK, row0);
-#pragma unroll
-            for (int i = 0; i < BN_CTA / 64; ++i)
-                ptx::tma_load_2d_pair(sb + i * B_BOX_BYTES, mb, fb, col0 + i * 64, kb * BK);
             last_phase[stage] = static_cast<int32_t>(phase);
             if (++stage == STAGES) {
                 stage = 0;
@@ -304,6 +305,42 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
         for (int s = 0; s < STAGES; ++s)
             if (last_phase[s] >= 0)
                 wait_own(w, ptx::smem_u32(&aux.full[s]), static_cast<uint32_t>(last_phase[s]));
+}
+
+// ---------------------------------------------------------------- B loader
+template <int MAX_E>
+__device__ void run_b_loader(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const WaitCtx& w, uint32_t rank)
+{
+    uint32_t stage = 0, phase = 0;
+    Ring ring;
+    for (;;) {
+        int4 task;
+        if (!read_task(aux, w, ring, rank, false, 0, task))
+            break;
+        if (task.x < 0)
+            break;
+        const int L = task.x;
+        const CUtensorMap* mb = &p.map_b[L][expert_of(p, task.y)];
+        const int nk = (p.layer[L].K + BK - 1) / BK;
+        const int32_t col0 = task.z * BN + static_cast<int32_t>(rank) * BN_CTA;
+        for (int kb = 0; kb < nk; ++kb) {
+            if (!wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY))
+                return;
+            const uint32_t fb = ptx::mapa(ptx::smem_u32(&aux.full[stage]), 0);   // the leader's barrier
+            const uint32_t sb = ptx::smem_u32(stages + stage * STAGE_BYTES) + A_STAGE_BYTES;
+            if (p.b3d) {
+                ptx::tma_load_3d_pair(sb, mb, fb, 0, kb * BK, col0 / 64);
+            } else {
+#pragma unroll
+                for (int i = 0; i < BN_CTA / 64; ++i)
+                    ptx::tma_load_2d_pair(sb + i * B_BOX_BYTES, mb, fb, col0 + i * 64, kb * BK);
+            }
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------- leader: MMA
@@ -509,6 +546,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&p.map_a[0]);
         ptx::prefetch_tmap(&p.map_a[1]);
+        if (MAX_E == 1) {
+            ptx::prefetch_tmap(&p.map_b[0][0]);
+            ptx::prefetch_tmap(&p.map_b[1][0]);
+        }
     }
     if (warp == 1) {
         // one collective allocation per CTA pair: both CTAs' warp 1 take part
@@ -528,10 +569,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
     if (warp == 0) {
         if (lane == 0)
             run_producer(p, aux, stages, w, m_blocks, total, rank);
+    } else if (warp == B_LOADER_WARP) {
+        if (lane == 0)
+            run_b_loader(p, aux, stages, w, rank);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0)
             run_mma(p, aux, stages, w, tmem_base);
-    } else {
+    } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
         run_epilogue(p, aux, w, tmem_base, rank, warp, lane);
     }
     __syncwarp();
