@@ -27,15 +27,16 @@ using namespace tffn;
 // [.., + 256 KiB)          decode split-K arrival counters
 // [SYNC_BYTES, ...)        data: H, grouped rows, partial sums
 // The sync region is zeroed when a workspace is (re)initialised; after that,
-// flags are compared against a per-call epoch and counters are reset by the
-// kernels, so no per-call clearing is needed.
+// flags are compared against the epoch kept in the control block (advanced by
+// every launch on the device, so CUDA-graph replays stay correct) and counters
+// are reset by the kernels: no per-call clearing is needed.
 constexpr size_t OFF_FLAGS = 256;
 constexpr size_t FLAG_WORDS = size_t(1) << 20;
 constexpr size_t OFF_DCOUNT = OFF_FLAGS + FLAG_WORDS * 4;
 constexpr size_t DCOUNT_WORDS = size_t(1) << 16;
 constexpr size_t SYNC_BYTES = size_t(5) << 20;
 static_assert(OFF_DCOUNT + DCOUNT_WORDS * 4 <= SYNC_BYTES, "sync region layout");
-constexpr uint32_t EPOCH_LIMIT = 0xFFFFFFF0u;      // flag words hold the epoch of their last write
+constexpr uint32_t EPOCH_LIMIT = 0x7FFFFFF0u;      // launches before the flag region is cleared
 
 constexpr int64_t DECODE_MAX_M = 32;
 
@@ -50,7 +51,7 @@ struct DeviceState {
     size_t user_bytes = 0;
     bool user_set = false;
     bool needs_reset = true;
-    uint32_t epoch = 0;
+    uint32_t launches = 0;   // flag-using launches since the flag region was cleared
 };
 
 std::mutex g_mu;
@@ -174,22 +175,24 @@ int workspace(DeviceState& d, size_t need, cudaStream_t s, uint8_t** base)
     if (d.needs_reset) {
         if (cudaMemsetAsync(b, 0, SYNC_BYTES, s) != cudaSuccess)
             return TFFN_ERR_CUDA;
-        d.epoch = 0;
+        d.launches = 0;
         d.needs_reset = false;
     }
     *base = static_cast<uint8_t*>(b);
     return TFFN_OK;
 }
 
-// Epoch for the next launch that uses ready flags.
-int next_epoch(DeviceState& d, uint8_t* base, cudaStream_t s, uint32_t* epoch)
+// Ready flags hold the epoch of the launch that stamped them, and the epoch
+// lives in the control block (each launch uses the stored value + 1).  The
+// host only counts launches so that, long before the 32-bit epoch could wrap,
+// the flag region is cleared again.
+int count_launch(DeviceState& d, uint8_t* base, cudaStream_t s)
 {
-    if (d.epoch >= EPOCH_LIMIT) {
-        if (cudaMemsetAsync(base + OFF_FLAGS, 0, FLAG_WORDS * 4, s) != cudaSuccess)
+    if (++d.launches >= EPOCH_LIMIT) {
+        if (cudaMemsetAsync(base, 0, SYNC_BYTES, s) != cudaSuccess)
             return TFFN_ERR_CUDA;
-        d.epoch = 0;
+        d.launches = 1;
     }
-    *epoch = ++d.epoch;
     return TFFN_OK;
 }
 
@@ -342,8 +345,7 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
     uint32_t* flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
 
     if (L.path == 2) {
-        uint32_t epoch = 0;
-        if ((rc = next_epoch(*d, base, s, &epoch)) != TFFN_OK)
+        if ((rc = count_launch(*d, base, s)) != TFFN_OK)
             return rc;
         decode::Params p{};
         p.X = static_cast<const __nv_bfloat16*>(X);
@@ -363,7 +365,6 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
         p.P = static_cast<int32_t>(P);
         p.act1 = act1;
         p.act2 = act2;
-        p.epoch = epoch;
         p.wait_limit_ns = wait_limit_ns();
         p.plan = decode::make_plan(M, N, O, P, d->sms);
         if (static_cast<size_t>(p.plan.slices[0]) * 4 > FLAG_WORDS ||
@@ -404,10 +405,8 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
     p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
 
     if (L.path == 1) {
-        uint32_t epoch = 0;
-        if ((rc = next_epoch(*d, base, s, &epoch)) != TFFN_OK)
+        if ((rc = count_launch(*d, base, s)) != TFFN_OK)
             return rc;
-        p.epoch = epoch;
         p.mode = MODE_FUSED;
         const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, MODE_FUSED);
         const int pairs = static_cast<int>(total < d->sms ? total : d->sms);
@@ -421,7 +420,6 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
     // two launches: layer 1, then layer 2
     for (int mode = MODE_LAYER1; mode <= MODE_LAYER2; ++mode) {
         p.mode = mode;
-        p.epoch = 0;
         const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, mode);
         const int pairs = static_cast<int>(total < d->sms ? total : d->sms);
         if (mode == MODE_LAYER1)
@@ -474,8 +472,7 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     rc = workspace(*d, L.total, s, &base);
     if (rc != TFFN_OK)
         return rc;
-    uint32_t epoch = 0;
-    if ((rc = next_epoch(*d, base, s, &epoch)) != TFFN_OK)
+    if ((rc = count_launch(*d, base, s)) != TFFN_OK)
         return rc;
 
     int32_t* idx = reinterpret_cast<int32_t*>(base + L.off_idx);
@@ -513,7 +510,6 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
     p.ctrl = reinterpret_cast<DevCtrl*>(base);
     p.wait_limit_ns = wait_limit_ns();
-    p.epoch = epoch;
     p.mode = MODE_FUSED;
     p.group_m = static_cast<int32_t>(g_opt_group.load() < 1 ? 1 : g_opt_group.load());
     p.skip_flag = static_cast<int32_t>(g_opt_skip.load());

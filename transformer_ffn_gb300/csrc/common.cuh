@@ -37,7 +37,8 @@ struct DevCtrl {
     uint32_t info;        // site-specific detail (tile / slice index)
     uint32_t ticket;      // engine: next task ticket
     uint32_t done;        // engine: CTAs that have exited
-    uint32_t dticket;     // decode: unused for now
+    uint32_t epoch;       // ready-flag value of the most recent launch; each launch
+                          // stamps and expects epoch + 1 and the last CTA out stores it
     uint32_t ddone;       // decode: CTAs that have exited
     uint32_t pad[56];
 };

@@ -14,6 +14,7 @@ struct Aux {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint32_t abort;
+    uint32_t epoch;     // this launch's ready-flag value (control block's + 1)
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
@@ -113,7 +114,7 @@ __device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uin
 // owns the whole K range, else store the partial and let the last arriver sum
 // the parts in part order.
 template <int MT>
-__device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, int cw, int lane)
+__device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, int cw, int lane, uint32_t epoch)
 {
     const Plan& pl = p.plan;
     const int64_t U = pl.units[layer], G = pl.grid, kch = pl.kch[layer];
@@ -208,7 +209,7 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
         __syncwarp();
         if (lane == 0) {
             __threadfence();
-            ptx::st_release_gpu(p.flags + slice * CONSUMER_WARPS + cw, p.epoch);
+            ptx::st_release_gpu(p.flags + slice * CONSUMER_WARPS + cw, epoch);
         }
     }
 }
@@ -329,7 +330,7 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
         const int npre_done = __shfl_sync(0xffffffffu, ok ? static_cast<int>(npre) : -1, 0);
         if (npre_done >= 0) {
             const int64_t count = (u1 - u0) < kch ? (u1 - u0) : kch;
-            const bool ready = wait_h_window(w, p.flags, p.epoch, u0 % kch, count, kch, lane);
+            const bool ready = wait_h_window(w, p.flags, aux.epoch, u0 % kch, count, kch, lane);
             if (lane == 0) {
                 ptx::fence_proxy_async_global();
                 // the prefetched stages expect their H bytes: issue them even
@@ -386,6 +387,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
             ptx::mbar_init(ptx::smem_u32(&aux.empty[s]), CONSUMER_WARPS);
         }
         aux.abort = 0u;
+        // device-side epoch: every CTA reads it before any can finish
+        aux.epoch = *reinterpret_cast<volatile uint32_t*>(&p.ctrl->epoch) + 1u;
         ptx::fence_barrier_init();
     }
     __syncthreads();
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
                 const int64_t slice = u / kch;
                 if (slice != cur) {
                     if (cur >= 0)
-                        flush<MT>(p, layer, cur, acc, cw, lane);
+                        flush<MT>(p, layer, cur, acc, cw, lane, aux.epoch);
                     zero(acc);
                     cur = slice;
                 }
@@ -424,11 +427,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
                 }
             }
             if (ok && cur >= 0)
-                flush<MT>(p, layer, cur, acc, cw, lane);
+                flush<MT>(p, layer, cur, acc, cw, lane, aux.epoch);
         }
     }
     __syncwarp();
     __syncthreads();
+    if (threadIdx.x == 0) {
+        // The last CTA out publishes this launch's epoch.
+        __threadfence();
+        if (atomicAdd(&p.ctrl->ddone, 1u) == gridDim.x - 1) {
+            p.ctrl->ddone = 0u;
+            p.ctrl->epoch = aux.epoch;
+            __threadfence();
+        }
+    }
 }
 
 }  // namespace decode

@@ -118,7 +118,6 @@ struct Params {
     DevCtrl* ctrl;
     int32_t M, N, O, P;
     int32_t act1, act2;
-    uint32_t epoch;
     uint64_t wait_limit_ns;
     Plan plan;
 };

@@ -70,7 +70,8 @@ constexpr int EPI_WARPS = 4;
 constexpr int FLAG_WORDS_PER_TILE = 2 * EPI_WARPS;        // one per epilogue warp of the pair
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int AUX_BYTES = 1024;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + 1024;   // + alignment slack
+constexpr int BIAS_BYTES = EPI_WARPS * BN * 4;             // each epilogue warp's fp32 bias slice
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + BIAS_BYTES + 1024;   // + alignment slack
 // Arrivals that free a task slot (counted on the leader): leader MMA thread,
 // leader B loader, leader epilogue warps, peer A loader, peer B loader, peer
 // epilogue warps.
@@ -101,7 +102,6 @@ struct Params {
     uint32_t* flags;                           // [m_blocks * n1 * 8] ready words
     DevCtrl* ctrl;
     uint64_t wait_limit_ns;
-    uint32_t epoch;                            // value of a ready flag word in this call
     int32_t mode;                              // EngineMode
     int32_t group_m;
     int32_t skip_flag;                         // test fault injection, -1 = off
@@ -121,6 +121,7 @@ struct Aux {
     int4 task[TASK_SLOTS];
     uint32_t tmem_base;
     uint32_t abort;
+    uint32_t epoch;                 // this launch's ready-flag value (control block's + 1)
 };
 static_assert(sizeof(Aux) <= AUX_BYTES, "aux block fits");
 
@@ -275,7 +276,7 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
         for (int kb = 0; kb < nk && ok; ++kb) {
             const int j = (kb * BK) / BN;   // layer-1 tile holding this H chunk
             if (j >= ready_upto) {
-                ok = wait_h_chunks(w, band_flags, p.epoch, j, n1, ready_upto,
+                ok = wait_h_chunks(w, band_flags, aux.epoch, j, n1, ready_upto,
                                    static_cast<uint32_t>(task.y * n1 + j));
                 if (!ok)
                     break;
@@ -400,39 +401,94 @@ __device__ void run_mma(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const
 }
 
 // ----------------------------------------------------------------- epilogue
-__device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int32_t col, int32_t ncols,
-                                            float (&b)[32])
+// The tile's 256 bias values, fetched by one warp into its own shared buffer
+// (fp32, zeros outside the matrix and for a NULL bias).  Issued before the
+// epilogue waits for its accumulator, so the global-memory latency overlaps
+// the tile's main loop instead of sitting in front of every column chunk.
+__device__ __forceinline__ void fetch_bias_slice(const __nv_bfloat16* bias, int32_t col0, int32_t ncols,
+                                                 float* slice, int lane)
 {
-    if (bias == nullptr) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            b[i] = 0.0f;
-        return;
-    }
-    if (col + 32 <= ncols) {
-        const uint4* src = reinterpret_cast<const uint4*>(bias + col);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 v = __ldg(src + q);
-            b[q * 8 + 0] = bf16_lo(v.x);
-            b[q * 8 + 1] = bf16_hi(v.x);
-            b[q * 8 + 2] = bf16_lo(v.y);
-            b[q * 8 + 3] = bf16_hi(v.y);
-            b[q * 8 + 4] = bf16_lo(v.z);
-            b[q * 8 + 5] = bf16_hi(v.z);
-            b[q * 8 + 6] = bf16_lo(v.w);
-            b[q * 8 + 7] = bf16_hi(v.w);
-        }
+    const int32_t c = col0 + lane * 8;   // 32 lanes x 8 columns = BN
+    float v[8];
+    if (bias != nullptr && c + 8 <= ncols) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(bias + c));
+        v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+        v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            b[i] = (col + i < ncols) ? __bfloat162float(bias[col + i]) : 0.0f;
+        for (int i = 0; i < 8; ++i)
+            v[i] = (bias != nullptr && c + i < ncols) ? __bfloat162float(bias[c + i]) : 0.0f;
+    }
+    float4* dst = reinterpret_cast<float4*>(slice + lane * 8);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Bias, activation, rounding and the row's store for one 32-column chunk.
+// The activation is a template argument, chosen once per tile.
+template <int ACT>
+__device__ __forceinline__ void store_chunk(const uint32_t (&acc)[32], uint32_t bias_smem, bool row_ok, void* out,
+                                            bool out_f32, int64_t row, int64_t ld_out, int32_t col, int32_t ncols)
+{
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float4 b;   // the same address in every lane: a broadcast
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(b.x), "=f"(b.y), "=f"(b.z), "=f"(b.w)
+                     : "r"(bias_smem + q * 16));
+        v[q * 4 + 0] = act_apply(ACT, __uint_as_float(acc[q * 4 + 0]) + b.x);
+        v[q * 4 + 1] = act_apply(ACT, __uint_as_float(acc[q * 4 + 1]) + b.y);
+        v[q * 4 + 2] = act_apply(ACT, __uint_as_float(acc[q * 4 + 2]) + b.z);
+        v[q * 4 + 3] = act_apply(ACT, __uint_as_float(acc[q * 4 + 3]) + b.w);
+    }
+    if (!row_ok)
+        return;
+    const int nvalid = ncols - col < 32 ? ncols - col : 32;   // multiple of 8
+    if (out_f32) {
+        float* dst = static_cast<float*>(out) + row * ld_out + col;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q * 4 < nvalid)
+                reinterpret_cast<float4*>(dst)[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    } else {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + row * ld_out + col;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (q * 8 < nvalid)
+                reinterpret_cast<uint4*>(dst)[q] =
+                    make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                               pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+    }
+}
+
+// Drain one 128 x BN accumulator quadrant-row by quadrant-row: chunk c+1's
+// TMEM load is in flight while chunk c is computed and stored.
+template <int ACT>
+__device__ __forceinline__ void drain_tile(uint32_t taddr, int nchunks, uint32_t bias_smem, bool row_ok, void* out,
+                                           bool out_f32, int64_t row, int64_t ld_out, int32_t col_base, int32_t ncols)
+{
+    uint32_t ra[32], rb[32];
+    __syncwarp();
+    ptx::tmem_ld_32x32b_x32(taddr, ra);
+    for (int c = 0; c < nchunks; c += 2) {
+        ptx::tmem_ld_wait();
+        if (c + 1 < nchunks)
+            ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, rb);
+        store_chunk<ACT>(ra, bias_smem + c * 128, row_ok, out, out_f32, row, ld_out, col_base + c * 32, ncols);
+        if (c + 1 < nchunks) {
+            ptx::tmem_ld_wait();
+            if (c + 2 < nchunks)
+                ptx::tmem_ld_32x32b_x32(taddr + (c + 2) * 32, ra);
+            store_chunk<ACT>(rb, bias_smem + (c + 1) * 128, row_ok, out, out_f32, row, ld_out,
+                             col_base + (c + 1) * 32, ncols);
+        }
     }
 }
 
 template <int MAX_E>
 __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w, uint32_t tmem_base,
-                             uint32_t rank, int warp, int lane)
+                             uint32_t rank, int warp, int lane, float* bias_slice)
 {
     const uint32_t quad = static_cast<uint32_t>(warp & 3);   // TMEM lanes [32*quad, 32*quad+32)
     const int32_t n1 = p.layer[0].n_tiles;
@@ -448,49 +504,32 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         const LayerArgs& la = p.layer[L];
         const uint32_t acc = iter & 1u;
         const uint32_t acc_phase = (iter >> 1) & 1u;
+        __syncwarp();   // the previous tile's reads of the slice are done
+        fetch_bias_slice(p.bias[L][expert_of(p, task.y)], task.z * BN, la.ncols, bias_slice, lane);
         if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_full[acc]), acc_phase, SITE_TMEM_FULL))
             break;
         ptx::tc_fence_after();
-
-        const __nv_bfloat16* bias = p.bias[L][expert_of(p, task.y)];
+        __syncwarp();   // every lane's part of the slice is in shared memory
+        // The layer's fields in registers: the TMEM loads below are volatile
+        // asm with a memory clobber, which would otherwise force every field
+        // to be re-read from the parameter block in every chunk.
+        const int32_t ncols = la.ncols;
+        const int act = la.act;
+        const bool out_f32 = la.out_f32 != 0;
+        const int64_t ld_out = la.ld_out;
+        void* const out = la.out;
         const int64_t row = static_cast<int64_t>(task.y) * BM + rank * BM_CTA + quad * 32 + lane;
         const bool row_ok = row < la.rows;
+        const int32_t col_base = task.z * BN;
+        const int nchunks = ncols - col_base >= BN ? BN / 32 : (ncols - col_base + 31) / 32;
         const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            const int32_t col = task.z * BN + c * 32;
-            if (col >= la.ncols)
-                break;
-            uint32_t r[32];
-            __syncwarp();
-            ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
-            ptx::tmem_ld_wait();
-            float b[32];
-            load_bias32(bias, col, la.ncols, b);
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                v[i] = act_apply(la.act, __uint_as_float(r[i]) + b[i]);
-            if (row_ok) {
-                const int nvalid = la.ncols - col < 32 ? la.ncols - col : 32;   // multiple of 8
-                if (la.out_f32) {
-                    float* dst = static_cast<float*>(la.out) + row * la.ld_out + col;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        if (q * 4 < nvalid)
-                            reinterpret_cast<float4*>(dst)[q] =
-                                make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
-                } else {
-                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(la.out) + row * la.ld_out + col;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (q * 8 < nvalid)
-                            reinterpret_cast<uint4*>(dst)[q] = make_uint4(
-                                pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                                pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-                }
-            }
-        }
+        const uint32_t bias_smem = ptx::smem_u32(bias_slice);
+        if (act == TFFN_ACT_GELU_TANH)
+            drain_tile<TFFN_ACT_GELU_TANH>(taddr, nchunks, bias_smem, row_ok, out, out_f32, row, ld_out, col_base, ncols);
+        else if (act == TFFN_ACT_RELU)
+            drain_tile<TFFN_ACT_RELU>(taddr, nchunks, bias_smem, row_ok, out, out_f32, row, ld_out, col_base, ncols);
+        else
+            drain_tile<TFFN_ACT_NONE>(taddr, nchunks, bias_smem, row_ok, out, out_f32, row, ld_out, col_base, ncols);
         // Accumulator drained: hand it back to the leader's MMA thread.
         ptx::tc_fence_before();
         __syncwarp();
@@ -507,7 +546,7 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
                 const int32_t fi = task.y * n1 + task.z;
                 if (fi != p.skip_flag) {
                     __threadfence();
-                    ptx::st_release_gpu(&p.flags[fi * FLAG_WORDS_PER_TILE + rank * EPI_WARPS + quad], p.epoch);
+                    ptx::st_release_gpu(&p.flags[fi * FLAG_WORDS_PER_TILE + rank * EPI_WARPS + quad], aux.epoch);
                 }
             }
         }
@@ -541,6 +580,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
         }
         ptx::mbar_init(ptx::smem_u32(&aux.drain), 1);
         aux.abort = 0u;
+        // The epoch lives on the device, so a launch replayed from a CUDA
+        // graph still gets a fresh value: every CTA reads it before any CTA
+        // can finish (the last CTA out is the only writer).
+        aux.epoch = *reinterpret_cast<volatile uint32_t*>(&p.ctrl->epoch) + 1u;
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -576,7 +619,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
         if (lane == 0 && rank == 0)
             run_mma(p, aux, stages, w, tmem_base);
     } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
-        run_epilogue(p, aux, w, tmem_base, rank, warp, lane);
+        float* bias_slice = reinterpret_cast<float*>(stages + STAGES * STAGE_BYTES + AUX_BYTES) + (warp - 2) * BN;
+        run_epilogue(p, aux, w, tmem_base, rank, warp, lane, bias_slice);
     }
     __syncwarp();
     ptx::tc_fence_before();
@@ -594,6 +638,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
         if (atomicAdd(&p.ctrl->done, 1u) == gridDim.x - 1) {
             p.ctrl->ticket = 0u;
             p.ctrl->done = 0u;
+            p.ctrl->epoch = aux.epoch;
             __threadfence();
         }
     }

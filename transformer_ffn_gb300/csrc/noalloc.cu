@@ -146,8 +146,7 @@ extern "C" int ffn_forward_decode_noalloc(const void* X, const void* W1, const v
     p.O = static_cast<int32_t>(O);
     p.P = static_cast<int32_t>(P);
     p.act1 = act1;
-    p.act2 = act2;
-    p.epoch = 1u;   // flags were just cleared
+    p.act2 = act2;   // flags and epoch were just cleared: the kernel uses epoch 1
     p.wait_limit_ns = 4000ull * 1000000ull;
     const uint32_t arows = M <= 16 ? 16u : 32u;
     if (map2d(&p.map_w[0], W1, O, N, 64, decode::KC) || map2d(&p.map_w[1], W2, P, O, 64, decode::KC) ||
