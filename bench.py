@@ -44,13 +44,22 @@ CONFIGS = {
                   label="large prefill FFN M=16384 N=8192 O=28672 P=8192, GELU-tanh + ReLU"),
     "moe": dict(kind="moe", M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="gelu_tanh", act2="none",
                 label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh"),
+    "moe_moderate": dict(kind="moe", M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="gelu_tanh",
+                         act2="none", router="moderate",
+                         label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh, "
+                               "moderately skewed router (logit offsets -ln(1+e))"),
+    "moe_stress": dict(kind="moe", M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="gelu_tanh",
+                       act2="none", router="stress",
+                       label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh, "
+                             "stress-skewed router (expert 0 in ~98% of tokens)"),
 }
 DEFAULT = "prefill"
 FLUSH_BYTES = 256 << 20
 
 # Dominant kernel of each workload (for the ncu traffic record).
 KERNEL = {"tiny": "engine_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
-          "moe": "engine_kernel", "decode": "decode_kernel"}
+          "moe": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
+          "decode": "decode_kernel"}
 KERNEL_SOURCES = {
     "engine_kernel": ["engine.cuh", "common.cuh", "ptx.cuh", "schedule.h", "engine_dense.cu",
                       "engine_grouped.cu"],
@@ -215,7 +224,8 @@ def max_over_ranks(x, world):
 def make_inputs(cfg, device, seed=0):
     from transformer_ffn_gb300 import synth
     if cfg["kind"] == "moe":
-        return synth.moe_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], cfg["E"], seed=seed, device=device)
+        return synth.moe_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], cfg["E"], seed=seed, device=device,
+                                router=cfg.get("router", "balanced"))
     return synth.ffn_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], seed=seed, device=device)
 
 
@@ -304,11 +314,22 @@ def time_steps(step, steps, flush_buf, stream):
     return [a.elapsed_time(b) / 1e3 for a, b in evs]
 
 
+def padded_rows(cfg, inp):
+    """Rows of the grouped layout, zero padding included (each expert's rows
+    rounded up to whole 256-row bands), from the routing the library returns."""
+    import transformer_ffn_gb300 as tffn
+    _, r = tffn.moe_ffn_forward(inp.X, inp.logits, cfg["k"], inp.W1, inp.b1, inp.W2, inp.b2,
+                                cfg["act1"], cfg["act2"], routing=True)
+    counts = r["expert_offsets"].diff().cpu().tolist()
+    return int(sum((c + 255) // 256 * 256 for c in counts))
+
+
 def run_gpu(args, world, rank, local):
     import torch
     import transformer_ffn_gb300 as tffn
 
     tffn.load()
+    tffn.set_option(tffn.OPT_MOE_ORDER, args.moe_order)
     cfg = CONFIGS[args.config]
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
@@ -383,6 +404,9 @@ def run_gpu(args, world, rank, local):
     }
     if cfg["kind"] == "moe":
         line["config"]["routed_rows"] = cfg["M"] * cfg["k"]
+        line["config"]["router"] = cfg.get("router", "balanced")
+        line["config"]["padded_rows"] = padded_rows(cfg, inp)
+        line["config"]["segment_order"] = "largest expert first" if args.moe_order else "expert index"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         Y_dev = out.clone()
         line["cpu_baseline"] = cpu_baseline(cfg, inp, Y_dev, budget_s=args.cpu_budget)
@@ -488,6 +512,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT, choices=sorted(CONFIGS))
+    ap.add_argument("--moe-order", type=int, default=1, choices=(0, 1),
+                    help="MoE grouped-layout segment order: 0 expert index, 1 largest expert first")
     ap.add_argument("--impl", default="tffn", choices=["tffn", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=4)

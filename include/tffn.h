@@ -180,12 +180,16 @@ const char* tffn_status_string(int status);
  *                         the waiting GEMM2 tile then times out and the call
  *                         reports TFFN_ERR_TIMEOUT through tffn_check()
  *   TFFN_OPT_GROUP_M      row bands per raster group of the engine (default 4)
+ *   TFFN_OPT_MOE_ORDER    order of the experts' row segments in the grouped
+ *                         layout: 0 expert index, 1 (default) largest row
+ *                         count first.  Results are identical either way.
  * Returns the previous value. */
 enum {
     TFFN_OPT_PATH = 1,
     TFFN_OPT_WAIT_LIMIT_MS = 2,
     TFFN_OPT_SKIP_FLAG = 3,
-    TFFN_OPT_GROUP_M = 4
+    TFFN_OPT_GROUP_M = 4,
+    TFFN_OPT_MOE_ORDER = 5
 };
 int64_t tffn_set_option(int option, int64_t value);
 

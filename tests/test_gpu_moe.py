@@ -111,3 +111,41 @@ def test_moe_full_size_sampled_tokens(cuda_lib):
     _assert_close(Y[tokens].float().cpu().numpy(), _oracle_y(inp, k, "gelu_tanh", "none", tokens=tokens),
                   "moe full size")
     assert torch.isfinite(Y.float()).all()
+
+
+@pytest.mark.parametrize("router", ["balanced", "moderate", "stress"])
+def test_moe_router_skew_and_segment_order(cuda_lib, router):
+    # Routing skew of the MoE benchmarks (balanced / moderate / stress) under
+    # both segment orders: identical routing, identical outputs bit for bit
+    # (each grouped row is computed the same way wherever its band sits).
+    T, N, O, P, E, k = 700, 64, 256, 128, 8, 2
+    inp = synth.moe_inputs(T, N, O, P, E, seed=21, device="cuda", router=router)
+    outs = []
+    prev = cuda_lib.set_option(cuda_lib.OPT_MOE_ORDER, 0)
+    try:
+        for order in (0, 1):
+            cuda_lib.set_option(cuda_lib.OPT_MOE_ORDER, order)
+            Y, r = cuda_lib.moe_ffn_forward(inp.X, inp.logits, k, inp.W1, inp.b1, inp.W2, inp.b2,
+                                            "gelu_tanh", "none", routing=True)
+            cuda_lib.check()
+            _check_routing(r, inp.logits, k, E)
+            outs.append(Y)
+    finally:
+        cuda_lib.set_option(cuda_lib.OPT_MOE_ORDER, prev)
+    assert torch.equal(outs[0], outs[1])
+    _assert_close(outs[1].float().cpu().numpy(), _oracle_y(inp, k, "gelu_tanh", "none"), router)
+
+
+def test_moe_full_size_stress_skew_sampled_tokens(cuda_lib):
+    # the MoE workload with expert 0 in ~98 % of the tokens
+    T, N, O, P, E, k = 8192, 4096, 14336, 4096, 8, 2
+    inp = synth.moe_inputs(T, N, O, P, E, seed=0, device="cuda", router="stress")
+    Y, r = cuda_lib.moe_ffn_forward(inp.X, inp.logits, k, inp.W1, inp.b1, inp.W2, inp.b2,
+                                    "gelu_tanh", "none", routing=True)
+    cuda_lib.check()
+    _check_routing(r, inp.logits, k, E)
+    offs = r["expert_offsets"].cpu().numpy()
+    assert offs[1] - offs[0] > 0.95 * T
+    tokens = [0, 3, 4096, 8191]
+    _assert_close(Y[tokens].float().cpu().numpy(), _oracle_y(inp, k, "gelu_tanh", "none", tokens=tokens),
+                  "moe stress full size")

@@ -61,6 +61,7 @@ std::atomic<int64_t> g_opt_path{0};
 std::atomic<int64_t> g_opt_wait_ms{4000};
 std::atomic<int64_t> g_opt_skip{-1};
 std::atomic<int64_t> g_opt_group{4};
+std::atomic<int64_t> g_opt_moe_order{1};
 
 thread_local int g_last_launches = 0;
 thread_local bool g_timing = false;
@@ -516,7 +517,8 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
 
     int fail = 0;
     fail |= launch_moe_route(gate_logits, T, E, top_k, idx, w, s);
-    fail |= launch_moe_plan(idx, T, E, top_k, engine::BM, pos, src, band, nb, routing ? routing->perm : nullptr,
+    fail |= launch_moe_plan(idx, T, E, top_k, engine::BM, g_opt_moe_order.load() != 0 ? 1 : 0, pos, src, band, nb,
+                            routing ? routing->perm : nullptr,
                             routing ? routing->expert_offsets : nullptr, s);
     fail |= launch_moe_gather(X, src, nb, engine::BM, N, Xp, d->sms * 4, s);
     if (!fail) {
@@ -619,6 +621,7 @@ int64_t tffn_set_option(int option, int64_t value)
     case TFFN_OPT_WAIT_LIMIT_MS: return g_opt_wait_ms.exchange(value);
     case TFFN_OPT_SKIP_FLAG: return g_opt_skip.exchange(value);
     case TFFN_OPT_GROUP_M: return g_opt_group.exchange(value);
+    case TFFN_OPT_MOE_ORDER: return g_opt_moe_order.exchange(value);
     default: return -1;
     }
 }

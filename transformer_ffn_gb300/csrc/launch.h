@@ -25,9 +25,9 @@ int launch_decode(const decode::Params& p, int grid, cudaStream_t s);
 
 int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w,
                      cudaStream_t s);
-int launch_moe_plan(const int32_t* idx, int64_t T, int E, int k, int bm, int32_t* pos, int32_t* row_src,
-                    int32_t* band_expert, int32_t* nbands, int32_t* perm_out, int32_t* offs_out,
-                    cudaStream_t s);
+int launch_moe_plan(const int32_t* idx, int64_t T, int E, int k, int bm, int size_desc, int32_t* pos,
+                    int32_t* row_src, int32_t* band_expert, int32_t* nbands, int32_t* perm_out,
+                    int32_t* offs_out, cudaStream_t s);
 int launch_moe_gather(const void* X, const int32_t* row_src, const int32_t* nbands, int bm, int64_t N,
                       void* Xp, int grid, cudaStream_t s);
 int launch_moe_combine(const float* Yp, const int32_t* pos, const float* w, int64_t T, int k, int64_t P,

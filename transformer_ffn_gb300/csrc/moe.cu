@@ -94,14 +94,20 @@ __device__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_sums, int32_t* 
 
 // Single CTA.  Entries i = t*k + s are split into contiguous chunks, one per
 // thread, so a per-expert exclusive scan over threads keeps token order.
+// The experts' padded segments are laid out in expert index order, or, with
+// size_desc, largest row count first (ties: lower index first), the schedule
+// order of "Fine-Grained Compute-Communication Overlap for MoE", section 4.4,
+// rule (ii).  The public outputs (perm, offsets) keep expert index order
+// either way: they describe the grouping, not the internal layout.
 __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(
-    const int32_t* __restrict__ topk_idx, int64_t T, int E, int k, int bm,
+    const int32_t* __restrict__ topk_idx, int64_t T, int E, int k, int bm, int size_desc,
     int32_t* __restrict__ pos, int32_t* __restrict__ row_src, int32_t* __restrict__ band_expert,
     int32_t* __restrict__ nbands, int32_t* __restrict__ perm_out, int32_t* __restrict__ offs_out)
 {
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t s_total[64];
-    __shared__ int32_t s_pad[65];
+    __shared__ int32_t s_pad[64];       // first grouped row of expert e's segment
+    __shared__ int32_t s_pad_end[64];   // one past its last (padding included)
     __shared__ int32_t s_off[65];
     const int64_t R = T * k;
     const int64_t chunk = (R + PLAN_THREADS - 1) / PLAN_THREADS;
@@ -122,14 +128,30 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        int32_t p = 0, o = 0;
+        int32_t order[64];
         for (int e = 0; e < E; ++e) {
+            // stable insertion: an expert goes after every earlier one that
+            // is at least as large
+            int j = e;
+            if (size_desc)
+                while (j > 0 && s_total[order[j - 1]] < s_total[e]) {
+                    order[j] = order[j - 1];
+                    --j;
+                }
+            order[j] = e;
+        }
+        int32_t p = 0;
+        for (int j = 0; j < E; ++j) {
+            const int e = order[j];
             s_pad[e] = p;
-            s_off[e] = o;
             p += (s_total[e] + bm - 1) / bm * bm;
+            s_pad_end[e] = p;
+        }
+        int32_t o = 0;
+        for (int e = 0; e < E; ++e) {
+            s_off[e] = o;
             o += s_total[e];
         }
-        s_pad[E] = p;
         s_off[E] = o;
         *nbands = p / bm;
     }
@@ -146,9 +168,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(
     }
     // Padding rows read no token; bands map to their expert.
     for (int e = 0; e < E; ++e) {
-        for (int32_t r = s_pad[e] + s_total[e] + threadIdx.x; r < s_pad[e + 1]; r += blockDim.x)
+        for (int32_t r = s_pad[e] + s_total[e] + threadIdx.x; r < s_pad_end[e]; r += blockDim.x)
             row_src[r] = -1;
-        for (int32_t b = s_pad[e] / bm + threadIdx.x; b < s_pad[e + 1] / bm; b += blockDim.x)
+        for (int32_t b = s_pad[e] / bm + threadIdx.x; b < s_pad_end[e] / bm; b += blockDim.x)
             band_expert[b] = e;
     }
     if (offs_out)
@@ -219,11 +241,11 @@ int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx,
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
-int launch_moe_plan(const int32_t* idx, int64_t T, int E, int k, int bm, int32_t* pos, int32_t* row_src,
-                    int32_t* band_expert, int32_t* nbands, int32_t* perm_out, int32_t* offs_out,
-                    cudaStream_t s)
+int launch_moe_plan(const int32_t* idx, int64_t T, int E, int k, int bm, int size_desc, int32_t* pos,
+                    int32_t* row_src, int32_t* band_expert, int32_t* nbands, int32_t* perm_out,
+                    int32_t* offs_out, cudaStream_t s)
 {
-    moe::plan_kernel<<<1, moe::PLAN_THREADS, 0, s>>>(idx, T, E, k, bm, pos, row_src, band_expert, nbands,
+    moe::plan_kernel<<<1, moe::PLAN_THREADS, 0, s>>>(idx, T, E, k, bm, size_desc, pos, row_src, band_expert, nbands,
                                                      perm_out, offs_out);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

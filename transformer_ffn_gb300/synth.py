@@ -10,7 +10,12 @@ weights with the dimensions of Llama/Mixtral-class FFNs):
   b1 ~ U(-0.1, 0.1)          bf16, O
   W2 ~ N(0, 1/O)             bf16, O x P
   b2 ~ U(-0.1, 0.1)          bf16, P
-  gate logits ~ N(0, 1)      fp32, T x E   (MoE only)
+  gate logits ~ N(0, 1)      fp32, T x E   (MoE only), plus a per-expert
+                             offset beta_e that sets the router's skew:
+      balanced   beta_e = 0                 (~T*k/E rows per expert)
+      moderate   beta_e = -ln(1 + e)        (Zipf-like popularity: E=8, top-2
+                                             gives ~36/22/14/9/7/5/4/3 %)
+      stress     beta_0 = 3, others 0       (expert 0 is in ~98 % of tokens)
 Each tensor is drawn in fp32 from one torch.Generator seeded with ``seed`` in
 the fixed order X, W1, b1, W2, b2 (experts in index order), logits, then
 rounded to bf16 (round to nearest even).
@@ -70,8 +75,24 @@ def ffn_inputs(M, N, O, P, seed=0, device="cpu", x_std=1.0) -> FFNInputs:
     return FFNInputs(X, W1, b1, W2, b2)
 
 
+ROUTERS = ("balanced", "moderate", "stress")
+
+
+def router_offsets(E, router="balanced") -> torch.Tensor:
+    """Per-expert logit offsets beta_e of the named router distribution."""
+    if router == "balanced":
+        return torch.zeros(E)
+    if router == "moderate":
+        return -torch.log1p(torch.arange(E, dtype=torch.float32))
+    if router == "stress":
+        b = torch.zeros(E)
+        b[0] = 3.0
+        return b
+    raise ValueError(f"unknown router distribution {router!r}")
+
+
 def moe_inputs(T, N, O, P, E, seed=0, device="cpu",
-               logits: Optional[torch.Tensor] = None) -> MoEInputs:
+               logits: Optional[torch.Tensor] = None, router="balanced") -> MoEInputs:
     g = _gen(device, seed)
     X = _normal((T, N), 1.0, g, device)
     W1, b1, W2, b2 = [], [], [], []
@@ -82,6 +103,8 @@ def moe_inputs(T, N, O, P, E, seed=0, device="cpu",
         b2.append(_uniform((P,), -0.1, 0.1, g, device))
     if logits is None:
         logits = torch.randn((T, E), generator=g, device=device, dtype=torch.float32)
+        if router != "balanced":
+            logits += router_offsets(E, router).to(device)
     return MoEInputs(X, logits, W1, b1, W2, b2)
 
 
