@@ -11,7 +11,7 @@ import numpy as np
 
 from . import build_oracle
 
-ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
+ACT_NONE, ACT_RELU, ACT_GELU_TANH, ACT_SILU = 0, 1, 2, 3
 
 _lib = None
 
@@ -37,6 +37,9 @@ def lib():
                                       ctypes.c_int, i64, i64, i64, i64, i64p, i64,
                                       ctypes.c_int, f64p, u16p]
         L.tffn_oracle_ffn.restype = ctypes.c_int
+        L.tffn_oracle_glu_ffn.argtypes = [u16p, u16p, u16p, u16p, ctypes.c_int, i64, i64, i64,
+                                          i64, i64p, i64, ctypes.c_int, f64p, u16p]
+        L.tffn_oracle_glu_ffn.restype = ctypes.c_int
         L.tffn_oracle_moe_route.argtypes = [f32p, i64, ctypes.c_int, ctypes.c_int,
                                             i32p, f64p]
         L.tffn_oracle_moe_route.restype = ctypes.c_int
@@ -102,6 +105,31 @@ def ffn(X, W1, b1, W2, b2, act1, act2, rows=None, round_h=True, want_h=False):
                                _ptr(H, ctypes.c_uint16))
     if rc != 0:
         raise RuntimeError(f"oracle ffn failed: {rc}")
+    return (Y, H) if want_h else Y
+
+
+def glu_ffn(X, W1, W3, W2, act=ACT_SILU, rows=None, round_h=True, want_h=False):
+    """Y (float64, len(rows) x P) of the gated FFN Y = (act(X W1) * (X W3)) W2."""
+    X, W1, W3, W2 = _u16(X), _u16(W1), _u16(W3), _u16(W2)
+    M, N = X.shape
+    N2, O = W1.shape
+    O2, P = W2.shape
+    assert N == N2 and O == O2 and W3.shape == W1.shape
+    if rows is None:
+        r = None
+        nrows = M
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = r.shape[0]
+    Y = np.empty((nrows, P), dtype=np.float64)
+    H = np.empty((nrows, O), dtype=np.uint16) if want_h else None
+    rc = lib().tffn_oracle_glu_ffn(_ptr(X, ctypes.c_uint16), _ptr(W1, ctypes.c_uint16),
+                                   _ptr(W3, ctypes.c_uint16), _ptr(W2, ctypes.c_uint16), int(act),
+                                   M, N, O, P, _ptr(r, ctypes.c_int64), nrows,
+                                   1 if round_h else 0, _ptr(Y, ctypes.c_double),
+                                   _ptr(H, ctypes.c_uint16))
+    if rc != 0:
+        raise RuntimeError(f"oracle glu_ffn failed: {rc}")
     return (Y, H) if want_h else Y
 
 

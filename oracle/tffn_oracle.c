@@ -22,6 +22,14 @@
  *   activations  The page names no formula.  GELU is the tanh form
  *                0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) of Hendrycks
  *                and Gimpel, "Gaussian Error Linear Units"; ReLU is max(x, 0).
+ *   glu_ffn      "Kernel fusion and tensor parallelism", section "Results": a
+ *                SwiGLU FFN has a third weight matrix whose product with the
+ *                input gates the activation, and no biases.  Written out as in
+ *                Shazeer, "GLU Variants Improve Transformer" (2020):
+ *                H = act(X W1) * (X W3) elementwise, Y = H W2, with W1, W3 in
+ *                R^{NxO}, W2 in R^{OxP}; SwiGLU takes act = SiLU (Swish with
+ *                beta 1), x sigma(x) = x / (1 + exp(-x)).  H is rounded to bf16
+ *                after the product, as in the two-layer FFN.
  *   moe_route    "Fine-Grained Compute-Communication Overlap for MoE" review
  *                (zhongzhuzhou.org), section 2.1: the router turns logits into a
  *                distribution over E experts and keeps the top k; the kept
@@ -104,6 +112,10 @@ double tffn_oracle_act(int act, double x)
         const double k1 = 0.044715;
         return 0.5 * x * (1.0 + tanh(k0 * (x + k1 * x * x * x)));
     }
+    case TFFN_ORACLE_ACT_SILU:
+        /* x sigma(x); for x below about -745 exp(-x) overflows to +inf and
+         * the quotient is -0, the limit of x sigma(x). */
+        return x / (1.0 + exp(-x));
     default:
         return NAN;
     }
@@ -112,7 +124,7 @@ double tffn_oracle_act(int act, double x)
 static int act_ok(int act)
 {
     return act == TFFN_ORACLE_ACT_NONE || act == TFFN_ORACLE_ACT_RELU ||
-           act == TFFN_ORACLE_ACT_GELU_TANH;
+           act == TFFN_ORACLE_ACT_GELU_TANH || act == TFFN_ORACLE_ACT_SILU;
 }
 
 static double bias_at(const uint16_t *b, int64_t j)
@@ -185,6 +197,73 @@ int tffn_oracle_ffn(const uint16_t *X, const uint16_t *W1, const uint16_t *b1,
             Y[r * P + k] = tffn_oracle_act(act2, acc2[k] + bias_at(b2, k));
     }
     free(acc1); free(hrow); free(acc2);
+    return 0;
+}
+
+/* ------------------------------------------------------------ gated FFN -- */
+
+int tffn_oracle_glu_ffn(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
+                        const uint16_t *W2, int act, int64_t M, int64_t N, int64_t O,
+                        int64_t P, const int64_t *rows, int64_t nrows, int round_h,
+                        double *Y, uint16_t *H)
+{
+    if (!X || !W1 || !W3 || !W2 || !Y || M < 0 || N < 1 || O < 1 || P < 1 || !act_ok(act))
+        return -1;
+    if (!rows)
+        nrows = M;
+
+    double *gate = malloc(sizeof(double) * (size_t)O);   /* one row of X W1 */
+    double *lin = malloc(sizeof(double) * (size_t)O);    /* one row of X W3 */
+    double *acc2 = malloc(sizeof(double) * (size_t)P);   /* one row of H W2 */
+    if (!gate || !lin || !acc2) {
+        free(gate); free(lin); free(acc2);
+        return -2;
+    }
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= M) {
+            free(gate); free(lin); free(acc2);
+            return -1;
+        }
+        /* The two input products, each summed over n in ascending order. */
+        for (int64_t j = 0; j < O; ++j) {
+            gate[j] = 0.0;
+            lin[j] = 0.0;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            double x = tffn_oracle_bf16_to_f64(X[i * N + n]);
+            const uint16_t *w1 = W1 + n * O;
+            const uint16_t *w3 = W3 + n * O;
+            for (int64_t j = 0; j < O; ++j) {
+                gate[j] += x * tffn_oracle_bf16_to_f64(w1[j]);
+                lin[j] += x * tffn_oracle_bf16_to_f64(w3[j]);
+            }
+        }
+        /* H[i,j] = act(gate) * lin, rounded to bf16; reuse gate[] for H. */
+        for (int64_t j = 0; j < O; ++j) {
+            double h = tffn_oracle_act(act, gate[j]) * lin[j];
+            if (round_h) {
+                uint16_t hb = tffn_oracle_f64_to_bf16(h);
+                if (H)
+                    H[r * O + j] = hb;
+                h = tffn_oracle_bf16_to_f64(hb);
+            }
+            gate[j] = h;
+        }
+        /* Y[i,k] = sum_o H[i,o] W2[o,k], o ascending; no bias, no second
+         * activation. */
+        for (int64_t k = 0; k < P; ++k)
+            acc2[k] = 0.0;
+        for (int64_t o = 0; o < O; ++o) {
+            double h = gate[o];
+            const uint16_t *w = W2 + o * P;
+            for (int64_t k = 0; k < P; ++k)
+                acc2[k] += h * tffn_oracle_bf16_to_f64(w[k]);
+        }
+        for (int64_t k = 0; k < P; ++k)
+            Y[r * P + k] = acc2[k];
+    }
+    free(gate); free(lin); free(acc2);
     return 0;
 }
 

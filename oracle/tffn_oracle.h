@@ -14,7 +14,8 @@ extern "C" {
 enum {
     TFFN_ORACLE_ACT_NONE = 0,
     TFFN_ORACLE_ACT_RELU = 1,
-    TFFN_ORACLE_ACT_GELU_TANH = 2
+    TFFN_ORACLE_ACT_GELU_TANH = 2,
+    TFFN_ORACLE_ACT_SILU = 3
 };
 
 double   tffn_oracle_bf16_to_f64(uint16_t h);
@@ -29,6 +30,13 @@ int tffn_oracle_ffn(const uint16_t *X, const uint16_t *W1, const uint16_t *b1,
                     int64_t M, int64_t N, int64_t O, int64_t P,
                     const int64_t *rows, int64_t nrows, int round_h,
                     double *Y, uint16_t *H);
+
+/* Gated FFN: Y = (act(X W1) * (X W3)) W2 for the listed rows (all M when
+ * rows is NULL); SwiGLU is act = SILU.  H (nullable) receives the bf16 rows. */
+int tffn_oracle_glu_ffn(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
+                        const uint16_t *W2, int act, int64_t M, int64_t N, int64_t O,
+                        int64_t P, const int64_t *rows, int64_t nrows, int round_h,
+                        double *Y, uint16_t *H);
 
 /* topk_idx[T*k], topk_w[T*k] (nullable) from fp32 logits[T*E]. */
 int tffn_oracle_moe_route(const float *logits, int64_t T, int E, int k,

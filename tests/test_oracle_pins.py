@@ -377,3 +377,124 @@ def test_moe_top2_is_weighted_sum_of_two_experts():
         y0 = oracle.ffn(X, W1[e[0]], b1[e[0]], W2[e[0]], b2[e[0]], ACT_GELU_TANH, ACT_NONE, rows=[t])
         y1 = oracle.ffn(X, W1[e[1]], b1[e[1]], W2[e[1]], b2[e[1]], ACT_GELU_TANH, ACT_NONE, rows=[t])
         np.testing.assert_allclose(got[r], g0 * y0[0] + g1 * y1[0], rtol=1e-13, atol=1e-14)
+
+
+# ------------------------------------------------------------ gated FFN ----
+# "Kernel fusion and tensor parallelism", section "Results": the SwiGLU FFN of
+# the benchmarked models has a third weight matrix that gates the activation
+# and no biases; written out as H = act(X W1) * (X W3), Y = H W2.
+
+ACT_SILU = oracle.ACT_SILU
+
+
+def test_silu_closed_forms_and_identities():
+    assert oracle.act(ACT_SILU, 0.0) == 0.0
+    for x in (0.1, 0.5, 1.0, 2.0, 5.5, 20.0):
+        # sigma(x) + sigma(-x) = 1, so silu(x) - silu(-x) = x
+        d = oracle.act(ACT_SILU, x) - oracle.act(ACT_SILU, -x)
+        assert abs(d - x) <= 4e-16 * max(1.0, abs(x))
+    assert oracle.act(ACT_SILU, 1.0) == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+    assert abs(oracle.act(ACT_SILU, 40.0) - 40.0) < 1e-15
+    assert abs(oracle.act(ACT_SILU, -40.0)) < 1e-15
+    v = oracle.act(ACT_SILU, -1000.0)
+    assert v == 0.0 and not math.isnan(v)
+
+
+def test_silu_matches_library_routine():
+    xs = torch.linspace(-30, 30, 6001, dtype=torch.float64)
+    ref = torch.nn.functional.silu(xs)
+    got = torch.tensor([oracle.act(ACT_SILU, float(x)) for x in xs], dtype=torch.float64)
+    assert torch.allclose(got, ref, rtol=1e-14, atol=1e-300)
+
+
+def _exact_glu(X, W1, W3, W2, act, M, N, O, P):
+    """Exact rational gated FFN for act in {NONE, RELU}, H rounded to bf16."""
+    Y, Hs = [], []
+    for i in range(M):
+        h = []
+        for j in range(O):
+            g = sum((Fraction(X[i * N + n]) * Fraction(W1[n * O + j]) for n in range(N)), Fraction(0))
+            u = sum((Fraction(X[i * N + n]) * Fraction(W3[n * O + j]) for n in range(N)), Fraction(0))
+            if act == ACT_RELU and g < 0:
+                g = Fraction(0)
+            h.append(_frac_to_bf16(g * u))
+        Hs.append(h)
+        Y.append([sum((h[o] * Fraction(W2[o * P + k]) for o in range(O)), Fraction(0)) for k in range(P)])
+    return Y, Hs
+
+
+def _bf16_fracs(rng, count):
+    raw = np.array([rng.uniform(-2, 2) for _ in range(count)], dtype=np.float32)
+    return (raw.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64).tolist()
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 1), (2, 3, 4, 5), (5, 9, 13, 6)])
+@pytest.mark.parametrize("act", [ACT_RELU, ACT_NONE])
+def test_glu_brute_force_exact(shape, act):
+    # ReGLU and the bilinear form are rational, so the exact answer is known;
+    # the gate and linear operands get different matrices, so swapping them
+    # (or the operand the activation goes on) fails
+    M, N, O, P = shape
+    rng = random.Random(sum(shape) * 17 + act)
+    X, W1, W3, W2 = (_bf16_fracs(rng, c) for c in (M * N, N * O, N * O, O * P))
+    want, want_h = _exact_glu(X, W1, W3, W2, act, M, N, O, P)
+    Yo, Ho = oracle.glu_ffn(_u16_of_values(X).reshape(M, N), _u16_of_values(W1).reshape(N, O),
+                            _u16_of_values(W3).reshape(N, O), _u16_of_values(W2).reshape(O, P),
+                            act, want_h=True)
+    for i in range(M):
+        for j in range(O):
+            assert oracle.bf16_to_f64(int(Ho[i, j])) == float(want_h[i][j])
+        for k in range(P):
+            w = float(want[i][k])
+            assert abs(Yo[i, k] - w) <= 1e-12 * max(1.0, abs(w))
+
+
+def test_swiglu_brute_force_python():
+    # SiLU is transcendental: pure-Python loops with math.exp on a tiny case
+    M, N, O, P = 3, 5, 7, 4
+    rng = random.Random(99)
+    X, W1, W3, W2 = (_bf16_fracs(rng, c) for c in (M * N, N * O, N * O, O * P))
+    Yo = oracle.glu_ffn(_u16_of_values(X).reshape(M, N), _u16_of_values(W1).reshape(N, O),
+                        _u16_of_values(W3).reshape(N, O), _u16_of_values(W2).reshape(O, P), ACT_SILU,
+                        round_h=False)
+    for i in range(M):
+        h = []
+        for j in range(O):
+            g = math.fsum(X[i * N + n] * W1[n * O + j] for n in range(N))
+            u = math.fsum(X[i * N + n] * W3[n * O + j] for n in range(N))
+            h.append(g / (1.0 + math.exp(-g)) * u)
+        for k in range(P):
+            want = math.fsum(h[o] * W2[o * P + k] for o in range(O))
+            assert abs(Yo[i, k] - want) <= 1e-13 * max(1.0, abs(want))
+
+
+@pytest.mark.parametrize("act", [ACT_SILU, ACT_GELU_TANH, ACT_RELU])
+def test_glu_with_unit_linear_branch_is_the_dense_ffn(act):
+    # a column of ones in X selected by W3 makes X W3 == 1 everywhere: the
+    # gated FFN is then the two-layer FFN with no biases, bit for bit
+    M, N, O, P = 6, 16, 40, 12
+    inp = synth.ffn_inputs(M, N, O, P, seed=31)
+    X, W1, W2 = (synth.to_u16(t) for t in (inp.X, inp.W1, inp.W2))
+    X = X.copy()
+    X[:, 3] = 0x3F80                              # 1.0
+    W3 = np.zeros((N, O), dtype=np.uint16)
+    W3[3, :] = 0x3F80
+    np.testing.assert_array_equal(oracle.glu_ffn(X, W1, W3, W2, act),
+                                  oracle.ffn(X, W1, None, W2, None, act, ACT_NONE))
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_glu_megatron_split_reproduces_unsplit(G):
+    # W1 and W3 split by columns, W2 by rows: each H column depends on one
+    # column of each, so the partial outputs sum to the unsplit result
+    M, N, O, P = 5, 24, 64, 16
+    a = synth.ffn_inputs(M, N, O, P, seed=40 + G)
+    b = synth.ffn_inputs(M, N, O, P, seed=50 + G)
+    X, W1, W2 = (synth.to_u16(t) for t in (a.X, a.W1, a.W2))
+    W3 = synth.to_u16(b.W1)
+    full = oracle.glu_ffn(X, W1, W3, W2, ACT_SILU)
+    s = O // G
+    acc = sum(oracle.glu_ffn(X, np.ascontiguousarray(W1[:, g * s:(g + 1) * s]),
+                             np.ascontiguousarray(W3[:, g * s:(g + 1) * s]),
+                             np.ascontiguousarray(W2[g * s:(g + 1) * s, :]), ACT_SILU) for g in range(G))
+    np.testing.assert_allclose(acc, full, rtol=1e-12, atol=1e-12)
