@@ -44,6 +44,9 @@ CONFIGS = {
                   label="large prefill FFN M=16384 N=8192 O=28672 P=8192, GELU-tanh + ReLU"),
     "moe": dict(kind="moe", M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="gelu_tanh", act2="none",
                 label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh"),
+    "swiglu": dict(kind="glu", M=4096, N=4096, O=14336, P=4096, act1="silu", act2="none",
+                   label="SwiGLU FFN (Llama 3 8B shape) M=4096 N=4096 O=14336 P=4096, "
+                         "Y = (SiLU(X W1) * (X W3)) W2, no biases"),
     "moe_moderate": dict(kind="moe", M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="gelu_tanh",
                          act2="none", router="moderate",
                          label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh, "
@@ -58,7 +61,7 @@ FLUSH_BYTES = 256 << 20
 
 # Dominant kernel of each workload (for the ncu traffic record).
 KERNEL = {"tiny": "engine_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
-          "moe": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
+          "swiglu": "engine_kernel", "moe": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
           "decode": "decode_kernel"}
 KERNEL_SOURCES = {
     "engine_kernel": ["engine.cuh", "common.cuh", "ptx.cuh", "schedule.h", "engine_dense.cu",
@@ -68,9 +71,11 @@ KERNEL_SOURCES = {
 
 
 def flops(cfg):
-    """Algorithmic FLOPs of one step: 2*rows*O*(N+P), routed rows for MoE."""
+    """Algorithmic FLOPs of one step: 2*rows*O*(N+P), routed rows for MoE;
+    2*M*O*(2N+P) for the gated FFN (two input products)."""
     rows = cfg["M"] * cfg.get("k", 1)
-    return 2.0 * rows * cfg["O"] * (cfg["N"] + cfg["P"])
+    n_in = 2 * cfg["N"] if cfg["kind"] == "glu" else cfg["N"]
+    return 2.0 * rows * cfg["O"] * (n_in + cfg["P"])
 
 
 def weight_bytes(cfg):
@@ -223,6 +228,8 @@ def max_over_ranks(x, world):
 
 def make_inputs(cfg, device, seed=0):
     from transformer_ffn_gb300 import synth
+    if cfg["kind"] == "glu":
+        return synth.glu_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], seed=seed, device=device)
     if cfg["kind"] == "moe":
         return synth.moe_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], cfg["E"], seed=seed, device=device,
                                 router=cfg.get("router", "balanced"))
@@ -232,6 +239,8 @@ def make_inputs(cfg, device, seed=0):
 def step_fn(cfg, inp, out, X=None):
     import transformer_ffn_gb300 as tffn
     X = inp.X if X is None else X
+    if cfg["kind"] == "glu":
+        return lambda: tffn.ffn_glu_forward(X, inp.W1, inp.W3, inp.W2, cfg["act1"], out=out)
     if cfg["kind"] == "moe":
         return lambda: tffn.moe_ffn_forward(X, inp.logits, cfg["k"], inp.W1, inp.b1, inp.W2, inp.b2,
                                             cfg["act1"], cfg["act2"], out=out)
@@ -274,6 +283,8 @@ def run_e2e(cfg, inp, args, flush_buf, stream):
             if moe:
                 tffn.moe_ffn_forward(X_dev[b], L_dev[b], cfg["k"], inp.W1, inp.b1, inp.W2, inp.b2,
                                      cfg["act1"], cfg["act2"], out=Y_dev[b], stream=comp)
+            elif cfg["kind"] == "glu":
+                tffn.ffn_glu_forward(X_dev[b], inp.W1, inp.W3, inp.W2, cfg["act1"], out=Y_dev[b], stream=comp)
             else:
                 tffn.ffn_forward(X_dev[b], inp.W1, inp.b1, inp.W2, inp.b2, cfg["act1"], cfg["act2"],
                                  out=Y_dev[b], stream=comp)
@@ -418,6 +429,8 @@ def run_gpu(args, world, rank, local):
 def _oracle_inputs(cfg, inp):
     from transformer_ffn_gb300 import synth
     u = synth.to_u16
+    if cfg["kind"] == "glu":
+        return (u(inp.X), u(inp.W1), u(inp.W3), u(inp.W2))
     if cfg["kind"] == "moe":
         return (u(inp.X), inp.logits.cpu().numpy(), [u(w) for w in inp.W1], [u(b) for b in inp.b1],
                 [u(w) for w in inp.W2], [u(b) for b in inp.b2])
@@ -426,7 +439,11 @@ def _oracle_inputs(cfg, inp):
 
 def _oracle_rows(cfg, host, rows):
     import oracle
-    acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "gelu_tanh": oracle.ACT_GELU_TANH}
+    acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "gelu_tanh": oracle.ACT_GELU_TANH,
+            "silu": oracle.ACT_SILU}
+    if cfg["kind"] == "glu":
+        X, W1, W3, W2 = host
+        return oracle.glu_ffn(X, W1, W3, W2, acts[cfg["act1"]], rows=rows)
     if cfg["kind"] == "moe":
         X, lg, W1, b1, W2, b2 = host
         return oracle.moe_ffn(X, lg, cfg["k"], W1, b1, W2, b2, acts[cfg["act1"]], acts[cfg["act2"]],

@@ -37,11 +37,13 @@ extern "C" {
 struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
 
 /* Elementwise activations.  GELU is the tanh form
- * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))). */
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))); SiLU (Swish with beta 1)
+ * is x sigma(x) = x / (1 + exp(-x)). */
 typedef enum {
     TFFN_ACT_NONE = 0,
     TFFN_ACT_RELU = 1,
-    TFFN_ACT_GELU_TANH = 2
+    TFFN_ACT_GELU_TANH = 2,
+    TFFN_ACT_SILU = 3
 } tffn_act;
 
 typedef enum {
@@ -80,6 +82,29 @@ typedef enum {
 int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, const void* b2,
                 int act1, int act2, int64_t M, int64_t N, int64_t O, int64_t P, void* Y,
                 struct CUstream_st* stream);
+
+/*
+ * ffn_glu_forward -- gated FFN: Y = (act(X W1) * (X W3)) W2, * elementwise;
+ * SwiGLU is act = TFFN_ACT_SILU (GeGLU: GELU, ReGLU: ReLU, bilinear: NONE).
+ *
+ * Defined by "Kernel fusion and tensor parallelism" (brunomaga.github.io),
+ * section "Results": the SwiGLU FFN of the benchmarked models has a third
+ * weight matrix, whose product with the input gates the activation, and no
+ * biases.  The gate is the activated product X W1; X W3 multiplies it
+ * (Shazeer, "GLU Variants Improve Transformer", 2020, equation for FFN_SwiGLU).
+ *
+ *   X  [M x N] bf16      W1 [N x O] bf16      W3 [N x O] bf16
+ *   W2 [O x P] bf16      Y  [M x P] bf16 (written; must not alias an input)
+ *   act: tffn_act code applied to X W1.
+ *
+ * Numerics: products accumulate in fp32; H = act(X W1) * (X W3) is rounded to
+ * bf16 (nearest even) where it is stored between the layers; Y is rounded to
+ * bf16.  Path: always the persistent tcgen05 engine; each layer-1 tile pairs
+ * 128 columns of W1 with the same 128 columns of W3 in one 256-column
+ * accumulator.  Errors and workspace as ffn_forward.
+ */
+int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W2, int act, int64_t M,
+                    int64_t N, int64_t O, int64_t P, void* Y, struct CUstream_st* stream);
 
 /* Optional routing outputs of moe_ffn_forward (every member nullable; device
  * pointers): topk_idx[T*k] int32 and topk_w[T*k] fp32, slot s of token t at

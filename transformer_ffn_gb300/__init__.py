@@ -13,15 +13,15 @@ import torch
 
 __all__ = ["ffn_forward", "moe_ffn_forward", "load", "check", "set_option", "workspace_bytes",
            "set_workspace", "last_launch_count", "timing_begin", "timing_end", "TffnError",
-           "ACT_NONE", "ACT_RELU", "ACT_GELU_TANH", "OPT_PATH", "OPT_WAIT_LIMIT_MS",
+           "ACT_NONE", "ACT_RELU", "ACT_GELU_TANH", "ACT_SILU", "ffn_glu_forward", "OPT_PATH", "OPT_WAIT_LIMIT_MS",
            "OPT_SKIP_FLAG", "OPT_GROUP_M", "OPT_MOE_ORDER", "LIB_PATH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtffn.so")
 
-ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
+ACT_NONE, ACT_RELU, ACT_GELU_TANH, ACT_SILU = 0, 1, 2, 3
 _ACTS = {"none": ACT_NONE, None: ACT_NONE, "relu": ACT_RELU, "gelu_tanh": ACT_GELU_TANH,
-         "gelu": ACT_GELU_TANH}
+         "gelu": ACT_GELU_TANH, "silu": ACT_SILU, "swish": ACT_SILU}
 OPT_PATH, OPT_WAIT_LIMIT_MS, OPT_SKIP_FLAG, OPT_GROUP_M, OPT_MOE_ORDER = 1, 2, 3, 4, 5
 
 _lib = None
@@ -50,6 +50,8 @@ def load():
     L = ctypes.CDLL(LIB_PATH)
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     L.ffn_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i64, i64, i64, vp, vp]
+    L.ffn_glu_forward.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, vp, vp]
+    L.ffn_glu_forward.restype = i32
     L.ffn_forward.restype = i32
     L.moe_ffn_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
                                   ctypes.POINTER(_Routing), vp]
@@ -136,6 +138,25 @@ def ffn_forward(X, W1, b1, W2, b2, act1="gelu_tanh", act2="none", out=None, stre
     rc = L.ffn_forward(_ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _act(act1), _act(act2),
                        M, N, O, P, _ptr(Y), _stream_ptr(stream))
     _raise(rc, "ffn_forward")
+    return Y
+
+
+def ffn_glu_forward(X, W1, W3, W2, act="silu", out=None, stream=None):
+    """Gated FFN Y = (act(X @ W1) * (X @ W3)) @ W2 in bf16 (SwiGLU: act="silu")."""
+    L = load()
+    dev = X.device
+    for name, t in (("X", X), ("W1", W1), ("W3", W3), ("W2", W2)):
+        _check_bf16(name, t, 2, dev)
+    M, N = X.shape
+    N2, O = W1.shape
+    O2, P = W2.shape
+    if N2 != N or O2 != O or tuple(W3.shape) != (N, O):
+        raise ValueError("shape mismatch")
+    Y = out if out is not None else torch.empty((M, P), dtype=torch.bfloat16, device=dev)
+    _check_bf16("out", Y, 2, dev)
+    rc = L.ffn_glu_forward(_ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _act(act), M, N, O, P, _ptr(Y),
+                           _stream_ptr(stream))
+    _raise(rc, "ffn_glu_forward")
     return Y
 
 

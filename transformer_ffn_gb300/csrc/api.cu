@@ -126,7 +126,7 @@ int make_map_b(CUtensorMap* m, const void* base, int64_t ncols, int64_t K, bool 
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool act_ok(int a) { return a == TFFN_ACT_NONE || a == TFFN_ACT_RELU || a == TFFN_ACT_GELU_TANH; }
+bool act_ok(int a) { return a == TFFN_ACT_NONE || a == TFFN_ACT_RELU || a == TFFN_ACT_GELU_TANH || a == TFFN_ACT_SILU; }
 bool dim_ok(int64_t d) { return d >= 8 && d % 8 == 0 && d < (int64_t(1) << 31); }
 
 // Current device's state, initialised on first use.
@@ -236,13 +236,15 @@ struct DenseLayout {
     size_t total = 0;
 };
 
-DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P)
+// glu: the gated form, whose layer-1 tiles cover 128 hidden columns each and
+// which has no weight-streaming (decode) path.
+DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, bool glu = false)
 {
     DenseLayout L;
     int64_t path = g_opt_path.load();
     if (path == 0)
-        path = (M <= DECODE_MAX_M) ? 2 : 1;
-    if (path == 2 && M > DECODE_MAX_M)
+        path = (M <= DECODE_MAX_M && !glu) ? 2 : 1;
+    if (path == 2 && (M > DECODE_MAX_M || glu))
         path = 1;
     L.path = static_cast<int>(path);
     L.off_h = SYNC_BYTES;
@@ -253,7 +255,8 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P)
         return L;
     }
     L.m_blocks = (M + engine::BM - 1) / engine::BM;
-    L.n1 = static_cast<int32_t>((O + engine::BN - 1) / engine::BN);
+    const int64_t h_cols = glu ? engine::BN_CTA : engine::BN;   // hidden columns per layer-1 tile
+    L.n1 = static_cast<int32_t>((O + h_cols - 1) / h_cols);
     L.n2 = static_cast<int32_t>((P + engine::BN - 1) / engine::BN);
     if (L.path == 1 && static_cast<size_t>(L.m_blocks) * L.n1 * engine::FLAG_WORDS_PER_TILE > FLAG_WORDS)
         L.path = 3;   // more layer-1 tiles than flags: run the layers as two launches
@@ -310,6 +313,48 @@ void fill_layer(engine::LayerArgs& la, int64_t K, int64_t ncols, int act, int ou
 }
 
 }  // namespace
+
+// Launch the dense engine as the layout says: one fused launch, or layer 1
+// and layer 2 as two launches.
+static int run_dense_engine(DeviceState& d, uint8_t* base, const DenseLayout& L, engine::Params<1>& p,
+                            cudaStream_t s)
+{
+    p.layer[0].n_tiles = L.n1;
+    p.m_blocks = L.m_blocks;
+    p.m_blocks_dev = nullptr;
+    p.band_expert = nullptr;
+    p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+    p.ctrl = reinterpret_cast<DevCtrl*>(base);
+    p.wait_limit_ns = wait_limit_ns();
+    p.group_m = static_cast<int32_t>(g_opt_group.load() < 1 ? 1 : g_opt_group.load());
+    p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
+    if (L.path == 1) {
+        int rc = count_launch(d, base, s);
+        if (rc != TFFN_OK)
+            return rc;
+        p.mode = MODE_FUSED;
+        const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, MODE_FUSED);
+        const int pairs = static_cast<int>(total < d.sms ? total : d.sms);
+        timing_start(s);
+        if (launch_engine_dense(p, pairs, s) != 0)
+            return TFFN_ERR_CUDA;
+        timing_stop(s);
+        g_last_launches = 1;
+        return TFFN_OK;
+    }
+    for (int mode = MODE_LAYER1; mode <= MODE_LAYER2; ++mode) {
+        p.mode = mode;
+        const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, mode);
+        const int pairs = static_cast<int>(total < d.sms ? total : d.sms);
+        if (mode == MODE_LAYER1)
+            timing_start(s);
+        if (launch_engine_dense(p, pairs, s) != 0)
+            return TFFN_ERR_CUDA;
+        ++g_last_launches;
+    }
+    timing_stop(s);
+    return TFFN_OK;
+}
 
 // ====================================================================== ABI
 
@@ -396,41 +441,49 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
     p.bias[1][0] = static_cast<const __nv_bfloat16*>(b2);
     fill_layer<1>(p.layer[0], N, O, act1, 0, rows_h, H);
     fill_layer<1>(p.layer[1], O, P, act2, 0, M, Y);
-    p.m_blocks = L.m_blocks;
-    p.m_blocks_dev = nullptr;
-    p.band_expert = nullptr;
-    p.flags = flags;
-    p.ctrl = ctrl;
-    p.wait_limit_ns = wait_limit_ns();
-    p.group_m = static_cast<int32_t>(g_opt_group.load() < 1 ? 1 : g_opt_group.load());
-    p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
 
-    if (L.path == 1) {
-        if ((rc = count_launch(*d, base, s)) != TFFN_OK)
-            return rc;
-        p.mode = MODE_FUSED;
-        const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, MODE_FUSED);
-        const int pairs = static_cast<int>(total < d->sms ? total : d->sms);
-        timing_start(s);
-        if (launch_engine_dense(p, pairs, s) != 0)
-            return TFFN_ERR_CUDA;
-        timing_stop(s);
-        g_last_launches = 1;
-        return TFFN_OK;
-    }
-    // two launches: layer 1, then layer 2
-    for (int mode = MODE_LAYER1; mode <= MODE_LAYER2; ++mode) {
-        p.mode = mode;
-        const int64_t total = engine_total_tickets(L.m_blocks, L.n1, L.n2, mode);
-        const int pairs = static_cast<int>(total < d->sms ? total : d->sms);
-        if (mode == MODE_LAYER1)
-            timing_start(s);
-        if (launch_engine_dense(p, pairs, s) != 0)
-            return TFFN_ERR_CUDA;
-        ++g_last_launches;
-    }
-    timing_stop(s);
-    return TFFN_OK;
+    return run_dense_engine(*d, base, L, p, s);
+}
+
+int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W2, int act, int64_t M, int64_t N,
+                    int64_t O, int64_t P, void* Y, struct CUstream_st* stream)
+{
+    g_last_launches = 0;
+    if (M < 0 || M >= (int64_t(1) << 31) || !dim_ok(N) || !dim_ok(O) || !dim_ok(P) || !act_ok(act))
+        return TFFN_ERR_INVALID_ARG;
+    if (M == 0)
+        return TFFN_OK;   // empty call: X and Y may be NULL
+    if (!X || !W1 || !W3 || !W2 || !Y)
+        return TFFN_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(Y))
+        return TFFN_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != TFFN_OK)
+        return rc;
+    const DenseLayout L = dense_layout(M, N, O, P, true);
+    uint8_t* base = nullptr;
+    rc = workspace(*d, L.total, s, &base);
+    if (rc != TFFN_OK)
+        return rc;
+
+    engine::Params<1> p;
+    std::memset(&p, 0, sizeof(p));
+    void* H = base + L.off_h;
+    const int64_t rows_h = L.m_blocks * engine::BM;
+    const bool b3d = (O % 64 == 0) && (P % 64 == 0);
+    if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) || make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) ||
+        make_map_b(&p.map_b[0][0], W1, O, N, b3d) || make_map_b(&p.map_b_lin, W3, O, N, b3d) ||
+        make_map_b(&p.map_b[1][0], W2, P, O, b3d))
+        return TFFN_ERR_INVALID_ARG;
+    p.b3d = b3d ? 1 : 0;
+    p.glu = 1;
+    fill_layer<1>(p.layer[0], N, O, act, 0, rows_h, H);
+    fill_layer<1>(p.layer[1], O, P, TFFN_ACT_NONE, 0, M, Y);
+    return run_dense_engine(*d, base, L, p, s);
 }
 
 int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const void* const* W1,

@@ -125,7 +125,9 @@ static __device__ __noinline__ bool wait_flag(const WaitCtx& w, const uint32_t* 
 
 // Activations (fp32).  GELU uses the tanh form written through the identity
 // 0.5 x (1 + tanh(u)) = x / (1 + exp(-2u)), which keeps full relative accuracy
-// for negative x where 1 + tanh(u) would cancel.
+// for negative x where 1 + tanh(u) would cancel.  SiLU is x sigma(x) =
+// x / (1 + exp(-x)); the exponent is capped at 80 so the denominator stays
+// finite (below x = -80 the result is below 1e-33 in magnitude either way).
 __device__ __forceinline__ float act_apply(int act, float x)
 {
     if (act == TFFN_ACT_RELU)
@@ -136,6 +138,8 @@ __device__ __forceinline__ float act_apply(int act, float x)
         const float u = k0 * fmaf(k1 * x, x * x, x);
         return __fdividef(x, 1.0f + __expf(-2.0f * u));
     }
+    if (act == TFFN_ACT_SILU)
+        return __fdividef(x, 1.0f + __expf(fminf(-x, 80.0f)));
     return x;
 }
 

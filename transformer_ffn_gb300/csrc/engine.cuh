@@ -106,7 +106,17 @@ struct Params {
     int32_t group_m;
     int32_t skip_flag;                         // test fault injection, -1 = off
     int32_t b3d;                               // 1: map_b are 3-D {64 cols, K, cols/64} maps
+    int32_t glu;                               // 1: layer 1 is gated, H = act(X W1) * (X W3)
+    CUtensorMap map_b_lin;                     // glu: W3, laid out like map_b[0][0]
 };
+
+// Hidden columns one layer-1 tile produces: a gated tile spends its 256
+// accumulator columns on 128 gate and 128 linear columns of the same H slice.
+template <int MAX_E>
+__device__ __forceinline__ int32_t h_cols_per_tile(const Params<MAX_E>& p)
+{
+    return p.glu ? BN_CTA : BN;
+}
 
 // Everything in shared memory besides the stage ring (same offsets in both
 // CTAs of a pair, which the cross-CTA addressing relies on).
@@ -274,7 +284,7 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
             p.flags + static_cast<uint32_t>(task.y * n1) * FLAG_WORDS_PER_TILE + rank * EPI_WARPS;
         bool ok = true;
         for (int kb = 0; kb < nk && ok; ++kb) {
-            const int j = (kb * BK) / BN;   // layer-1 tile holding this H chunk
+            const int j = (kb * BK) / h_cols_per_tile(p);   // layer-1 tile holding this H chunk
             if (j >= ready_upto) {
                 ok = wait_h_chunks(w, band_flags, aux.epoch, j, n1, ready_upto,
                                    static_cast<uint32_t>(task.y * n1 + j));
@@ -321,9 +331,12 @@ __device__ void run_b_loader(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
         if (task.x < 0)
             break;
         const int L = task.x;
-        const CUtensorMap* mb = &p.map_b[L][expert_of(p, task.y)];
+        // A gated layer-1 tile: the leader CTA's B half is W1's 128 columns,
+        // the peer's half the same 128 columns of W3.
+        const bool gated = p.glu && L == 0;
+        const CUtensorMap* mb = (gated && rank == 1) ? &p.map_b_lin : &p.map_b[L][expert_of(p, task.y)];
         const int nk = (p.layer[L].K + BK - 1) / BK;
-        const int32_t col0 = task.z * BN + static_cast<int32_t>(rank) * BN_CTA;
+        const int32_t col0 = gated ? task.z * BN_CTA : task.z * BN + static_cast<int32_t>(rank) * BN_CTA;
         for (int kb = 0; kb < nk; ++kb) {
             if (!wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY))
                 return;
@@ -424,6 +437,28 @@ __device__ __forceinline__ void fetch_bias_slice(const __nv_bfloat16* bias, int3
     dst[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// Rounding and the row's store of 32 finished values at column col.
+__device__ __forceinline__ void store_row_chunk(const float (&v)[32], void* out, bool out_f32, int64_t row,
+                                                int64_t ld_out, int32_t col, int32_t ncols)
+{
+    const int nvalid = ncols - col < 32 ? ncols - col : 32;   // multiple of 8
+    if (out_f32) {
+        float* dst = static_cast<float*>(out) + row * ld_out + col;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q * 4 < nvalid)
+                reinterpret_cast<float4*>(dst)[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    } else {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + row * ld_out + col;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (q * 8 < nvalid)
+                reinterpret_cast<uint4*>(dst)[q] =
+                    make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                               pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+    }
+}
+
 // Bias, activation, rounding and the row's store for one 32-column chunk.
 // The activation is a template argument, chosen once per tile.
 template <int ACT>
@@ -442,24 +477,8 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&acc)[32], uint32_t 
         v[q * 4 + 2] = act_apply(ACT, __uint_as_float(acc[q * 4 + 2]) + b.z);
         v[q * 4 + 3] = act_apply(ACT, __uint_as_float(acc[q * 4 + 3]) + b.w);
     }
-    if (!row_ok)
-        return;
-    const int nvalid = ncols - col < 32 ? ncols - col : 32;   // multiple of 8
-    if (out_f32) {
-        float* dst = static_cast<float*>(out) + row * ld_out + col;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            if (q * 4 < nvalid)
-                reinterpret_cast<float4*>(dst)[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
-    } else {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + row * ld_out + col;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (q * 8 < nvalid)
-                reinterpret_cast<uint4*>(dst)[q] =
-                    make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                               pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-    }
+    if (row_ok)
+        store_row_chunk(v, out, out_f32, row, ld_out, col, ncols);
 }
 
 // Drain one 128 x BN accumulator quadrant-row by quadrant-row: chunk c+1's
@@ -486,6 +505,49 @@ __device__ __forceinline__ void drain_tile(uint32_t taddr, int nchunks, uint32_t
     }
 }
 
+// Drain a gated layer-1 tile: accumulator columns [0, 128) hold X W1 and
+// [128, 256) hold X W3 for the same 128 hidden columns; H = act(gate) * lin.
+template <int ACT>
+__device__ __forceinline__ void drain_glu(uint32_t taddr, int nchunks, bool row_ok, void* out, int64_t row,
+                                          int64_t ld_out, int32_t col_base, int32_t ncols)
+{
+    for (int c = 0; c < nchunks; ++c) {
+        uint32_t g[32], u[32];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
+        ptx::tmem_ld_32x32b_x32(taddr + BN_CTA + c * 32, u);
+        ptx::tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            v[i] = act_apply(ACT, __uint_as_float(g[i])) * __uint_as_float(u[i]);
+        if (row_ok)
+            store_row_chunk(v, out, false, row, ld_out, col_base + c * 32, ncols);
+    }
+}
+
+// One finished accumulator tile, with the activation resolved to a template
+// argument once.
+__device__ __forceinline__ void drain_any(int act, bool gated, uint32_t taddr, int nchunks, uint32_t bias_smem,
+                                          bool row_ok, void* out, bool out_f32, int64_t row, int64_t ld_out,
+                                          int32_t col_base, int32_t ncols)
+{
+#define TFFN_DRAIN(A)                                                                                        \
+    do {                                                                                                     \
+        if (gated)                                                                                           \
+            drain_glu<A>(taddr, nchunks, row_ok, out, row, ld_out, col_base, ncols);                         \
+        else                                                                                                 \
+            drain_tile<A>(taddr, nchunks, bias_smem, row_ok, out, out_f32, row, ld_out, col_base, ncols);    \
+    } while (0)
+    switch (act) {
+    case TFFN_ACT_GELU_TANH: TFFN_DRAIN(TFFN_ACT_GELU_TANH); break;
+    case TFFN_ACT_SILU: TFFN_DRAIN(TFFN_ACT_SILU); break;
+    case TFFN_ACT_RELU: TFFN_DRAIN(TFFN_ACT_RELU); break;
+    default: TFFN_DRAIN(TFFN_ACT_NONE); break;
+    }
+#undef TFFN_DRAIN
+}
+
 template <int MAX_E>
 __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w, uint32_t tmem_base,
                              uint32_t rank, int warp, int lane, float* bias_slice)
@@ -504,8 +566,10 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         const LayerArgs& la = p.layer[L];
         const uint32_t acc = iter & 1u;
         const uint32_t acc_phase = (iter >> 1) & 1u;
+        const bool gated = p.glu && L == 0;   // gated layer 1: no bias
         __syncwarp();   // the previous tile's reads of the slice are done
-        fetch_bias_slice(p.bias[L][expert_of(p, task.y)], task.z * BN, la.ncols, bias_slice, lane);
+        if (!gated)
+            fetch_bias_slice(p.bias[L][expert_of(p, task.y)], task.z * BN, la.ncols, bias_slice, lane);
         if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_full[acc]), acc_phase, SITE_TMEM_FULL))
             break;
         ptx::tc_fence_after();
@@ -520,16 +584,12 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         void* const out = la.out;
         const int64_t row = static_cast<int64_t>(task.y) * BM + rank * BM_CTA + quad * 32 + lane;
         const bool row_ok = row < la.rows;
-        const int32_t col_base = task.z * BN;
-        const int nchunks = ncols - col_base >= BN ? BN / 32 : (ncols - col_base + 31) / 32;
+        const int32_t tile_cols = gated ? BN_CTA : BN;
+        const int32_t col_base = task.z * tile_cols;
+        const int nchunks = ncols - col_base >= tile_cols ? tile_cols / 32 : (ncols - col_base + 31) / 32;
         const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * BN;
-        const uint32_t bias_smem = ptx::smem_u32(bias_slice);
-        if (act == TFFN_ACT_GELU_TANH)
-            drain_tile<TFFN_ACT_GELU_TANH>(taddr, nchunks, bias_smem, row_ok, out, out_f32, row, ld_out, col_base, ncols);
-        else if (act == TFFN_ACT_RELU)
-            drain_tile<TFFN_ACT_RELU>(taddr, nchunks, bias_smem, row_ok, out, out_f32, row, ld_out, col_base, ncols);
-        else
-            drain_tile<TFFN_ACT_NONE>(taddr, nchunks, bias_smem, row_ok, out, out_f32, row, ld_out, col_base, ncols);
+        drain_any(act, gated, taddr, nchunks, ptx::smem_u32(bias_slice), row_ok, out, out_f32, row, ld_out, col_base,
+                  ncols);
         // Accumulator drained: hand it back to the leader's MMA thread.
         ptx::tc_fence_before();
         __syncwarp();
@@ -592,6 +652,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
         if (MAX_E == 1) {
             ptx::prefetch_tmap(&p.map_b[0][0]);
             ptx::prefetch_tmap(&p.map_b[1][0]);
+            if (p.glu)
+                ptx::prefetch_tmap(&p.map_b_lin);
         }
     }
     if (warp == 1) {

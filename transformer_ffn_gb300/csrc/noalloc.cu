@@ -55,7 +55,7 @@ int map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint
 
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dim8(int64_t d) { return d >= 8 && d % 8 == 0 && d < (int64_t(1) << 31); }
-bool act_valid(int a) { return a == TFFN_ACT_NONE || a == TFFN_ACT_RELU || a == TFFN_ACT_GELU_TANH; }
+bool act_valid(int a) { return a == TFFN_ACT_NONE || a == TFFN_ACT_RELU || a == TFFN_ACT_GELU_TANH || a == TFFN_ACT_SILU; }
 
 // One-time set-up of the current device: the array's device address, the SM
 // count and the tensor-map encoder.

@@ -10,6 +10,7 @@ weights with the dimensions of Llama/Mixtral-class FFNs):
   b1 ~ U(-0.1, 0.1)          bf16, O
   W2 ~ N(0, 1/O)             bf16, O x P
   b2 ~ U(-0.1, 0.1)          bf16, P
+  W3 ~ N(0, 1/N)             bf16, N x O   (gated FFN only; no biases there)
   gate logits ~ N(0, 1)      fp32, T x E   (MoE only), plus a per-expert
                              offset beta_e that sets the router's skew:
       balanced   beta_e = 0                 (~T*k/E rows per expert)
@@ -56,6 +57,14 @@ class FFNInputs:
 
 
 @dataclass
+class GLUInputs:
+    X: torch.Tensor
+    W1: torch.Tensor
+    W3: torch.Tensor
+    W2: torch.Tensor
+
+
+@dataclass
 class MoEInputs:
     X: torch.Tensor
     logits: torch.Tensor
@@ -73,6 +82,17 @@ def ffn_inputs(M, N, O, P, seed=0, device="cpu", x_std=1.0) -> FFNInputs:
     W2 = _normal((O, P), (1.0 / O) ** 0.5, g, device)
     b2 = _uniform((P,), -0.1, 0.1, g, device)
     return FFNInputs(X, W1, b1, W2, b2)
+
+
+def glu_inputs(M, N, O, P, seed=0, device="cpu") -> GLUInputs:
+    """Gated FFN operands, drawn in the order X, W1, W3, W2 (no biases); W3 is
+    distributed like W1."""
+    g = _gen(device, seed)
+    X = _normal((M, N), 1.0, g, device)
+    W1 = _normal((N, O), (1.0 / N) ** 0.5, g, device)
+    W3 = _normal((N, O), (1.0 / N) ** 0.5, g, device)
+    W2 = _normal((O, P), (1.0 / O) ** 0.5, g, device)
+    return GLUInputs(X, W1, W3, W2)
 
 
 ROUTERS = ("balanced", "moderate", "stress")
