@@ -57,6 +57,7 @@ CONFIGS = {
                              "stress-skewed router (expert 0 in ~98% of tokens)"),
 }
 DEFAULT = "prefill"
+FFN_PATHS = {"auto": 0, "fused": 1, "decode": 2, "two": 3, "reduce": 4}
 FLUSH_BYTES = 256 << 20
 
 # Dominant kernel of each workload (for the ncu traffic record).
@@ -67,7 +68,19 @@ KERNEL_SOURCES = {
     "engine_kernel": ["engine.cuh", "common.cuh", "ptx.cuh", "schedule.h", "engine_dense.cu",
                       "engine_grouped.cu"],
     "decode_kernel": ["decode.cu", "decode.cuh", "common.cuh", "ptx.cuh"],
+    "reduce_kernel": ["reduce.cuh", "reduce_params.cuh", "engine.cuh", "common.cuh", "ptx.cuh", "engine_reduce.cu"],
 }
+
+
+def dominant_kernel(config, ffn_path="auto"):
+    """The kernel whose launches the roofline times for this workload."""
+    if ffn_path == "reduce" and CONFIGS[config]["kind"] == "ffn":
+        return "reduce_kernel"
+    if ffn_path == "decode" and CONFIGS[config]["kind"] == "ffn":
+        return "decode_kernel"
+    if ffn_path in ("fused", "two"):
+        return "engine_kernel"
+    return KERNEL[config]
 
 
 def flops(cfg):
@@ -117,18 +130,19 @@ def kernel_sha(kernel):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config):
+def recorded_traffic(config, kernel=None):
     """DRAM bytes per launch from the committed ncu record, if it was taken
     on the kernel source as it is now (else None)."""
+    kernel = kernel or KERNEL[config]
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_sha(KERNEL[config])
+    want = kernel_sha(kernel)
     for line in open(path):
         if line.startswith("#") or "=" not in line:
             continue
         kv = dict(p.split("=", 1) for p in line.split())
-        if kv.get("config") == config and kv.get("src_sha") == want:
+        if kv.get("config") == config and kv.get("kernel") == kernel and kv.get("src_sha") == want:
             return float(kv["dram_bytes_per_launch"])
     return None
 
@@ -341,6 +355,7 @@ def run_gpu(args, world, rank, local):
 
     tffn.load()
     tffn.set_option(tffn.OPT_MOE_ORDER, args.moe_order)
+    tffn.set_option(tffn.OPT_PATH, FFN_PATHS[args.ffn_path])
     cfg = CONFIGS[args.config]
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
@@ -385,9 +400,9 @@ def run_gpu(args, world, rank, local):
         roof = {"bound": "tensor", "achieved": flops(cfg) / dom_s / 1e12, "peak": peak_tf, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json {'hbm_gbs' if is_hbm_bound(cfg) else 'bf16_tflops'})"
-    roof["kernel"] = KERNEL[args.config]
+    roof["kernel"] = dominant_kernel(args.config, args.ffn_path)
     roof["kernel_ms"] = dom_s * 1e3
-    roof["traffic"] = recorded_traffic(args.config)
+    roof["traffic"] = recorded_traffic(args.config, roof["kernel"])
 
     # ---- end to end through the public API: every step uploads its input from
     # pinned host memory, runs the FFN and downloads its result.  Steps are
@@ -413,6 +428,8 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed_block": wall,
     }
+    if args.ffn_path != "auto":
+        line["config"]["path"] = args.ffn_path
     if cfg["kind"] == "moe":
         line["config"]["routed_rows"] = cfg["M"] * cfg["k"]
         line["config"]["router"] = cfg.get("router", "balanced")
@@ -529,6 +546,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT, choices=sorted(CONFIGS))
+    ap.add_argument("--ffn-path", default="auto", choices=sorted(FFN_PATHS),
+                    help="dense FFN path: auto, fused (engine), decode, two (two launches), "
+                         "reduce (the reduce-add form of the fused-FFN page, section Step 1)")
     ap.add_argument("--moe-order", type=int, default=1, choices=(0, 1),
                     help="MoE grouped-layout segment order: 0 expert index, 1 largest expert first")
     ap.add_argument("--impl", default="tffn", choices=["tffn", "reference"])

@@ -198,7 +198,12 @@ const char* tffn_status_string(int status);
 
 /* Tuning and test controls (process-wide):
  *   TFFN_OPT_PATH         0 auto, 1 fused engine, 2 decode stream, 3 engine
- *                         as two launches (layer 1, then layer 2)
+ *                         as two launches (layer 1, then layer 2), 4 the
+ *                         reduce-add form of "Kernel fusion and tensor
+ *                         parallelism", section "Step 1" (each H tile times
+ *                         its row of W2 tiles, reduced asynchronously into an
+ *                         fp32 Y; results vary in the last bits run to run);
+ *                         ffn_forward only
  *   TFFN_OPT_WAIT_LIMIT_MS  device wait limit in ms (default 4000)
  *   TFFN_OPT_SKIP_FLAG    test fault injection: the engine never publishes
  *                         the ready flag of this GEMM1 tile index (-1 = off);

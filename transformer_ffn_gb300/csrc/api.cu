@@ -15,6 +15,7 @@
 #include "decode.cuh"
 #include "engine.cuh"
 #include "launch.h"
+#include "reduce_params.cuh"
 #include "schedule.h"
 
 namespace {
@@ -125,6 +126,20 @@ int make_map_b(CUtensorMap* m, const void* base, int64_t ncols, int64_t K, bool 
                : make_map(m, base, static_cast<uint64_t>(ncols), static_cast<uint64_t>(K), 64, 64);
 }
 
+// fp32 [outer x inner] row-major, box {32, 32} with 128-byte swizzle: the
+// target of the reduce-add form's tile reductions.
+int make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer)
+{
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -1;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool act_ok(int a) { return a == TFFN_ACT_NONE || a == TFFN_ACT_RELU || a == TFFN_ACT_GELU_TANH || a == TFFN_ACT_SILU; }
 bool dim_ok(int64_t d) { return d >= 8 && d % 8 == 0 && d < (int64_t(1) << 31); }
@@ -228,7 +243,7 @@ uint64_t wait_limit_ns()
 
 // ------------------------------------------------------------------ layouts
 struct DenseLayout {
-    int path = 0;          // 1 engine fused, 2 decode, 3 engine two launches
+    int path = 0;          // 1 engine fused, 2 decode, 3 engine two launches, 4 reduce-add form
     int64_t m_blocks = 0;
     int32_t n1 = 0, n2 = 0;
     size_t off_h = 0;      // engine: H [m_blocks*BM x O]; decode: H [M x O]
@@ -246,8 +261,22 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, bool glu = 
         path = (M <= DECODE_MAX_M && !glu) ? 2 : 1;
     if (path == 2 && (M > DECODE_MAX_M || glu))
         path = 1;
+    if (path == 4 && glu)
+        path = 1;
     L.path = static_cast<int>(path);
     L.off_h = SYNC_BYTES;
+    if (L.path == 4) {
+        // the reduce-add form: an fp32 accumulator of Y instead of H; one
+        // counter per 32-row strip of each Y tile in the flag region
+        L.m_blocks = (M + engine::BM - 1) / engine::BM;
+        L.n1 = static_cast<int32_t>((O + engine::BN - 1) / engine::BN);
+        L.n2 = static_cast<int32_t>((P + engine::BN - 1) / engine::BN);
+        if (static_cast<size_t>(L.m_blocks) * L.n2 * reduce::COUNTERS_PER_TILE <= FLAG_WORDS) {
+            L.total = align_up(L.off_h + static_cast<size_t>(L.m_blocks) * engine::BM * P * 4, 256);
+            return L;
+        }
+        L.path = 1;
+    }
     if (L.path == 2) {
         const decode::Plan pl = decode::make_plan(M, N, O, P, 1);
         L.off_part = align_up(L.off_h + static_cast<size_t>(M) * O * 2, 256);
@@ -422,6 +451,47 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
             return TFFN_ERR_INVALID_ARG;
         timing_start(s);
         if (launch_decode(p, p.plan.grid, s) != 0)
+            return TFFN_ERR_CUDA;
+        timing_stop(s);
+        g_last_launches = 1;
+        return TFFN_OK;
+    }
+
+    if (L.path == 4) {
+        reduce::Params rp;
+        std::memset(&rp, 0, sizeof(rp));
+        float* acc = reinterpret_cast<float*>(base + L.off_h);
+        const int64_t rows_acc = L.m_blocks * engine::BM;
+        const bool b3d = (O % 64 == 0) && (P % 64 == 0);
+        if (make_map(&rp.map_x, X, N, M, 64, engine::BM_CTA) || make_map_b(&rp.map_w1, W1, O, N, b3d) ||
+            make_map_b(&rp.map_w2, W2, P, O, b3d) || make_map_f32(&rp.map_acc, acc, P, rows_acc))
+            return TFFN_ERR_INVALID_ARG;
+        rp.b1 = static_cast<const __nv_bfloat16*>(b1);
+        rp.b2 = static_cast<const __nv_bfloat16*>(b2);
+        rp.acc = acc;
+        rp.Y = static_cast<__nv_bfloat16*>(Y);
+        rp.counters = flags;
+        rp.ctrl = ctrl;
+        rp.wait_limit_ns = wait_limit_ns();
+        rp.M = M;
+        rp.N = static_cast<int32_t>(N);
+        rp.O = static_cast<int32_t>(O);
+        rp.P = static_cast<int32_t>(P);
+        rp.act1 = act1;
+        rp.act2 = act2;
+        rp.m_blocks = static_cast<int32_t>(L.m_blocks);
+        rp.n_h = L.n1;
+        rp.n_p = L.n2;
+        rp.b3d = b3d ? 1 : 0;
+        // the counters and the accumulator start at zero in every call
+        const size_t counter_bytes = static_cast<size_t>(L.m_blocks) * L.n2 * reduce::COUNTERS_PER_TILE * 4;
+        if (cudaMemsetAsync(flags, 0, counter_bytes, s) != cudaSuccess ||
+            cudaMemsetAsync(acc, 0, static_cast<size_t>(rows_acc) * P * 4, s) != cudaSuccess)
+            return TFFN_ERR_CUDA;
+        const int64_t total = L.m_blocks * static_cast<int64_t>(L.n1);
+        const int pairs = static_cast<int>(total < d->sms ? total : d->sms);
+        timing_start(s);
+        if (launch_reduce(rp, pairs, s) != 0)
             return TFFN_ERR_CUDA;
         timing_stop(s);
         g_last_launches = 1;

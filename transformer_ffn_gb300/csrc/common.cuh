@@ -27,6 +27,8 @@ enum WaitSite : uint32_t {
     SITE_DRAIN = 8,          // exit path waiting for its own copies / MMAs
     SITE_SLICE_FLAG = 9,     // decode layer 2 waiting for a hidden slice
     SITE_STAGE = 10,         // decode consumer waiting for a stage
+    SITE_H_SMEM = 11,        // reduce-add form: MMA waiting for the H tile in shared memory
+    SITE_H_FREE = 12,        // reduce-add form: epilogue waiting for the H tile's readers
 };
 
 // Control block at the start of the workspace (256 bytes).

@@ -179,7 +179,8 @@ struct Ring {
 
 // Read the next task from this CTA's ring and free the slot on the leader
 // (warp_wide: the whole warp waits, lane 0 arrives).  False on abort/timeout.
-__device__ __forceinline__ bool read_task(Aux& aux, const WaitCtx& w, Ring& r, uint32_t rank, bool warp_wide,
+template <class AuxT>
+__device__ __forceinline__ bool read_task(AuxT& aux, const WaitCtx& w, Ring& r, uint32_t rank, bool warp_wide,
                                           int lane, int4& task)
 {
     if (!wait_mbar_cl(w, ptx::smem_u32(&aux.task_full[r.slot]), r.phase, SITE_TASK_FULL))
