@@ -57,7 +57,7 @@ CONFIGS = {
                              "stress-skewed router (expert 0 in ~98% of tokens)"),
 }
 DEFAULT = "prefill"
-FFN_PATHS = {"auto": 0, "fused": 1, "decode": 2, "two": 3, "reduce": 4}
+FFN_PATHS = {"auto": 0, "fused": 1, "decode": 2, "two": 3, "reduce": 4, "b2b": 5}
 FLUSH_BYTES = 256 << 20
 
 # Dominant kernel of each workload (for the ncu traffic record).
@@ -69,6 +69,7 @@ KERNEL_SOURCES = {
                       "engine_grouped.cu"],
     "decode_kernel": ["decode.cu", "decode.cuh", "common.cuh", "ptx.cuh"],
     "reduce_kernel": ["reduce.cuh", "reduce_params.cuh", "engine.cuh", "common.cuh", "ptx.cuh", "engine_reduce.cu"],
+    "b2b_kernel": ["reduce.cuh", "reduce_params.cuh", "engine.cuh", "common.cuh", "ptx.cuh", "engine_reduce.cu"],
 }
 
 
@@ -76,6 +77,8 @@ def dominant_kernel(config, ffn_path="auto"):
     """The kernel whose launches the roofline times for this workload."""
     if ffn_path == "reduce" and CONFIGS[config]["kind"] == "ffn":
         return "reduce_kernel"
+    if ffn_path == "b2b" and CONFIGS[config]["kind"] == "ffn":
+        return "b2b_kernel"
     if ffn_path == "decode" and CONFIGS[config]["kind"] == "ffn":
         return "decode_kernel"
     if ffn_path in ("fused", "two"):
@@ -548,7 +551,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT, choices=sorted(CONFIGS))
     ap.add_argument("--ffn-path", default="auto", choices=sorted(FFN_PATHS),
                     help="dense FFN path: auto, fused (engine), decode, two (two launches), "
-                         "reduce (the reduce-add form of the fused-FFN page, section Step 1)")
+                         "reduce (the reduce-add form of the fused-FFN page, section Step 1), "
+                         "b2b (back-to-back, H on chip)")
     ap.add_argument("--moe-order", type=int, default=1, choices=(0, 1),
                     help="MoE grouped-layout segment order: 0 expert index, 1 largest expert first")
     ap.add_argument("--impl", default="tffn", choices=["tffn", "reference"])

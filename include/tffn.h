@@ -202,8 +202,11 @@ const char* tffn_status_string(int status);
  *                         reduce-add form of "Kernel fusion and tensor
  *                         parallelism", section "Step 1" (each H tile times
  *                         its row of W2 tiles, reduced asynchronously into an
- *                         fp32 Y; results vary in the last bits run to run);
- *                         ffn_forward only
+ *                         fp32 Y; results vary in the last bits run to run),
+ *                         5 back-to-back (each task walks the hidden tiles of
+ *                         one band for one Y tile, H only in shared memory,
+ *                         products summed in tensor memory; for small FFNs);
+ *                         4 and 5 apply to ffn_forward only
  *   TFFN_OPT_WAIT_LIMIT_MS  device wait limit in ms (default 4000)
  *   TFFN_OPT_SKIP_FLAG    test fault injection: the engine never publishes
  *                         the ready flag of this GEMM1 tile index (-1 = off);

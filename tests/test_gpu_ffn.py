@@ -85,6 +85,16 @@ def test_decode_path_full(cuda_lib, shape, acts):
     _assert_close(Y.float().cpu().numpy(), _oracle(inp, *acts), f"decode {shape}")
 
 
+@pytest.mark.parametrize("path", [1, 3])
+@pytest.mark.parametrize("shape", [(16, 4096, 1024, 256), (64, 2048, 256, 512), (300, 1024, 136, 200)])
+def test_engine_input_wider_than_hidden(cuda_lib, path, shape):
+    # N > O: a layer-1 tile has more k-blocks than there are H tiles (a
+    # down-projecting FFN); layer-1 tasks must not wait on H flags
+    inp = _case(*shape, seed=sum(shape))
+    Y = _run(cuda_lib, inp, "gelu_tanh", "none", path=path)
+    _assert_close(Y.float().cpu().numpy(), _oracle(inp, "gelu_tanh", "none"), f"N > O {shape}")
+
+
 def test_fused_equals_two_launches_bitwise(cuda_lib):
     inp = _case(300, 256, 1024, 384, seed=3)
     a = _run(cuda_lib, inp, "gelu_tanh", "none", path=1)

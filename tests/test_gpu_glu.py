@@ -36,6 +36,7 @@ def _assert_close(got, want, what=""):
     (200, 128, 256, 128, "relu"),        # ReGLU
     (96, 64, 128, 64, "none"),           # bilinear
     (16, 512, 640, 256, "silu"),         # decode-sized batch (engine path)
+    (64, 2048, 256, 256, "silu"),        # N > O: more layer-1 k-blocks than H tiles
 ])
 def test_glu_small_full(cuda_lib, M, N, O, P, act):
     X, W1, W3, W2 = _inputs(M, N, O, P, seed=M + O)

@@ -51,6 +51,7 @@ def _check_routing(r, logits, k, E):
     (1, 64, 128, 64, 8, 2, ("gelu_tanh", "none")),
     (40, 64, 128, 64, 1, 1, ("relu", "none")),
     (50, 64, 128, 64, 4, 4, ("gelu_tanh", "none")),      # top_k = E
+    (200, 1024, 256, 128, 4, 2, ("gelu_tanh", "none")),  # N > O
 ])
 def test_moe_small_full(cuda_lib, T, N, O, P, E, k, acts):
     inp = _inputs(T, N, O, P, E, seed=T + E)

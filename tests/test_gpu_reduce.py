@@ -80,3 +80,53 @@ def test_reduce_form_full_size_sampled_rows(reduce_path):
     rows = [0, 255, 2048, 4095]
     _assert_close(Y[rows].float().cpu().numpy(), _oracle(inp, ("gelu_tanh", "none"), rows=rows), "full size")
     assert torch.isfinite(Y.float()).all()
+
+
+# ------------------------------------------------- back-to-back form (path 5)
+# Each task walks the hidden tiles of one band for one Y tile; H lives only in
+# shared memory and the products are summed in tensor memory (no reductions),
+# so the results are bit-reproducible.
+
+@pytest.fixture
+def b2b_path(cuda_lib):
+    prev = cuda_lib.set_option(cuda_lib.OPT_PATH, 5)
+    yield cuda_lib
+    cuda_lib.set_option(cuda_lib.OPT_PATH, prev)
+
+
+@pytest.mark.parametrize("M,N,O,P,acts", [
+    (64, 256, 1024, 256, ("gelu_tanh", "none")),     # the tiny FFN: one task
+    (300, 136, 328, 200, ("gelu_tanh", "relu")),     # ragged rows, hidden and output tails, 2-D maps
+    (513, 64, 512, 576, ("relu", "gelu_tanh")),      # three bands x three Y tiles
+    (16, 512, 256, 128, ("silu", "none")),           # one hidden tile
+    (8, 64, 4096, 64, ("gelu_tanh", "none")),        # sixteen hidden tiles summed in tensor memory
+])
+def test_b2b_form_small_full(b2b_path, M, N, O, P, acts):
+    inp = synth.ffn_inputs(M, N, O, P, seed=M + O, device="cuda")
+    Y = b2b_path.ffn_forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, *acts)
+    b2b_path.check()
+    assert b2b_path.last_launch_count() == 1
+    _assert_close(Y.float().cpu().numpy(), _oracle(inp, acts), "b2b form")
+
+
+def test_b2b_form_deterministic_and_close_to_engine(b2b_path):
+    inp = synth.ffn_inputs(700, 256, 1536, 512, seed=4, device="cuda")
+    a = b2b_path.ffn_forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh", "none")
+    b = b2b_path.ffn_forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh", "none")
+    b2b_path.set_option(b2b_path.OPT_PATH, 1)
+    e = b2b_path.ffn_forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh", "none")
+    b2b_path.check()
+    assert torch.equal(a, b)
+    d = (a.float() - e.float()).abs()
+    assert torch.all(d <= 2e-2 + 2e-2 * e.float().abs())
+
+
+def test_b2b_form_full_size_sampled_rows(b2b_path):
+    # the prefill workload through the back-to-back form (H recomputed for each
+    # of the 16 Y tiles of a band): slow, but exact
+    M, N, O, P = 4096, 4096, 16384, 4096
+    inp = synth.ffn_inputs(M, N, O, P, seed=0, device="cuda")
+    Y = b2b_path.ffn_forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh", "none")
+    b2b_path.check()
+    rows = [1, 1000, 4095]
+    _assert_close(Y[rows].float().cpu().numpy(), _oracle(inp, ("gelu_tanh", "none"), rows=rows), "b2b full size")

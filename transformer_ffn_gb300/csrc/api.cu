@@ -243,7 +243,8 @@ uint64_t wait_limit_ns()
 
 // ------------------------------------------------------------------ layouts
 struct DenseLayout {
-    int path = 0;          // 1 engine fused, 2 decode, 3 engine two launches, 4 reduce-add form
+    int path = 0;          // 1 engine fused, 2 decode, 3 engine two launches, 4 reduce-add form,
+                           // 5 back-to-back (H on chip)
     int64_t m_blocks = 0;
     int32_t n1 = 0, n2 = 0;
     size_t off_h = 0;      // engine: H [m_blocks*BM x O]; decode: H [M x O]
@@ -261,7 +262,7 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, bool glu = 
         path = (M <= DECODE_MAX_M && !glu) ? 2 : 1;
     if (path == 2 && (M > DECODE_MAX_M || glu))
         path = 1;
-    if (path == 4 && glu)
+    if ((path == 4 || path == 5) && glu)
         path = 1;
     L.path = static_cast<int>(path);
     L.off_h = SYNC_BYTES;
@@ -276,6 +277,14 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, bool glu = 
             return L;
         }
         L.path = 1;
+    }
+    if (L.path == 5) {
+        // back-to-back: nothing but the control block
+        L.m_blocks = (M + engine::BM - 1) / engine::BM;
+        L.n1 = static_cast<int32_t>((O + engine::BN - 1) / engine::BN);
+        L.n2 = static_cast<int32_t>((P + engine::BN - 1) / engine::BN);
+        L.total = SYNC_BYTES;
+        return L;
     }
     if (L.path == 2) {
         const decode::Plan pl = decode::make_plan(M, N, O, P, 1);
@@ -457,14 +466,14 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
         return TFFN_OK;
     }
 
-    if (L.path == 4) {
+    if (L.path == 4 || L.path == 5) {
         reduce::Params rp;
         std::memset(&rp, 0, sizeof(rp));
         float* acc = reinterpret_cast<float*>(base + L.off_h);
         const int64_t rows_acc = L.m_blocks * engine::BM;
         const bool b3d = (O % 64 == 0) && (P % 64 == 0);
         if (make_map(&rp.map_x, X, N, M, 64, engine::BM_CTA) || make_map_b(&rp.map_w1, W1, O, N, b3d) ||
-            make_map_b(&rp.map_w2, W2, P, O, b3d) || make_map_f32(&rp.map_acc, acc, P, rows_acc))
+            make_map_b(&rp.map_w2, W2, P, O, b3d) || (L.path == 4 && make_map_f32(&rp.map_acc, acc, P, rows_acc)))
             return TFFN_ERR_INVALID_ARG;
         rp.b1 = static_cast<const __nv_bfloat16*>(b1);
         rp.b2 = static_cast<const __nv_bfloat16*>(b2);
@@ -483,6 +492,16 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
         rp.n_h = L.n1;
         rp.n_p = L.n2;
         rp.b3d = b3d ? 1 : 0;
+        if (L.path == 5) {   // one task per (band, Y tile)
+            const int64_t total = L.m_blocks * static_cast<int64_t>(L.n2);
+            const int pairs = static_cast<int>(total < d->sms ? total : d->sms);
+            timing_start(s);
+            if (launch_b2b(rp, pairs, s) != 0)
+                return TFFN_ERR_CUDA;
+            timing_stop(s);
+            g_last_launches = 1;
+            return TFFN_OK;
+        }
         // the counters and the accumulator start at zero in every call
         const size_t counter_bytes = static_cast<size_t>(L.m_blocks) * L.n2 * reduce::COUNTERS_PER_TILE * 4;
         if (cudaMemsetAsync(flags, 0, counter_bytes, s) != cudaSuccess ||

@@ -285,7 +285,9 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
             p.flags + static_cast<uint32_t>(task.y * n1) * FLAG_WORDS_PER_TILE + rank * EPI_WARPS;
         bool ok = true;
         for (int kb = 0; kb < nk && ok; ++kb) {
-            const int j = (kb * BK) / h_cols_per_tile(p);   // layer-1 tile holding this H chunk
+            // Layer 2 only: the k-block reads H, whose chunk comes from
+            // layer-1 tile j (a layer-1 task's k runs over N, not over H).
+            const int j = wait_h ? (kb * BK) / h_cols_per_tile(p) : 0;
             if (j >= ready_upto) {
                 ok = wait_h_chunks(w, band_flags, aux.epoch, j, n1, ready_upto,
                                    static_cast<uint32_t>(task.y * n1 + j));

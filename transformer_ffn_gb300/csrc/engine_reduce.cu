@@ -1,5 +1,6 @@
-// engine_reduce.cu -- cluster launch of the reduce-add form (reduce.cuh):
-// clusters of two CTAs, grid capped at the CTA pairs the GPU keeps resident.
+// engine_reduce.cu -- cluster launches of the reduce-add and back-to-back
+// forms (reduce.cuh): clusters of two CTAs, grid capped at the CTA pairs the
+// GPU keeps resident.
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -7,10 +8,13 @@
 
 namespace tffn {
 
-int launch_reduce(const reduce::Params& p, int max_pairs, cudaStream_t s)
+namespace {
+
+using KernelFn = void (*)(reduce::Params);
+
+int launch_pairs(KernelFn kernel, bool& ready, int& resident_pairs, const reduce::Params& p, int max_pairs,
+                 cudaStream_t s)
 {
-    static bool ready = false;
-    static int resident_pairs = 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -23,12 +27,12 @@ int launch_reduce(const reduce::Params& p, int max_pairs, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!ready) {
-        if (cudaFuncSetAttribute(reduce::reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 reduce::SMEM_BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, reduce::SMEM_BYTES) !=
+            cudaSuccess)
             return -1;
         cfg.gridDim = dim3(2);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, reduce::reduce_kernel, &cfg) != cudaSuccess || n < 1)
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1)
             return -1;
         resident_pairs = n;
         ready = true;
@@ -37,9 +41,25 @@ int launch_reduce(const reduce::Params& p, int max_pairs, cudaStream_t s)
     if (pairs < 1)
         pairs = 1;
     cfg.gridDim = dim3(2 * pairs);
-    if (cudaLaunchKernelEx(&cfg, reduce::reduce_kernel, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess)
         return -1;
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int launch_reduce(const reduce::Params& p, int max_pairs, cudaStream_t s)
+{
+    static bool ready = false;
+    static int resident_pairs = 0;
+    return launch_pairs(reduce::reduce_kernel, ready, resident_pairs, p, max_pairs, s);
+}
+
+int launch_b2b(const reduce::Params& p, int max_pairs, cudaStream_t s)
+{
+    static bool ready = false;
+    static int resident_pairs = 0;
+    return launch_pairs(reduce::b2b_kernel, ready, resident_pairs, p, max_pairs, s);
 }
 
 }  // namespace tffn

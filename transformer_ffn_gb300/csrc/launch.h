@@ -26,6 +26,7 @@ int launch_engine_dense(const engine::Params<1>& p, int max_pairs, cudaStream_t 
 int launch_engine_grouped(const engine::Params<MOE_MAX_E>& p, int max_pairs, cudaStream_t s);
 int launch_decode(const decode::Params& p, int grid, cudaStream_t s);
 int launch_reduce(const reduce::Params& p, int max_pairs, cudaStream_t s);
+int launch_b2b(const reduce::Params& p, int max_pairs, cudaStream_t s);
 
 int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w,
                      cudaStream_t s);
