@@ -47,6 +47,8 @@ CONFIGS = {
     "swiglu": dict(kind="glu", M=4096, N=4096, O=14336, P=4096, act1="silu", act2="none",
                    label="SwiGLU FFN (Llama 3 8B shape) M=4096 N=4096 O=14336 P=4096, "
                          "Y = (SiLU(X W1) * (X W3)) W2, no biases"),
+    "swiglu_decode": dict(kind="glu", M=16, N=4096, O=14336, P=4096, act1="silu", act2="none",
+                          label="SwiGLU FFN decode (Llama 3 8B shape) M=16 N=4096 O=14336 P=4096"),
     "moe_moderate": dict(kind="moe", M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="gelu_tanh",
                          act2="none", router="moderate",
                          label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh, "
@@ -62,7 +64,7 @@ FLUSH_BYTES = 256 << 20
 
 # Dominant kernel of each workload (for the ncu traffic record).
 KERNEL = {"tiny": "engine_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
-          "swiglu": "engine_kernel", "moe": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
+          "swiglu": "engine_kernel", "swiglu_decode": "decode_kernel", "moe": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
           "decode": "decode_kernel"}
 KERNEL_SOURCES = {
     "engine_kernel": ["engine.cuh", "common.cuh", "ptx.cuh", "schedule.h", "engine_dense.cu",
@@ -95,13 +97,16 @@ def flops(cfg):
 
 
 def weight_bytes(cfg):
-    """Bytes the decode step must move: W1, W2, X, Y, b1, b2 (bf16)."""
+    """Bytes the decode step must move: W1, W2, X, Y, b1, b2 (bf16); the gated
+    FFN reads W1, W3, W2 and has no biases."""
     M, N, O, P = cfg["M"], cfg["N"], cfg["O"], cfg["P"]
+    if cfg["kind"] == "glu":
+        return 2.0 * (2 * N * O + O * P + M * N + M * P)
     return 2.0 * (N * O + O * P + M * N + M * P + O + P)
 
 
 def is_hbm_bound(cfg):
-    return cfg["kind"] == "ffn" and cfg["M"] <= 32
+    return cfg["kind"] in ("ffn", "glu") and cfg["M"] <= 32
 
 
 def metric_of(cfg):

@@ -99,9 +99,10 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
  *
  * Numerics: products accumulate in fp32; H = act(X W1) * (X W3) is rounded to
  * bf16 (nearest even) where it is stored between the layers; Y is rounded to
- * bf16.  Path: always the persistent tcgen05 engine; each layer-1 tile pairs
- * 128 columns of W1 with the same 128 columns of W3 in one 256-column
- * accumulator.  Errors and workspace as ffn_forward.
+ * bf16.  Paths: M <= 32 streams the weights (each layer-1 unit loads the same
+ * 64 columns of W1 and W3); larger M runs the persistent tcgen05 engine, each
+ * layer-1 tile pairing 128 columns of W1 with the same 128 columns of W3 in
+ * one 256-column accumulator.  Errors and workspace as ffn_forward.
  */
 int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W2, int act, int64_t M,
                     int64_t N, int64_t O, int64_t P, void* Y, struct CUstream_st* stream);
@@ -178,7 +179,10 @@ int ffn_forward_decode_noalloc(const void* X, const void* W1, const void* b1, co
                                const void* b2, int act1, int act2, int64_t M, int64_t N, int64_t O,
                                int64_t P, void* Y, struct CUstream_st* stream);
 
-/* Bytes of workspace a call of this shape needs (E = 0 for ffn_forward). */
+/* Bytes of workspace a call of this shape needs on the current device
+ * (E = 0: ffn_forward or ffn_glu_forward, whichever needs more; E >= 1:
+ * moe_ffn_forward with top_k).  Without a usable device the decode part is
+ * sized for up to 1024 CTAs. */
 size_t tffn_workspace_bytes(int64_t M, int64_t N, int64_t O, int64_t P, int E, int top_k);
 
 /* Use a caller-owned device buffer (>= 256-byte aligned) as the workspace of

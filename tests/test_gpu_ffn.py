@@ -77,6 +77,8 @@ def test_engine_ragged_shapes(cuda_lib, shape, acts):
     ((17, 1024, 2048, 512), ("relu", "gelu_tanh")),     # two m tiles
     ((32, 64, 128, 64), ("gelu_tanh", "none")),
     ((8, 4096, 8192, 1024), ("relu", "none")),          # long split-K ranges
+    ((16, 4096, 1024, 256), ("gelu_tanh", "none")),     # N > O: more layer-1 k than hidden columns
+    ((4, 2048, 136, 4096), ("relu", "none")),           # N > O, narrow ragged hidden, wide output
 ])
 def test_decode_path_full(cuda_lib, shape, acts):
     M, N, O, P = shape

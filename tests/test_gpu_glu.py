@@ -108,3 +108,47 @@ def test_dense_ffn_with_silu_on_both_paths(cuda_lib):
         want = oracle.ffn(u(inp.X), u(inp.W1), u(inp.b1), u(inp.W2), u(inp.b2), oracle.ACT_SILU,
                           oracle.ACT_SILU)
         _assert_close(Y.float().cpu().numpy(), want, f"silu M={M}")
+
+
+# ------------------------------------------------ weight-streaming path, M <= 32
+
+@pytest.mark.parametrize("M,N,O,P,act", [
+    (1, 256, 384, 136, "silu"),
+    (5, 136, 200, 264, "silu"),          # hidden tail: 200 = 3 x 64 + 8
+    (16, 2048, 136, 4096, "gelu_tanh"),  # N > O, narrow hidden
+    (32, 1024, 2048, 512, "silu"),       # two 16-row tiles
+    (8, 4096, 8192, 1024, "relu"),       # long split-K ranges
+])
+def test_glu_decode_path_full(cuda_lib, M, N, O, P, act):
+    X, W1, W3, W2 = _inputs(M, N, O, P, seed=3 * M + O)
+    prev = cuda_lib.set_option(cuda_lib.OPT_PATH, 2)
+    try:
+        Y = cuda_lib.ffn_glu_forward(X, W1, W3, W2, act)
+        assert cuda_lib.last_launch_count() == 1
+    finally:
+        cuda_lib.set_option(cuda_lib.OPT_PATH, prev)
+    cuda_lib.check()
+    _assert_close(Y.float().cpu().numpy(), _oracle(X, W1, W3, W2, act), f"glu decode {act}")
+
+
+def test_glu_decode_deterministic_and_close_to_engine(cuda_lib):
+    X, W1, W3, W2 = _inputs(24, 1024, 3072, 1024, seed=12)
+    a = cuda_lib.ffn_glu_forward(X, W1, W3, W2, "silu")      # auto: the weight stream at M <= 32
+    b = cuda_lib.ffn_glu_forward(X, W1, W3, W2, "silu")
+    prev = cuda_lib.set_option(cuda_lib.OPT_PATH, 1)
+    try:
+        e = cuda_lib.ffn_glu_forward(X, W1, W3, W2, "silu")
+    finally:
+        cuda_lib.set_option(cuda_lib.OPT_PATH, prev)
+    cuda_lib.check()
+    assert torch.equal(a, b)
+    d = (a.float() - e.float()).abs()
+    assert torch.all(d <= 2e-2 + 2e-2 * e.float().abs())
+
+
+def test_glu_decode_llama3_8b_full(cuda_lib):
+    # decode step of the Llama 3 8B SwiGLU FFN: M 16, N 4096, O 14336, P 4096
+    X, W1, W3, W2 = _inputs(16, 4096, 14336, 4096, seed=0)
+    Y = cuda_lib.ffn_glu_forward(X, W1, W3, W2, "silu")
+    cuda_lib.check()
+    _assert_close(Y.float().cpu().numpy(), _oracle(X, W1, W3, W2, "silu"), "glu decode 8B")

@@ -252,15 +252,16 @@ struct DenseLayout {
     size_t total = 0;
 };
 
-// glu: the gated form, whose layer-1 tiles cover 128 hidden columns each and
-// which has no weight-streaming (decode) path.
-DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, bool glu = false)
+// glu: the gated form, whose layer-1 engine tiles cover 128 hidden columns
+// each (and decode slices 64).  sms: the CTA count the decode launch plans
+// for (its split-K partial area depends on it).
+DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, int sms, bool glu = false)
 {
     DenseLayout L;
     int64_t path = g_opt_path.load();
     if (path == 0)
-        path = (M <= DECODE_MAX_M && !glu) ? 2 : 1;
-    if (path == 2 && (M > DECODE_MAX_M || glu))
+        path = (M <= DECODE_MAX_M) ? 2 : 1;
+    if (path == 2 && M > DECODE_MAX_M)
         path = 1;
     if ((path == 4 || path == 5) && glu)
         path = 1;
@@ -287,7 +288,7 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, bool glu = 
         return L;
     }
     if (L.path == 2) {
-        const decode::Plan pl = decode::make_plan(M, N, O, P, 1);
+        const decode::Plan pl = decode::make_plan(M, N, O, P, sms, glu);
         L.off_part = align_up(L.off_h + static_cast<size_t>(M) * O * 2, 256);
         L.total = L.off_part + pl.partial_bytes;
         return L;
@@ -351,6 +352,52 @@ void fill_layer(engine::LayerArgs& la, int64_t K, int64_t ncols, int act, int ou
 }
 
 }  // namespace
+
+// The weight-streaming decode launch (dense, or gated when W3 is given).
+static int run_decode(DeviceState& d, uint8_t* base, const DenseLayout& L, const void* X, const void* W1,
+                      const void* W3, const void* b1, const void* W2, const void* b2, int act1, int act2, int64_t M,
+                      int64_t N, int64_t O, int64_t P, void* Y, cudaStream_t s)
+{
+    int rc = count_launch(d, base, s);
+    if (rc != TFFN_OK)
+        return rc;
+    const bool glu = W3 != nullptr;
+    decode::Params p{};
+    p.X = static_cast<const __nv_bfloat16*>(X);
+    p.W1 = static_cast<const __nv_bfloat16*>(W1);
+    p.b1 = static_cast<const __nv_bfloat16*>(b1);
+    p.W2 = static_cast<const __nv_bfloat16*>(W2);
+    p.b2 = static_cast<const __nv_bfloat16*>(b2);
+    p.Y = static_cast<__nv_bfloat16*>(Y);
+    p.H = reinterpret_cast<__nv_bfloat16*>(base + L.off_h);
+    p.partial = reinterpret_cast<float*>(base + L.off_part);
+    p.counters = reinterpret_cast<uint32_t*>(base + OFF_DCOUNT);
+    p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+    p.ctrl = reinterpret_cast<DevCtrl*>(base);
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.O = static_cast<int32_t>(O);
+    p.P = static_cast<int32_t>(P);
+    p.act1 = act1;
+    p.act2 = act2;
+    p.glu = glu ? 1 : 0;
+    p.wait_limit_ns = wait_limit_ns();
+    p.plan = decode::make_plan(M, N, O, P, d.sms, glu);
+    if (static_cast<size_t>(p.plan.slices[0]) * 4 > FLAG_WORDS ||
+        (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * 4 > DCOUNT_WORDS)
+        return TFFN_ERR_UNSUPPORTED;
+    const uint32_t arows = M <= 16 ? 16u : 32u;
+    if (make_map(&p.map_w[0], W1, O, N, 64, decode::KC) || make_map(&p.map_w[1], W2, P, O, 64, decode::KC) ||
+        make_map(&p.map_a[0], X, N, M, 64, arows) || make_map(&p.map_a[1], p.H, O, M, 64, arows) ||
+        (glu && make_map(&p.map_w3, W3, O, N, 64, decode::KC)))
+        return TFFN_ERR_INVALID_ARG;
+    timing_start(s);
+    if (launch_decode(p, p.plan.grid, s) != 0)
+        return TFFN_ERR_CUDA;
+    timing_stop(s);
+    g_last_launches = 1;
+    return TFFN_OK;
+}
 
 // Launch the dense engine as the layout says: one fused launch, or layer 1
 // and layer 2 as two launches.
@@ -420,7 +467,7 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
     int rc = device_state(&d);
     if (rc != TFFN_OK)
         return rc;
-    const DenseLayout L = dense_layout(M, N, O, P);
+    const DenseLayout L = dense_layout(M, N, O, P, d->sms);
     uint8_t* base = nullptr;
     rc = workspace(*d, L.total, s, &base);
     if (rc != TFFN_OK)
@@ -428,43 +475,8 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
     DevCtrl* ctrl = reinterpret_cast<DevCtrl*>(base);
     uint32_t* flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
 
-    if (L.path == 2) {
-        if ((rc = count_launch(*d, base, s)) != TFFN_OK)
-            return rc;
-        decode::Params p{};
-        p.X = static_cast<const __nv_bfloat16*>(X);
-        p.W1 = static_cast<const __nv_bfloat16*>(W1);
-        p.b1 = static_cast<const __nv_bfloat16*>(b1);
-        p.W2 = static_cast<const __nv_bfloat16*>(W2);
-        p.b2 = static_cast<const __nv_bfloat16*>(b2);
-        p.Y = static_cast<__nv_bfloat16*>(Y);
-        p.H = reinterpret_cast<__nv_bfloat16*>(base + L.off_h);
-        p.partial = reinterpret_cast<float*>(base + L.off_part);
-        p.counters = reinterpret_cast<uint32_t*>(base + OFF_DCOUNT);
-        p.flags = flags;
-        p.ctrl = ctrl;
-        p.M = static_cast<int32_t>(M);
-        p.N = static_cast<int32_t>(N);
-        p.O = static_cast<int32_t>(O);
-        p.P = static_cast<int32_t>(P);
-        p.act1 = act1;
-        p.act2 = act2;
-        p.wait_limit_ns = wait_limit_ns();
-        p.plan = decode::make_plan(M, N, O, P, d->sms);
-        if (static_cast<size_t>(p.plan.slices[0]) * 4 > FLAG_WORDS ||
-            (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * 4 > DCOUNT_WORDS)
-            return TFFN_ERR_UNSUPPORTED;
-        const uint32_t arows = M <= 16 ? 16u : 32u;
-        if (make_map(&p.map_w[0], W1, O, N, 64, decode::KC) || make_map(&p.map_w[1], W2, P, O, 64, decode::KC) ||
-            make_map(&p.map_a[0], X, N, M, 64, arows) || make_map(&p.map_a[1], p.H, O, M, 64, arows))
-            return TFFN_ERR_INVALID_ARG;
-        timing_start(s);
-        if (launch_decode(p, p.plan.grid, s) != 0)
-            return TFFN_ERR_CUDA;
-        timing_stop(s);
-        g_last_launches = 1;
-        return TFFN_OK;
-    }
+    if (L.path == 2)
+        return run_decode(*d, base, L, X, W1, nullptr, b1, W2, b2, act1, act2, M, N, O, P, Y, s);
 
     if (L.path == 4 || L.path == 5) {
         reduce::Params rp;
@@ -553,11 +565,13 @@ int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W
     int rc = device_state(&d);
     if (rc != TFFN_OK)
         return rc;
-    const DenseLayout L = dense_layout(M, N, O, P, true);
+    const DenseLayout L = dense_layout(M, N, O, P, d->sms, true);
     uint8_t* base = nullptr;
     rc = workspace(*d, L.total, s, &base);
     if (rc != TFFN_OK)
         return rc;
+    if (L.path == 2)
+        return run_decode(*d, base, L, X, W1, W3, nullptr, W2, nullptr, act, TFFN_ACT_NONE, M, N, O, P, Y, s);
 
     engine::Params<1> p;
     std::memset(&p, 0, sizeof(p));
@@ -688,8 +702,20 @@ size_t tffn_workspace_bytes(int64_t M, int64_t N, int64_t O, int64_t P, int E, i
 {
     if (M < 0 || !dim_ok(N) || !dim_ok(O) || !dim_ok(P))
         return 0;
-    if (E <= 0)
-        return dense_layout(M, N, O, P).total;
+    if (E <= 0) {
+        // the dense and the gated FFN, on the current device (or, without
+        // one, planned for up to 1024 CTAs)
+        int sms = 1024;
+        DeviceState* d = nullptr;
+        {
+            std::lock_guard<std::mutex> lock(g_mu);
+            if (device_state(&d) == TFFN_OK)
+                sms = d->sms;
+        }
+        const size_t a = dense_layout(M, N, O, P, sms).total;
+        const size_t b = dense_layout(M, N, O, P, sms, true).total;
+        return a > b ? a : b;
+    }
     if (top_k < 1 || top_k > E)
         return 0;
     return moe_layout(M, N, O, P, E, top_k).total;

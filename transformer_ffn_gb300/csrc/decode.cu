@@ -8,7 +8,7 @@
 namespace tffn {
 namespace decode {
 
-static_assert(SLICE == KC, "layer 2 reads exactly one layer-1 slice of H per unit");
+static_assert(SLICE == KC, "a layer-2 unit reads one dense (or two gated) layer-1 slices of H");
 
 struct Aux {
     uint64_t full[STAGES];
@@ -68,11 +68,13 @@ __device__ __forceinline__ void zero(Acc<MT>& a)
 // fragments of four k-steps are loaded first and the MMAs issued after, so the
 // shared-memory latency of the loads overlaps instead of sitting in front of
 // every MMA.
-template <int MT>
+// Gated (GLU): n8 tiles 0-1 come from the W1 box and 2-3 from the W3 box,
+// the same 16 columns (chunks 2cw, 2cw+1) of each.
+template <int MT, bool GLU>
 __device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uint32_t a_base, int cw, int lane)
 {
-    const uint32_t wbox = w_base + static_cast<uint32_t>(cw >> 1) * W_BOX_BYTES;
-    const uint32_t cb_chunk = static_cast<uint32_t>(cw & 1) * 4;   // 32 columns = 4 chunks
+    const uint32_t wbox_dense = w_base + static_cast<uint32_t>(cw >> 1) * W_BOX_BYTES;
+    const uint32_t cb_chunk = GLU ? static_cast<uint32_t>(cw) * 2 : static_cast<uint32_t>(cw & 1) * 4;
     const uint32_t j = static_cast<uint32_t>(lane >> 3);
     const uint32_t r = static_cast<uint32_t>(lane & 7);
 #pragma unroll
@@ -92,7 +94,8 @@ __device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uin
             const uint32_t krow = static_cast<uint32_t>(ks * 16) + (j & 1u) * 8u + r;
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr) {
-                const uint32_t nchunk = cb_chunk + static_cast<uint32_t>(pr * 2) + (j >> 1);
+                const uint32_t wbox = GLU ? w_base + static_cast<uint32_t>(pr) * W_BOX_BYTES : wbox_dense;
+                const uint32_t nchunk = cb_chunk + (GLU ? 0u : static_cast<uint32_t>(pr * 2)) + (j >> 1);
                 ldsm_x4_t(wbox + sw128(krow, nchunk), b[kk][pr][0], b[kk][pr][1], b[kk][pr][2], b[kk][pr][3]);
             }
         }
@@ -175,6 +178,35 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
             *cnt = 0u;   // every part has arrived: ready for the next call
     }
 
+    if (layer == 0 && p.glu) {
+        // Gated: H = act(gate) * lin for this warp's 16 hidden columns.
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const int col = static_cast<int>(slice) * (SLICE / 2) + cw * 16 + n * 8 + 2 * q;
+            if (col >= p.O)
+                continue;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const int r0 = m * 16 + g, r1 = r0 + 8;
+                if (r0 < M)
+                    *reinterpret_cast<uint32_t*>(p.H + static_cast<int64_t>(r0) * p.O + col) =
+                        pack_bf16x2(act_apply(p.act1, acc.c[m][n][0]) * acc.c[m][n + 2][0],
+                                    act_apply(p.act1, acc.c[m][n][1]) * acc.c[m][n + 2][1]);
+                if (r1 < M)
+                    *reinterpret_cast<uint32_t*>(p.H + static_cast<int64_t>(r1) * p.O + col) =
+                        pack_bf16x2(act_apply(p.act1, acc.c[m][n][2]) * acc.c[m][n + 2][2],
+                                    act_apply(p.act1, acc.c[m][n][3]) * acc.c[m][n + 2][3]);
+            }
+        }
+        ptx::fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();
+            ptx::st_release_gpu(p.flags + slice * CONSUMER_WARPS + cw, epoch);
+        }
+        return;
+    }
+
     // Epilogue: bias, activation, bf16.
     const __nv_bfloat16* bias = layer == 0 ? p.b1 : p.b2;
     const int act = layer == 0 ? p.act1 : p.act2;
@@ -214,18 +246,22 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
     }
 }
 
-// Wait, with the whole warp, until every layer-1 slice of H in the cyclic
-// window [k0, k0 + count) of kch slices is ready (all four words equal the
-// epoch).  Relaxed loads spread over the lanes, then an acquire fence in every
-// lane: one pass over many flags instead of one serialised acquire per unit.
+// Wait, with the whole warp, until every layer-1 slice of H read by the
+// cyclic window [k0, k0 + count) of kch layer-2 K chunks is ready (all four
+// words equal the epoch; h_per_k slices per chunk).  Relaxed loads spread over
+// the lanes, then an acquire fence in every lane: one pass over many flags
+// instead of one serialised acquire per unit.
 __device__ bool wait_h_window(const WaitCtx& w, const uint32_t* flags, uint32_t epoch, int64_t k0, int64_t count,
-                              int64_t kch, int lane)
+                              int64_t kch, int h_per_k, int64_t h_slices, int lane)
 {
     const uint64_t t0 = ptx::globaltimer();
     for (;;) {
         bool mine = true;
-        for (int64_t i = lane; i < count && mine; i += 32) {
-            const uint32_t* f = flags + ((k0 + i) % kch) * CONSUMER_WARPS;
+        for (int64_t i = lane; i < count * h_per_k && mine; i += 32) {
+            const int64_t hs = ((k0 + i / h_per_k) % kch) * h_per_k + i % h_per_k;
+            if (hs >= h_slices)
+                continue;   // past the last hidden column: nothing to wait for
+            const uint32_t* f = flags + hs * CONSUMER_WARPS;
             uint32_t v[CONSUMER_WARPS];
 #pragma unroll
             for (int q = 0; q < CONSUMER_WARPS; ++q)
@@ -273,6 +309,13 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
     auto issue_w = [&](int layer, int64_t slice, int64_t kc, uint32_t st) {
         const uint32_t fb = ptx::smem_u32(&aux.full[st]);
         const uint32_t sw = ptx::smem_u32(stages + st * STAGE_BYTES);
+        if (layer == 0 && p.glu) {   // the same 64 hidden columns of W1 and of W3
+            ptx::tma_load_2d_hint(sw, &p.map_w[0], fb, static_cast<int32_t>(slice * (SLICE / 2)),
+                                  static_cast<int32_t>(kc * KC), evict_first);
+            ptx::tma_load_2d_hint(sw + W_BOX_BYTES, &p.map_w3, fb, static_cast<int32_t>(slice * (SLICE / 2)),
+                                  static_cast<int32_t>(kc * KC), evict_first);
+            return;
+        }
         ptx::tma_load_2d_hint(sw, &p.map_w[layer], fb, static_cast<int32_t>(slice * SLICE),
                               static_cast<int32_t>(kc * KC), evict_first);
         ptx::tma_load_2d_hint(sw + W_BOX_BYTES, &p.map_w[layer], fb, static_cast<int32_t>(slice * SLICE + 64),
@@ -330,7 +373,8 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
         const int npre_done = __shfl_sync(0xffffffffu, ok ? static_cast<int>(npre) : -1, 0);
         if (npre_done >= 0) {
             const int64_t count = (u1 - u0) < kch ? (u1 - u0) : kch;
-            const bool ready = wait_h_window(w, p.flags, aux.epoch, u0 % kch, count, kch, lane);
+            const bool ready = wait_h_window(w, p.flags, aux.epoch, u0 % kch, count, kch, pl.h_per_k, pl.slices[0],
+                                             lane);
             if (lane == 0) {
                 ptx::fence_proxy_async_global();
                 // the prefetched stages expect their H bytes: issue them even
@@ -417,7 +461,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
                 if (!ok)
                     break;
                 const uint32_t sw = ptx::smem_u32(stages + stage * STAGE_BYTES);
-                compute_stage<MT>(acc, sw, sw + W_STAGE_BYTES, cw, lane);
+                if (layer == 0 && p.glu)
+                    compute_stage<MT, true>(acc, sw, sw + W_STAGE_BYTES, cw, lane);
+                else
+                    compute_stage<MT, false>(acc, sw, sw + W_STAGE_BYTES, cw, lane);
                 __syncwarp();
                 if (lane == 0)
                     ptx::mbar_arrive(ptx::smem_u32(&aux.empty[stage]));

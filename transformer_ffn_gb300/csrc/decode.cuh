@@ -15,6 +15,12 @@
 // flags that Stream-K uses).  A finished layer-1 slice of H publishes a ready
 // flag; layer-2 units wait on the flag of the H slice they read.
 //
+// Gated FFN (H = act(X W1) * (X W3)): a layer-1 unit covers 64 hidden
+// columns; its stage holds the W1 box and the W3 box of those columns, and
+// each consumer warp takes 16 columns of each, so every thread ends with the
+// gate and linear fragments of the same H elements.  A layer-2 K chunk then
+// reads two layer-1 slices of H.
+//
 // Layout per CTA: warp 0 issues TMA copies (W tile [KC x SLICE] as two
 // 128-byte-swizzled boxes, plus the [rows x KC] tile of X or H); warps 1..4
 // each own 32 of the SLICE columns and run mma.sync m16n8k16 (bf16, fp32
@@ -47,6 +53,7 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
 
 struct Plan {
     int32_t grid;
+    int32_t h_per_k;        // layer-1 slices of H per layer-2 K chunk (1; 2 for the gated form)
     int32_t slices[2];      // output slices per layer
     int32_t kch[2];         // K chunks per slice
     int64_t units[2];       // slices * kch
@@ -68,11 +75,13 @@ __host__ __device__ inline int64_t range_start(int64_t c, int64_t U, int64_t G)
 
 // grid is the CTA count the caller wants; it is lowered so that every CTA
 // owns at least one unit of each layer.
-inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid)
+inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool glu = false)
 {
     (void)M;
     Plan pl{};
-    pl.slices[0] = static_cast<int32_t>((O + SLICE - 1) / SLICE);
+    const int64_t h_cols = glu ? SLICE / 2 : SLICE;   // hidden columns per layer-1 slice
+    pl.h_per_k = static_cast<int32_t>(KC / h_cols);
+    pl.slices[0] = static_cast<int32_t>((O + h_cols - 1) / h_cols);
     pl.kch[0] = static_cast<int32_t>((N + KC - 1) / KC);
     pl.slices[1] = static_cast<int32_t>((P + SLICE - 1) / SLICE);
     pl.kch[1] = static_cast<int32_t>((O + KC - 1) / KC);
@@ -105,6 +114,7 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid)
 struct Params {
     CUtensorMap map_w[2];      // W1 {O, N}, W2 {P, O}; box {64, KC}
     CUtensorMap map_a[2];      // X {N, M}, H {O, M}; box {64, 16 * m_tiles}
+    CUtensorMap map_w3;        // gated form: W3 {O, N}; box {64, KC}
     const __nv_bfloat16* X;
     const __nv_bfloat16* W1;
     const __nv_bfloat16* b1;
@@ -118,6 +128,7 @@ struct Params {
     DevCtrl* ctrl;
     int32_t M, N, O, P;
     int32_t act1, act2;
+    int32_t glu;               // 1: layer 1 is gated (no biases)
     uint64_t wait_limit_ns;
     Plan plan;
 };
