@@ -66,12 +66,16 @@ FLUSH_BYTES = 256 << 20
 KERNEL = {"tiny": "engine_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
           "swiglu": "engine_kernel", "swiglu_decode": "decode_kernel", "moe": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
           "decode": "decode_kernel"}
+# Sources a kernel's DRAM traffic depends on: its own code and the host code
+# that builds its tensor maps (box shapes, L2 promotion).
 KERNEL_SOURCES = {
     "engine_kernel": ["engine.cuh", "common.cuh", "ptx.cuh", "schedule.h", "engine_dense.cu",
-                      "engine_grouped.cu"],
-    "decode_kernel": ["decode.cu", "decode.cuh", "common.cuh", "ptx.cuh"],
-    "reduce_kernel": ["reduce.cuh", "reduce_params.cuh", "engine.cuh", "common.cuh", "ptx.cuh", "engine_reduce.cu"],
-    "b2b_kernel": ["reduce.cuh", "reduce_params.cuh", "engine.cuh", "common.cuh", "ptx.cuh", "engine_reduce.cu"],
+                      "engine_grouped.cu", "api.cu"],
+    "decode_kernel": ["decode.cu", "decode.cuh", "common.cuh", "ptx.cuh", "api.cu"],
+    "reduce_kernel": ["reduce.cuh", "reduce_params.cuh", "engine.cuh", "common.cuh", "ptx.cuh", "engine_reduce.cu",
+                      "api.cu"],
+    "b2b_kernel": ["reduce.cuh", "reduce_params.cuh", "engine.cuh", "common.cuh", "ptx.cuh", "engine_reduce.cu",
+                   "api.cu"],
 }
 
 
@@ -319,7 +323,8 @@ def run_e2e(cfg, inp, args, flush_buf, stream):
     for i in range(max(2, args.warmup)):
         step(i)
     torch.cuda.synchronize()
-    flush_buf.zero_()
+    if flush_buf is not None:
+        flush_buf.zero_()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(up)
@@ -334,12 +339,38 @@ def run_e2e(cfg, inp, args, flush_buf, stream):
 
 
 # ----------------------------------------------------------------- GPU arm
+def input_bytes(cfg):
+    """Bytes of one step's inputs: activations, weights, biases (and logits)."""
+    M, N, O, P = cfg["M"], cfg["N"], cfg["O"], cfg["P"]
+    if cfg["kind"] == "glu":
+        return 2 * (M * N + 2 * N * O + O * P)
+    experts = cfg.get("E", 1)
+    b = 2 * M * N + experts * 2 * (N * O + O * P + O + P)
+    if cfg["kind"] == "moe":
+        b += 4 * M * cfg["E"]
+    return b
+
+
+def l2_policy(cfg, dev):
+    """Flush L2 between timed steps unless one step's inputs exceed twice its
+    size (then no step can find the previous one's data in L2 anyway)."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    ib = input_bytes(cfg)
+    if ib > 2 * l2:
+        return False, (f"not flushed: each step's inputs ({ib / 2**20:.0f} MiB) exceed twice the "
+                       f"L2 ({l2 / 2**20:.0f} MiB)")
+    return True, f"flushed between steps ({FLUSH_BYTES >> 20} MiB write outside the step events)"
+
+
 def time_steps(step, steps, flush_buf, stream):
-    """Per-step device time (s) of `steps` steps, L2 flushed between them."""
+    """Per-step device time (s) of `steps` steps (flush_buf, if given, is
+    written between them to flush L2)."""
     import torch
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in evs:
-        flush_buf.zero_()
+        if flush_buf is not None:
+            flush_buf.zero_()
         a.record(stream)
         step()
         b.record(stream)
@@ -369,11 +400,13 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     inp = make_inputs(cfg, dev)
     out = torch.empty((cfg["M"], cfg["P"]), dtype=torch.bfloat16, device=dev)
-    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    do_flush, l2_note = l2_policy(cfg, dev)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if do_flush else None
     step = step_fn(cfg, inp, out)
 
     for _ in range(args.warmup):
-        flush_buf.zero_()
+        if flush_buf is not None:
+            flush_buf.zero_()
         step()
     tffn.check()
     launches_per_step = tffn.last_launch_count()
@@ -426,7 +459,7 @@ def run_gpu(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; X~N(0,1), W~N(0,1/fan_in), b~U(-0.1,0.1), bf16)",
         "config": {"workload": cfg["label"], "parallelism": f"replicas{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between steps (256 MiB write outside the step events)",
+                   "l2": l2_note,
                    "global_batch": cfg["M"] * world, "flops_per_step": flops(cfg)},
         "roofline": roof,
         "e2e": {"value": rate(cfg, e2e_mean) * world, "unit": unit, "h2d_bytes_per_step": h2d,

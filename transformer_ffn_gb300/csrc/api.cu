@@ -91,16 +91,18 @@ int get_encode()
 
 // Row-major bf16 matrix [outer x inner], box [box_outer x box_inner], 128-byte
 // swizzle, zero fill outside the matrix.
+// promo: L2 sector promotion of each fetch (256 B by default; 128 B for
+// boxes whose 128-byte rows are not followed by the same CTA's next box).
 int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-             uint32_t box_outer)
+             uint32_t box_outer, CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
 {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * 2};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? 0 : -1;
 }
 
@@ -387,9 +389,15 @@ static int run_decode(DeviceState& d, uint8_t* base, const DenseLayout& L, const
         (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * 4 > DCOUNT_WORDS)
         return TFFN_ERR_UNSUPPORTED;
     const uint32_t arows = M <= 16 ? 16u : 32u;
-    if (make_map(&p.map_w[0], W1, O, N, 64, decode::KC) || make_map(&p.map_w[1], W2, P, O, 64, decode::KC) ||
-        make_map(&p.map_a[0], X, N, M, 64, arows) || make_map(&p.map_a[1], p.H, O, M, 64, arows) ||
-        (glu && make_map(&p.map_w3, W3, O, N, 64, decode::KC)))
+    // Gated layer 1 loads 64-column boxes of W1 and W3 (128 B per row) whose
+    // neighbours belong to other units: no promotion past 128 B, or every
+    // weight row would be fetched twice.
+    const CUtensorMapL2promotion w1_promo =
+        glu ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+    if (make_map(&p.map_w[0], W1, O, N, 64, decode::KC, w1_promo) ||
+        make_map(&p.map_w[1], W2, P, O, 64, decode::KC) || make_map(&p.map_a[0], X, N, M, 64, arows) ||
+        make_map(&p.map_a[1], p.H, O, M, 64, arows) ||
+        (glu && make_map(&p.map_w3, W3, O, N, 64, decode::KC, w1_promo)))
         return TFFN_ERR_INVALID_ARG;
     timing_start(s);
     if (launch_decode(p, p.plan.grid, s) != 0)
