@@ -29,6 +29,7 @@ enum WaitSite : uint32_t {
     SITE_STAGE = 10,         // decode consumer waiting for a stage
     SITE_H_SMEM = 11,        // reduce-add form: MMA waiting for the H tile in shared memory
     SITE_H_FREE = 12,        // reduce-add form: epilogue waiting for the H tile's readers
+    SITE_BIAS = 13,          // engine epilogue: the CTA's shared bias slice
 };
 
 // Control block at the start of the workspace (256 bytes).

@@ -73,7 +73,8 @@ constexpr int EPI_WARPS = 4;
 constexpr int FLAG_WORDS_PER_TILE = 2 * EPI_WARPS;        // one per epilogue warp of the pair
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int AUX_BYTES = 1024;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + 1024;   // + alignment slack
+constexpr int BIAS_BYTES = BN * 4;                        // the tile's fp32 bias, shared by the epilogue warps
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + BIAS_BYTES + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 // Arrivals that free a task slot (counted on the leader): leader MMA thread,
 // leader B loader, leader epilogue warps, peer A loader, peer B loader, peer
@@ -131,6 +132,8 @@ struct Aux {
     uint64_t task_full[TASK_SLOTS];
     uint64_t task_empty[TASK_SLOTS];    // leader only
     uint64_t drain;                 // leader: every MMA issued has completed
+    uint64_t bias_ready;            // the four epilogue warps wrote the tile's bias slice
+    uint64_t bias_free;             // the four epilogue warps are done reading it
     int4 task[TASK_SLOTS];
     uint32_t tmem_base;
     uint32_t abort;
@@ -420,15 +423,21 @@ __device__ void run_mma(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const
 }
 
 // ----------------------------------------------------------------- epilogue
-// The tile's bias is read by the epilogue with broadcast global loads: its
-// four 128-byte lines are pulled into L1 before the epilogue waits for the
-// accumulator, so the loads hit L1 (the shared memory all goes to the stage
-// ring).
-__device__ __forceinline__ void prefetch_bias_l1(const __nv_bfloat16* bias, int32_t col0, int32_t ncols, int lane)
+// The tile's 256 bias values (fp32; zeros outside the matrix and for a NULL
+// bias) in one shared slice: epilogue warp q fetches columns [64q, 64q+64),
+// two per lane, before the accumulator wait, so the global latency overlaps
+// the main loop.
+__device__ __forceinline__ void fetch_bias_part(const __nv_bfloat16* bias, int32_t col0, int32_t ncols, float* slice,
+                                                uint32_t quad, int lane)
 {
-    const int32_t c = col0 + lane * 64;   // lanes 0..3: 64 columns = 128 B each
-    if (bias != nullptr && lane < BN / 64 && c < ncols)
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(bias + c));
+    const int32_t i = static_cast<int32_t>(quad) * 64 + lane * 2;
+    const int32_t c = col0 + i;
+    float2 v = make_float2(0.0f, 0.0f);
+    if (bias != nullptr && c < ncols) {   // ncols is even: both columns are inside
+        const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(bias + c));
+        v = make_float2(bf16_lo(u), bf16_hi(u));
+    }
+    *reinterpret_cast<float2*>(slice + i) = v;
 }
 
 // Rounding and the row's store of 32 finished values at column col.
@@ -456,21 +465,20 @@ __device__ __forceinline__ void store_row_chunk(const float (&v)[32], void* out,
 // Bias, activation, rounding and the row's store for one 32-column chunk.
 // The activation is a template argument, chosen once per tile.
 template <int ACT>
-__device__ __forceinline__ void store_chunk(const uint32_t (&acc)[32], const __nv_bfloat16* bias, bool row_ok,
-                                            void* out, bool out_f32, int64_t row, int64_t ld_out, int32_t col,
-                                            int32_t ncols)
+__device__ __forceinline__ void store_chunk(const uint32_t (&acc)[32], uint32_t bias_smem, bool row_ok, void* out,
+                                            bool out_f32, int64_t row, int64_t ld_out, int32_t col, int32_t ncols)
 {
     float v[32];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {   // 8 columns per group; ncols % 8 == 0
-        uint4 bu = make_uint4(0u, 0u, 0u, 0u);
-        if (bias != nullptr && col + g * 8 < ncols)   // the same address in every lane: a broadcast
-            bu = __ldg(reinterpret_cast<const uint4*>(bias + col + g * 8));
-        const float b[8] = {bf16_lo(bu.x), bf16_hi(bu.x), bf16_lo(bu.y), bf16_hi(bu.y),
-                            bf16_lo(bu.z), bf16_hi(bu.z), bf16_lo(bu.w), bf16_hi(bu.w)};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            v[g * 8 + e] = act_apply(ACT, __uint_as_float(acc[g * 8 + e]) + b[e]);
+    for (int q = 0; q < 8; ++q) {
+        float4 b;   // the same address in every lane: a broadcast
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(b.x), "=f"(b.y), "=f"(b.z), "=f"(b.w)
+                     : "r"(bias_smem + q * 16));
+        v[q * 4 + 0] = act_apply(ACT, __uint_as_float(acc[q * 4 + 0]) + b.x);
+        v[q * 4 + 1] = act_apply(ACT, __uint_as_float(acc[q * 4 + 1]) + b.y);
+        v[q * 4 + 2] = act_apply(ACT, __uint_as_float(acc[q * 4 + 2]) + b.z);
+        v[q * 4 + 3] = act_apply(ACT, __uint_as_float(acc[q * 4 + 3]) + b.w);
     }
     if (row_ok)
         store_row_chunk(v, out, out_f32, row, ld_out, col, ncols);
@@ -479,9 +487,8 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&acc)[32], const __n
 // Drain one 128 x BN accumulator quadrant-row by quadrant-row: chunk c+1's
 // TMEM load is in flight while chunk c is computed and stored.
 template <int ACT>
-__device__ __forceinline__ void drain_tile(uint32_t taddr, int nchunks, const __nv_bfloat16* bias, bool row_ok,
-                                           void* out, bool out_f32, int64_t row, int64_t ld_out, int32_t col_base,
-                                           int32_t ncols)
+__device__ __forceinline__ void drain_tile(uint32_t taddr, int nchunks, uint32_t bias_smem, bool row_ok, void* out,
+                                           bool out_f32, int64_t row, int64_t ld_out, int32_t col_base, int32_t ncols)
 {
     uint32_t ra[32], rb[32];
     __syncwarp();
@@ -490,12 +497,13 @@ __device__ __forceinline__ void drain_tile(uint32_t taddr, int nchunks, const __
         ptx::tmem_ld_wait();
         if (c + 1 < nchunks)
             ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, rb);
-        store_chunk<ACT>(ra, bias, row_ok, out, out_f32, row, ld_out, col_base + c * 32, ncols);
+        store_chunk<ACT>(ra, bias_smem + c * 128, row_ok, out, out_f32, row, ld_out, col_base + c * 32, ncols);
         if (c + 1 < nchunks) {
             ptx::tmem_ld_wait();
             if (c + 2 < nchunks)
                 ptx::tmem_ld_32x32b_x32(taddr + (c + 2) * 32, ra);
-            store_chunk<ACT>(rb, bias, row_ok, out, out_f32, row, ld_out, col_base + (c + 1) * 32, ncols);
+            store_chunk<ACT>(rb, bias_smem + (c + 1) * 128, row_ok, out, out_f32, row, ld_out,
+                             col_base + (c + 1) * 32, ncols);
         }
     }
 }
@@ -523,16 +531,16 @@ __device__ __forceinline__ void drain_glu(uint32_t taddr, int nchunks, bool row_
 
 // One finished accumulator tile, with the activation resolved to a template
 // argument once.
-__device__ __forceinline__ void drain_any(int act, bool gated, uint32_t taddr, int nchunks,
-                                          const __nv_bfloat16* bias, bool row_ok, void* out, bool out_f32, int64_t row,
-                                          int64_t ld_out, int32_t col_base, int32_t ncols)
+__device__ __forceinline__ void drain_any(int act, bool gated, uint32_t taddr, int nchunks, uint32_t bias_smem,
+                                          bool row_ok, void* out, bool out_f32, int64_t row, int64_t ld_out,
+                                          int32_t col_base, int32_t ncols)
 {
 #define TFFN_DRAIN(A)                                                                                        \
     do {                                                                                                     \
         if (gated)                                                                                           \
             drain_glu<A>(taddr, nchunks, row_ok, out, row, ld_out, col_base, ncols);                         \
         else                                                                                                 \
-            drain_tile<A>(taddr, nchunks, bias, row_ok, out, out_f32, row, ld_out, col_base, ncols);         \
+            drain_tile<A>(taddr, nchunks, bias_smem, row_ok, out, out_f32, row, ld_out, col_base, ncols);    \
     } while (0)
     switch (act) {
     case TFFN_ACT_GELU_TANH: TFFN_DRAIN(TFFN_ACT_GELU_TANH); break;
@@ -545,7 +553,7 @@ __device__ __forceinline__ void drain_any(int act, bool gated, uint32_t taddr, i
 
 template <int MAX_E>
 __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w, uint32_t tmem_base,
-                             uint32_t rank, int warp, int lane)
+                             uint32_t rank, int warp, int lane, float* bias_slice)
 {
     const uint32_t quad = static_cast<uint32_t>(warp & 3);   // TMEM lanes [32*quad, 32*quad+32)
     const int32_t n1 = p.layer[0].n_tiles;
@@ -562,9 +570,18 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         const uint32_t acc = iter & 1u;
         const uint32_t acc_phase = (iter >> 1) & 1u;
         const bool gated = p.glu && L == 0;   // gated layer 1: no bias
-        const __nv_bfloat16* const bias = gated ? nullptr : p.bias[L][expert_of(p, task.y)];
-        prefetch_bias_l1(bias, task.z * BN, la.ncols, lane);
-        if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_full[acc]), acc_phase, SITE_TMEM_FULL))
+        // The shared bias slice: every epilogue warp is done with the previous
+        // tile's before any writes this tile's part (bounded waits: a warp
+        // that gives up leaves the others to time out, not to hang).
+        if (iter > 0 && !wait_mbar(w, ptx::smem_u32(&aux.bias_free), (iter - 1) & 1u, SITE_BIAS))
+            break;
+        fetch_bias_part(gated ? nullptr : p.bias[L][expert_of(p, task.y)], task.z * BN, la.ncols, bias_slice, quad,
+                        lane);
+        __syncwarp();
+        if (lane == 0)
+            ptx::mbar_arrive(ptx::smem_u32(&aux.bias_ready));
+        if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_full[acc]), acc_phase, SITE_TMEM_FULL) ||
+            !wait_mbar(w, ptx::smem_u32(&aux.bias_ready), iter & 1u, SITE_BIAS))
             break;
         ptx::tc_fence_after();
         // The layer's fields in registers: the TMEM loads below are volatile
@@ -581,7 +598,11 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         const int32_t col_base = task.z * tile_cols;
         const int nchunks = ncols - col_base >= tile_cols ? tile_cols / 32 : (ncols - col_base + 31) / 32;
         const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * BN;
-        drain_any(act, gated, taddr, nchunks, bias, row_ok, out, out_f32, row, ld_out, col_base, ncols);
+        drain_any(act, gated, taddr, nchunks, ptx::smem_u32(bias_slice), row_ok, out, out_f32, row, ld_out, col_base,
+                  ncols);
+        __syncwarp();
+        if (lane == 0)
+            ptx::mbar_arrive(ptx::smem_u32(&aux.bias_free));
         // Accumulator drained: hand it back to the leader's MMA thread.
         ptx::tc_fence_before();
         __syncwarp();
@@ -631,6 +652,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
             ptx::mbar_init(ptx::smem_u32(&aux.task_empty[s]), TASK_CONSUMERS);
         }
         ptx::mbar_init(ptx::smem_u32(&aux.drain), 1);
+        ptx::mbar_init(ptx::smem_u32(&aux.bias_ready), EPI_WARPS);
+        ptx::mbar_init(ptx::smem_u32(&aux.bias_free), EPI_WARPS);
         aux.abort = 0u;
         // The epoch lives on the device, so a launch replayed from a CUDA
         // graph still gets a fresh value: every CTA reads it before any CTA
@@ -673,7 +696,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
         if (lane == 0 && rank == 0)
             run_mma(p, aux, stages, w, tmem_base);
     } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
-        run_epilogue(p, aux, w, tmem_base, rank, warp, lane);
+        float* bias_slice = reinterpret_cast<float*>(stages + STAGES * STAGE_BYTES + AUX_BYTES);
+        run_epilogue(p, aux, w, tmem_base, rank, warp, lane, bias_slice);
     }
     __syncwarp();
     ptx::tc_fence_before();
