@@ -51,6 +51,9 @@ def lib():
                                           i64, i64, i64, i64, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_int, i64p, i64, f64p]
         L.tffn_oracle_moe_ffn.restype = ctypes.c_int
+        L.tffn_oracle_moe_glu_ffn.argtypes = [u16p, f32p, ctypes.c_int, vpp, vpp, vpp, i64, i64, i64, i64,
+                                              ctypes.c_int, ctypes.c_int, i64p, i64, f64p]
+        L.tffn_oracle_moe_glu_ffn.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -190,4 +193,35 @@ def moe_ffn(X, logits, top_k, W1s, b1s, W2s, b2s, act1, act2, tokens=None):
                                    _ptr(Y, ctypes.c_double))
     if rc != 0:
         raise RuntimeError(f"oracle moe_ffn failed: {rc}")
+    return Y
+
+
+def moe_glu_ffn(X, logits, top_k, W1s, W3s, W2s, act=ACT_SILU, tokens=None):
+    """Y (float64, len(tokens) x P) of the routed, gate-weighted gated experts."""
+    X = _u16(X)
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    T, N = X.shape
+    E = len(W1s)
+    W1s = [_u16(w) for w in W1s]
+    W3s = [_u16(w) for w in W3s]
+    W2s = [_u16(w) for w in W2s]
+    O = W1s[0].shape[1]
+    P = W2s[0].shape[1]
+
+    def arr(lst):
+        a = (ctypes.c_void_p * E)(*[x.ctypes.data for x in lst])
+        return ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p)), a
+
+    a1, a3, a2 = arr(W1s), arr(W3s), arr(W2s)
+    if tokens is None:
+        tk, ntok = None, T
+    else:
+        tk = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+        ntok = tk.shape[0]
+    Y = np.empty((ntok, P), dtype=np.float64)
+    rc = lib().tffn_oracle_moe_glu_ffn(_ptr(X, ctypes.c_uint16), _ptr(logits, ctypes.c_float), int(top_k),
+                                       a1[0], a3[0], a2[0], T, N, O, P, E, int(act), _ptr(tk, ctypes.c_int64),
+                                       ntok, _ptr(Y, ctypes.c_double))
+    if rc != 0:
+        raise RuntimeError(f"oracle moe_glu_ffn failed: {rc}")
     return Y

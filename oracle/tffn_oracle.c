@@ -38,6 +38,9 @@
  *                expert index.
  *   moe_permute  same page, section 4.2: rows grouped contiguously by expert;
  *                single-GPU order is (expert ascending, token ascending).
+ *   moe_glu_ffn  moe_ffn with gated experts (each expert the glu_ffn above,
+ *                no biases): the SwiGLU experts of the MoE models the
+ *                fused-FFN page benchmarks.
  *   moe_ffn      same page, sections 2.1-2.2, steps 3 and 5: every kept
  *                expert runs the FFN above on the token; the layer output is
  *                the gate-weighted sum of those outputs.  Expert outputs are
@@ -363,6 +366,45 @@ int tffn_oracle_moe_ffn(const uint16_t *X, const float *logits, int top_k,
             rc = tffn_oracle_ffn(X + t * N, W1[e], b1 ? b1[e] : NULL, W2[e],
                                  b2 ? b2[e] : NULL, act1, act2, 1, N, O, P,
                                  &one, 1, 1, ye, NULL);
+            for (int64_t c = 0; c < P; ++c)
+                Y[r * P + c] += w[s] * ye[c];
+        }
+    }
+    free(idx); free(w); free(ye);
+    return rc;
+}
+
+int tffn_oracle_moe_glu_ffn(const uint16_t *X, const float *logits, int top_k,
+                            const uint16_t *const *W1, const uint16_t *const *W3,
+                            const uint16_t *const *W2, int64_t T, int64_t N, int64_t O,
+                            int64_t P, int E, int act, const int64_t *tokens, int64_t ntok,
+                            double *Y)
+{
+    if (!X || !logits || !W1 || !W3 || !W2 || !Y || T < 0 || E < 1 || top_k < 1 ||
+        top_k > E)
+        return -1;
+    if (!tokens)
+        ntok = T;
+    int32_t *idx = malloc(sizeof(int32_t) * (size_t)top_k);
+    double *w = malloc(sizeof(double) * (size_t)top_k);
+    double *ye = malloc(sizeof(double) * (size_t)P);
+    if (!idx || !w || !ye) {
+        free(idx); free(w); free(ye);
+        return -2;
+    }
+    int rc = 0;
+    for (int64_t r = 0; r < ntok && rc == 0; ++r) {
+        int64_t t = tokens ? tokens[r] : r;
+        if (t < 0 || t >= T) { rc = -1; break; }
+        rc = tffn_oracle_moe_route(logits + t * E, 1, E, top_k, idx, w);
+        for (int64_t c = 0; c < P; ++c)
+            Y[r * P + c] = 0.0;
+        for (int s = 0; s < top_k && rc == 0; ++s) {
+            int e = idx[s];
+            int64_t one = 0;
+            /* The token's row alone, through expert e's gated FFN. */
+            rc = tffn_oracle_glu_ffn(X + t * N, W1[e], W3[e], W2[e], act, 1, N, O, P,
+                                     &one, 1, 1, ye, NULL);
             for (int64_t c = 0; c < P; ++c)
                 Y[r * P + c] += w[s] * ye[c];
         }

@@ -54,6 +54,13 @@ int tffn_oracle_moe_ffn(const uint16_t *X, const float *logits, int top_k,
                         int act1, int act2, const int64_t *tokens, int64_t ntok,
                         double *Y);
 
+/* MoE with gated experts: expert e is glu_ffn(W1[e], W3[e], W2[e], act). */
+int tffn_oracle_moe_glu_ffn(const uint16_t *X, const float *logits, int top_k,
+                            const uint16_t *const *W1, const uint16_t *const *W3,
+                            const uint16_t *const *W2, int64_t T, int64_t N, int64_t O,
+                            int64_t P, int E, int act, const int64_t *tokens, int64_t ntok,
+                            double *Y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -498,3 +498,43 @@ def test_glu_megatron_split_reproduces_unsplit(G):
                              np.ascontiguousarray(W3[:, g * s:(g + 1) * s]),
                              np.ascontiguousarray(W2[g * s:(g + 1) * s, :]), ACT_SILU) for g in range(G))
     np.testing.assert_allclose(acc, full, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------- gated-expert MoE ----
+
+def _glu_experts(E, N, O, P, seed):
+    exps = [synth.glu_inputs(1, N, O, P, seed=seed + e) for e in range(E)]
+    u = synth.to_u16
+    return [u(g.W1) for g in exps], [u(g.W3) for g in exps], [u(g.W2) for g in exps]
+
+
+def test_moe_glu_single_expert_is_the_gated_ffn():
+    T, N, O, P = 9, 16, 24, 8
+    X = synth.to_u16(synth.glu_inputs(T, N, O, P, seed=3).X)
+    W1, W3, W2 = _glu_experts(1, N, O, P, seed=10)
+    logits = np.zeros((T, 1), dtype=np.float32)
+    np.testing.assert_array_equal(oracle.moe_glu_ffn(X, logits, 1, W1, W3, W2),
+                                  oracle.glu_ffn(X, W1[0], W3[0], W2[0], ACT_SILU))
+
+
+def test_moe_glu_top2_is_the_weighted_sum_of_two_gated_experts():
+    T, N, O, P, E = 7, 16, 24, 8, 4
+    X = synth.to_u16(synth.glu_inputs(T, N, O, P, seed=4).X)
+    W1, W3, W2 = _glu_experts(E, N, O, P, seed=20)
+    rng = np.random.default_rng(5)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    got = oracle.moe_glu_ffn(X, logits, 2, W1, W3, W2)
+    idx, w = oracle.moe_route(logits, 2)
+    for t in range(T):
+        want = sum(w[t, s] * oracle.glu_ffn(X[t:t + 1], W1[idx[t, s]], W3[idx[t, s]], W2[idx[t, s]], ACT_SILU)[0]
+                   for s in range(2))
+        np.testing.assert_allclose(got[t], want, rtol=1e-13, atol=1e-13)
+
+
+def test_moe_glu_equal_gates_all_experts_is_their_mean():
+    T, N, O, P, E = 5, 16, 24, 8, 3
+    X = synth.to_u16(synth.glu_inputs(T, N, O, P, seed=6).X)
+    W1, W3, W2 = _glu_experts(E, N, O, P, seed=30)
+    got = oracle.moe_glu_ffn(X, np.zeros((T, E), dtype=np.float32), E, W1, W3, W2)
+    want = sum(oracle.glu_ffn(X, W1[e], W3[e], W2[e], ACT_SILU) for e in range(E)) / E
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)

@@ -16,7 +16,8 @@
 // the pair (128 each) and B's columns split between the pair (128 each), and
 // writes each CTA's tensor memory with its 128 rows x 256 columns.  Each CTA
 // therefore streams only half of the B tile: 32 KiB per 64-deep k-stage per
-// SM, six stages deep.
+// SM, seven stages deep (all of a CTA's shared memory but the barrier block
+// and one 1 KiB bias slice).
 //
 // CTA layout (224 threads, one CTA per SM, two CTAs per cluster):
 //   warp 0      A loader.  The leader (cluster rank 0) takes tickets and
@@ -37,6 +38,9 @@
 //               quadrant per warp, one row per thread), bias, activation,
 //               round, store; the accumulator is double-buffered so the
 //               epilogue of one tile overlaps the main loop of the next.
+//               The four warps share the tile's bias slice in shared memory
+//               (each fetches a quarter before the accumulator wait).
+//   warp 1 of the peer CTA has no role after the allocation.
 //
 // Operands: A (X or H) is row-major [rows x K]: K-major, 128-byte swizzle,
 // boxes of 64 (K) x 128 (rows).  B (W1 or W2) is row-major [K x cols]: the
