@@ -49,6 +49,10 @@ CONFIGS = {
                          "Y = (SiLU(X W1) * (X W3)) W2, no biases"),
     "swiglu_decode": dict(kind="glu", M=16, N=4096, O=14336, P=4096, act1="silu", act2="none",
                           label="SwiGLU FFN decode (Llama 3 8B shape) M=16 N=4096 O=14336 P=4096"),
+    "moe_swiglu": dict(kind="moe", glu=True, M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="silu",
+                       act2="none",
+                       label="MoE FFN with SwiGLU experts (Mixtral-class) T=8192 N=4096 E=8 O=14336 P=4096, "
+                             "softmax top-2"),
     "moe_moderate": dict(kind="moe", M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="gelu_tanh",
                          act2="none", router="moderate",
                          label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh, "
@@ -66,7 +70,7 @@ SPEC_HBM_GBS = 8000.0       # GB300 HBM3e
 
 # Dominant kernel of each workload (for the ncu traffic record).
 KERNEL = {"tiny": "engine_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
-          "swiglu": "engine_kernel", "swiglu_decode": "decode_kernel", "moe": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
+          "swiglu": "engine_kernel", "swiglu_decode": "decode_kernel", "moe": "engine_kernel", "moe_swiglu": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
           "decode": "decode_kernel"}
 # Sources a kernel's DRAM traffic depends on: its own code and the host code
 # that builds its tensor maps (box shapes, L2 promotion).
@@ -98,7 +102,7 @@ def flops(cfg):
     """Algorithmic FLOPs of one step: 2*rows*O*(N+P), routed rows for MoE;
     2*M*O*(2N+P) for the gated FFN (two input products)."""
     rows = cfg["M"] * cfg.get("k", 1)
-    n_in = 2 * cfg["N"] if cfg["kind"] == "glu" else cfg["N"]
+    n_in = 2 * cfg["N"] if (cfg["kind"] == "glu" or cfg.get("glu")) else cfg["N"]
     return 2.0 * rows * cfg["O"] * (n_in + cfg["P"])
 
 
@@ -258,10 +262,23 @@ def make_inputs(cfg, device, seed=0):
     from transformer_ffn_gb300 import synth
     if cfg["kind"] == "glu":
         return synth.glu_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], seed=seed, device=device)
+    if cfg["kind"] == "moe" and cfg.get("glu"):
+        return synth.moe_glu_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], cfg["E"], seed=seed, device=device,
+                                    router=cfg.get("router", "balanced"))
     if cfg["kind"] == "moe":
         return synth.moe_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], cfg["E"], seed=seed, device=device,
                                 router=cfg.get("router", "balanced"))
     return synth.ffn_inputs(cfg["M"], cfg["N"], cfg["O"], cfg["P"], seed=seed, device=device)
+
+
+def moe_call(cfg, inp, X, logits, out=None, routing=False, stream=None):
+    """One MoE step through the library (gated experts when the workload has them)."""
+    import transformer_ffn_gb300 as tffn
+    if cfg.get("glu"):
+        return tffn.moe_glu_forward(X, logits, cfg["k"], inp.W1, inp.W3, inp.W2, cfg["act1"], out=out,
+                                    routing=routing, stream=stream)
+    return tffn.moe_ffn_forward(X, logits, cfg["k"], inp.W1, inp.b1, inp.W2, inp.b2, cfg["act1"], cfg["act2"],
+                                out=out, routing=routing, stream=stream)
 
 
 def step_fn(cfg, inp, out, X=None):
@@ -270,8 +287,7 @@ def step_fn(cfg, inp, out, X=None):
     if cfg["kind"] == "glu":
         return lambda: tffn.ffn_glu_forward(X, inp.W1, inp.W3, inp.W2, cfg["act1"], out=out)
     if cfg["kind"] == "moe":
-        return lambda: tffn.moe_ffn_forward(X, inp.logits, cfg["k"], inp.W1, inp.b1, inp.W2, inp.b2,
-                                            cfg["act1"], cfg["act2"], out=out)
+        return lambda: moe_call(cfg, inp, X, inp.logits, out=out)
     return lambda: tffn.ffn_forward(X, inp.W1, inp.b1, inp.W2, inp.b2, cfg["act1"], cfg["act2"], out=out)
 
 
@@ -309,8 +325,7 @@ def run_e2e(cfg, inp, args, flush_buf, stream):
         comp.wait_event(downloaded[b])          # step i-2's result has left Y_dev[b]
         with torch.cuda.stream(comp):
             if moe:
-                tffn.moe_ffn_forward(X_dev[b], L_dev[b], cfg["k"], inp.W1, inp.b1, inp.W2, inp.b2,
-                                     cfg["act1"], cfg["act2"], out=Y_dev[b], stream=comp)
+                moe_call(cfg, inp, X_dev[b], L_dev[b], out=Y_dev[b], stream=comp)
             elif cfg["kind"] == "glu":
                 tffn.ffn_glu_forward(X_dev[b], inp.W1, inp.W3, inp.W2, cfg["act1"], out=Y_dev[b], stream=comp)
             else:
@@ -347,7 +362,10 @@ def input_bytes(cfg):
     if cfg["kind"] == "glu":
         return 2 * (M * N + 2 * N * O + O * P)
     experts = cfg.get("E", 1)
-    b = 2 * M * N + experts * 2 * (N * O + O * P + O + P)
+    if cfg.get("glu"):
+        b = 2 * M * N + experts * 2 * (2 * N * O + O * P)
+    else:
+        b = 2 * M * N + experts * 2 * (N * O + O * P + O + P)
     if cfg["kind"] == "moe":
         b += 4 * M * cfg["E"]
     return b
@@ -383,9 +401,7 @@ def time_steps(step, steps, flush_buf, stream):
 def padded_rows(cfg, inp):
     """Rows of the grouped layout, zero padding included (each expert's rows
     rounded up to whole 256-row bands), from the routing the library returns."""
-    import transformer_ffn_gb300 as tffn
-    _, r = tffn.moe_ffn_forward(inp.X, inp.logits, cfg["k"], inp.W1, inp.b1, inp.W2, inp.b2,
-                                cfg["act1"], cfg["act2"], routing=True)
+    _, r = moe_call(cfg, inp, inp.X, inp.logits, routing=True)
     counts = r["expert_offsets"].diff().cpu().tolist()
     return int(sum((c + 255) // 256 * 256 for c in counts))
 
@@ -496,6 +512,9 @@ def _oracle_inputs(cfg, inp):
     u = synth.to_u16
     if cfg["kind"] == "glu":
         return (u(inp.X), u(inp.W1), u(inp.W3), u(inp.W2))
+    if cfg["kind"] == "moe" and cfg.get("glu"):
+        return (u(inp.X), inp.logits.cpu().numpy(), [u(w) for w in inp.W1], [u(w) for w in inp.W3],
+                [u(w) for w in inp.W2])
     if cfg["kind"] == "moe":
         return (u(inp.X), inp.logits.cpu().numpy(), [u(w) for w in inp.W1], [u(b) for b in inp.b1],
                 [u(w) for w in inp.W2], [u(b) for b in inp.b2])
@@ -509,6 +528,9 @@ def _oracle_rows(cfg, host, rows):
     if cfg["kind"] == "glu":
         X, W1, W3, W2 = host
         return oracle.glu_ffn(X, W1, W3, W2, acts[cfg["act1"]], rows=rows)
+    if cfg["kind"] == "moe" and cfg.get("glu"):
+        X, lg, W1, W3, W2 = host
+        return oracle.moe_glu_ffn(X, lg, cfg["k"], W1, W3, W2, acts[cfg["act1"]], tokens=rows)
     if cfg["kind"] == "moe":
         X, lg, W1, b1, W2, b2 = host
         return oracle.moe_ffn(X, lg, cfg["k"], W1, b1, W2, b2, acts[cfg["act1"]], acts[cfg["act2"]],

@@ -151,6 +151,24 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
                     tffn_routing* routing, struct CUstream_st* stream);
 
 /*
+ * moe_glu_forward -- moe_ffn_forward with gated experts: expert e computes
+ * (act(x W1[e]) * (x W3[e])) W2[e] (ffn_glu_forward's FFN, no biases), as in
+ * the SwiGLU experts of the MoE models the fused-FFN page benchmarks
+ * ("Kernel fusion and tensor parallelism", sections "Expert sharding" and
+ * "Results").  Routing, gate weights, grouping and the weighted sum are
+ * moe_ffn_forward's.
+ *
+ *   W1, W3: HOST arrays of E DEVICE pointers, each [N x O] bf16
+ *   W2:     HOST array of E DEVICE pointers, each [O x P] bf16
+ *   act:    tffn_act code applied to x W1[e] (TFFN_ACT_SILU for SwiGLU)
+ * Other arguments, errors and workspace as moe_ffn_forward (the workspace is
+ * tffn_workspace_bytes(T, N, O, P, E, top_k)).
+ */
+int moe_glu_forward(const void* X, const float* gate_logits, int top_k, const void* const* W1,
+                    const void* const* W3, const void* const* W2, void* Y, int64_t T, int64_t N, int64_t O,
+                    int64_t P, int E, int act, tffn_routing* routing, struct CUstream_st* stream);
+
+/*
  * ffn_forward_decode_noalloc -- ffn_forward for M <= 32 rows (the decode
  * shapes) that allocates nothing.  The paper has no counterpart: this entry
  * point exists for callers that cannot allocate device memory -- plugins

@@ -13,7 +13,7 @@ import torch
 
 __all__ = ["ffn_forward", "moe_ffn_forward", "load", "check", "set_option", "workspace_bytes",
            "set_workspace", "last_launch_count", "timing_begin", "timing_end", "TffnError",
-           "ACT_NONE", "ACT_RELU", "ACT_GELU_TANH", "ACT_SILU", "ffn_glu_forward", "OPT_PATH", "OPT_WAIT_LIMIT_MS",
+           "ACT_NONE", "ACT_RELU", "ACT_GELU_TANH", "ACT_SILU", "ffn_glu_forward", "moe_glu_forward", "OPT_PATH", "OPT_WAIT_LIMIT_MS",
            "OPT_SKIP_FLAG", "OPT_GROUP_M", "OPT_MOE_ORDER", "LIB_PATH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -56,6 +56,9 @@ def load():
     L.moe_ffn_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
                                   ctypes.POINTER(_Routing), vp]
     L.moe_ffn_forward.restype = i32
+    L.moe_glu_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32,
+                                  ctypes.POINTER(_Routing), vp]
+    L.moe_glu_forward.restype = i32
     L.tffn_workspace_bytes.argtypes = [i64, i64, i64, i64, i32, i32]
     L.tffn_workspace_bytes.restype = ctypes.c_size_t
     L.tffn_set_workspace.argtypes = [vp, ctypes.c_size_t]
@@ -209,6 +212,48 @@ def moe_ffn_forward(X, gate_logits, top_k, W1, b1, W2, b2, act1="gelu_tanh", act
                            ctypes.cast(b2a, ctypes.c_void_p) if b2a is not None else None,
                            _ptr(Y), T, N, O, P, E, _act(act1), _act(act2), rp, _stream_ptr(stream))
     _raise(rc, "moe_ffn_forward")
+    return (Y, r) if routing else Y
+
+
+def moe_glu_forward(X, gate_logits, top_k, W1, W3, W2, act="silu", out=None, routing=False, stream=None):
+    """Top-k routed MoE with gated experts: expert e is (act(x W1[e]) * (x W3[e])) W2[e]
+    (SwiGLU with act="silu").  W1, W3, W2 are lists of per-expert tensors;
+    routing as moe_ffn_forward."""
+    L = load()
+    dev = X.device
+    _check_bf16("X", X, 2, dev)
+    T, N = X.shape
+    E = len(W1)
+    if len(W3) != E or len(W2) != E:
+        raise ValueError("expert lists differ in length")
+    if gate_logits.dtype != torch.float32 or gate_logits.shape != (T, E) or not gate_logits.is_contiguous():
+        raise ValueError("gate_logits must be contiguous float32 [T, E]")
+    O = W1[0].shape[1]
+    P = W2[0].shape[1]
+    for e in range(E):
+        for name, t, shape in ((f"W1[{e}]", W1[e], (N, O)), (f"W3[{e}]", W3[e], (N, O)), (f"W2[{e}]", W2[e], (O, P))):
+            _check_bf16(name, t, 2, dev)
+            if tuple(t.shape) != shape:
+                raise ValueError(f"{name} shape")
+    arr = ctypes.c_void_p * E
+    w1a = arr(*[t.data_ptr() for t in W1])
+    w3a = arr(*[t.data_ptr() for t in W3])
+    w2a = arr(*[t.data_ptr() for t in W2])
+    Y = out if out is not None else torch.empty((T, P), dtype=torch.bfloat16, device=dev)
+    _check_bf16("out", Y, 2, dev)
+    r = None
+    rp = None
+    if routing:
+        r = {"topk_idx": torch.empty((T, top_k), dtype=torch.int32, device=dev),
+             "topk_w": torch.empty((T, top_k), dtype=torch.float32, device=dev),
+             "perm": torch.empty((T * top_k,), dtype=torch.int32, device=dev),
+             "expert_offsets": torch.empty((E + 1,), dtype=torch.int32, device=dev)}
+        rp = ctypes.pointer(_Routing(r["topk_idx"].data_ptr(), r["topk_w"].data_ptr(),
+                                     r["perm"].data_ptr(), r["expert_offsets"].data_ptr()))
+    rc = L.moe_glu_forward(_ptr(X), _ptr(gate_logits), int(top_k), ctypes.cast(w1a, ctypes.c_void_p),
+                           ctypes.cast(w3a, ctypes.c_void_p), ctypes.cast(w2a, ctypes.c_void_p), _ptr(Y), T, N, O, P,
+                           E, _act(act), rp, _stream_ptr(stream))
+    _raise(rc, "moe_glu_forward")
     return (Y, r) if routing else Y
 
 

@@ -311,14 +311,16 @@ struct MoeLayout {
     size_t off_idx, off_w, off_pos, off_src, off_band, off_nb, off_xp, off_h, off_yp, total;
 };
 
-MoeLayout moe_layout(int64_t T, int64_t N, int64_t O, int64_t P, int E, int k)
+// glu: gated experts, whose layer-1 tiles cover 128 hidden columns
+MoeLayout moe_layout(int64_t T, int64_t N, int64_t O, int64_t P, int E, int k, bool glu = false)
 {
     MoeLayout L;
     L.R = T * k;
     L.Rmax = static_cast<int64_t>(align_up(static_cast<size_t>(L.R + static_cast<int64_t>(E) * (engine::BM - 1)),
                                            engine::BM));
     L.mbmax = L.Rmax / engine::BM;
-    L.n1 = static_cast<int32_t>((O + engine::BN - 1) / engine::BN);
+    const int64_t h_cols = glu ? engine::BN_CTA : engine::BN;
+    L.n1 = static_cast<int32_t>((O + h_cols - 1) / h_cols);
     L.n2 = static_cast<int32_t>((P + engine::BN - 1) / engine::BN);
     size_t o = SYNC_BYTES;
     auto take = [&](size_t bytes) {
@@ -587,7 +589,7 @@ int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W
     const int64_t rows_h = L.m_blocks * engine::BM;
     const bool b3d = (O % 64 == 0) && (P % 64 == 0);
     if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) || make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) ||
-        make_map_b(&p.map_b[0][0], W1, O, N, b3d) || make_map_b(&p.map_b_lin, W3, O, N, b3d) ||
+        make_map_b(&p.map_b[0][0], W1, O, N, b3d) || make_map_b(&p.map_b_lin[0], W3, O, N, b3d) ||
         make_map_b(&p.map_b[1][0], W2, P, O, b3d))
         return TFFN_ERR_INVALID_ARG;
     p.b3d = b3d ? 1 : 0;
@@ -597,12 +599,14 @@ int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W
     return run_dense_engine(*d, base, L, p, s);
 }
 
-int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const void* const* W1,
-                    const void* const* b1, const void* const* W2, const void* const* b2, void* Y, int64_t T,
-                    int64_t N, int64_t O, int64_t P, int E, int act1, int act2, tffn_routing* routing,
-                    struct CUstream_st* stream)
+// The MoE forward; W3 (an array of E pointers) non-null: gated experts.
+static int moe_forward(const void* X, const float* gate_logits, int top_k, const void* const* W1,
+                       const void* const* W3, const void* const* b1, const void* const* W2, const void* const* b2,
+                       void* Y, int64_t T, int64_t N, int64_t O, int64_t P, int E, int act1, int act2,
+                       tffn_routing* routing, struct CUstream_st* stream)
 {
     g_last_launches = 0;
+    const bool glu = W3 != nullptr;
     if (E < 1 || E > MOE_MAX_E || top_k < 1 || top_k > E)
         return TFFN_ERR_INVALID_ARG;
     if (T < 0 || T * top_k >= (int64_t(1) << 30) || !dim_ok(N) || !dim_ok(O) || !dim_ok(P))
@@ -618,6 +622,8 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     for (int e = 0; e < E; ++e) {
         if (!W1[e] || !W2[e] || !aligned16(W1[e]) || !aligned16(W2[e]))
             return TFFN_ERR_INVALID_ARG;
+        if (glu && (!W3[e] || !aligned16(W3[e])))
+            return TFFN_ERR_INVALID_ARG;
         if (b1 && b1[e] && !aligned16(b1[e]))
             return TFFN_ERR_INVALID_ARG;
         if (b2 && b2[e] && !aligned16(b2[e]))
@@ -630,7 +636,7 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     int rc = device_state(&d);
     if (rc != TFFN_OK)
         return rc;
-    const MoeLayout L = moe_layout(T, N, O, P, E, top_k);
+    const MoeLayout L = moe_layout(T, N, O, P, E, top_k, glu);
     if (static_cast<size_t>(L.mbmax) * L.n1 * engine::FLAG_WORDS_PER_TILE > FLAG_WORDS)
         return TFFN_ERR_UNSUPPORTED;
     uint8_t* base = nullptr;
@@ -660,6 +666,8 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     for (int e = 0; e < E && !bad; ++e) {
         bad |= make_map_b(&p.map_b[0][e], W1[e], O, N, b3d);
         bad |= make_map_b(&p.map_b[1][e], W2[e], P, O, b3d);
+        if (glu)
+            bad |= make_map_b(&p.map_b_lin[e], W3[e], O, N, b3d);
         p.bias[0][e] = b1 ? static_cast<const __nv_bfloat16*>(b1[e]) : nullptr;
         p.bias[1][e] = b2 ? static_cast<const __nv_bfloat16*>(b2[e]) : nullptr;
     }
@@ -669,6 +677,8 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
     }
     fill_layer<MOE_MAX_E>(p.layer[0], N, O, act1, 0, L.Rmax, H);
     fill_layer<MOE_MAX_E>(p.layer[1], O, P, act2, 1, L.Rmax, Yp);
+    p.layer[0].n_tiles = L.n1;
+    p.glu = glu ? 1 : 0;
     p.m_blocks = -1;
     p.m_blocks_dev = nb;
     p.band_expert = band;
@@ -704,6 +714,25 @@ int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const vo
             cudaSuccess)
         return TFFN_ERR_CUDA;
     return TFFN_OK;
+}
+
+int moe_ffn_forward(const void* X, const float* gate_logits, int top_k, const void* const* W1,
+                    const void* const* b1, const void* const* W2, const void* const* b2, void* Y, int64_t T,
+                    int64_t N, int64_t O, int64_t P, int E, int act1, int act2, tffn_routing* routing,
+                    struct CUstream_st* stream)
+{
+    return moe_forward(X, gate_logits, top_k, W1, nullptr, b1, W2, b2, Y, T, N, O, P, E, act1, act2, routing,
+                       stream);
+}
+
+int moe_glu_forward(const void* X, const float* gate_logits, int top_k, const void* const* W1,
+                    const void* const* W3, const void* const* W2, void* Y, int64_t T, int64_t N, int64_t O,
+                    int64_t P, int E, int act, tffn_routing* routing, struct CUstream_st* stream)
+{
+    if (!W3 && T > 0)
+        return TFFN_ERR_INVALID_ARG;
+    return moe_forward(X, gate_logits, top_k, W1, W3, nullptr, W2, nullptr, Y, T, N, O, P, E, act, TFFN_ACT_NONE,
+                       routing, stream);
 }
 
 size_t tffn_workspace_bytes(int64_t M, int64_t N, int64_t O, int64_t P, int E, int top_k)

@@ -115,7 +115,7 @@ struct Params {
     int32_t skip_flag;                         // test fault injection, -1 = off
     int32_t b3d;                               // 1: map_b are 3-D {64 cols, K, cols/64} maps
     int32_t glu;                               // 1: layer 1 is gated, H = act(X W1) * (X W3)
-    CUtensorMap map_b_lin;                     // glu: W3, laid out like map_b[0][0]
+    CUtensorMap map_b_lin[MAX_E];              // glu: W3[e], laid out like map_b[0][e]
 };
 
 // Hidden columns one layer-1 tile produces: a gated tile spends its 256
@@ -347,7 +347,8 @@ __device__ void run_b_loader(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
         // A gated layer-1 tile: the leader CTA's B half is W1's 128 columns,
         // the peer's half the same 128 columns of W3.
         const bool gated = p.glu && L == 0;
-        const CUtensorMap* mb = (gated && rank == 1) ? &p.map_b_lin : &p.map_b[L][expert_of(p, task.y)];
+        const int e = expert_of(p, task.y);
+        const CUtensorMap* mb = (gated && rank == 1) ? &p.map_b_lin[e] : &p.map_b[L][e];
         const int nk = (p.layer[L].K + BK - 1) / BK;
         const int32_t col0 = gated ? task.z * BN_CTA : task.z * BN + static_cast<int32_t>(rank) * BN_CTA;
         for (int kb = 0; kb < nk; ++kb) {
@@ -672,7 +673,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
             ptx::prefetch_tmap(&p.map_b[0][0]);
             ptx::prefetch_tmap(&p.map_b[1][0]);
             if (p.glu)
-                ptx::prefetch_tmap(&p.map_b_lin);
+                ptx::prefetch_tmap(&p.map_b_lin[0]);
         }
     }
     if (warp == 1) {

@@ -128,6 +128,31 @@ def moe_inputs(T, N, O, P, E, seed=0, device="cpu",
     return MoEInputs(X, logits, W1, b1, W2, b2)
 
 
+@dataclass
+class MoEGLUInputs:
+    X: torch.Tensor
+    logits: torch.Tensor
+    W1: List[torch.Tensor]
+    W3: List[torch.Tensor]
+    W2: List[torch.Tensor]
+
+
+def moe_glu_inputs(T, N, O, P, E, seed=0, device="cpu", router="balanced") -> MoEGLUInputs:
+    """Gated-expert MoE operands: X, then W1, W3, W2 of each expert in index
+    order (no biases), then the logits (with the router's offsets)."""
+    g = _gen(device, seed)
+    X = _normal((T, N), 1.0, g, device)
+    W1, W3, W2 = [], [], []
+    for _ in range(E):
+        W1.append(_normal((N, O), (1.0 / N) ** 0.5, g, device))
+        W3.append(_normal((N, O), (1.0 / N) ** 0.5, g, device))
+        W2.append(_normal((O, P), (1.0 / O) ** 0.5, g, device))
+    logits = torch.randn((T, E), generator=g, device=device, dtype=torch.float32)
+    if router != "balanced":
+        logits += router_offsets(E, router).to(device)
+    return MoEGLUInputs(X, logits, W1, W3, W2)
+
+
 def to_u16(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (host copy)."""
     assert t.dtype == torch.bfloat16
