@@ -308,7 +308,8 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, int sms, bo
 struct MoeLayout {
     int64_t R = 0, Rmax = 0, mbmax = 0;
     int32_t n1 = 0, n2 = 0;
-    size_t off_idx, off_w, off_pos, off_src, off_band, off_nb, off_xp, off_h, off_yp, total;
+    size_t off_idx, off_w, off_pos, off_hist, off_bpad, off_boff, off_pad, off_band, off_nb, off_xp, off_h, off_yp,
+        total;
 };
 
 // glu: gated experts, whose layer-1 tiles cover 128 hidden columns
@@ -331,7 +332,11 @@ MoeLayout moe_layout(int64_t T, int64_t N, int64_t O, int64_t P, int E, int k, b
     L.off_idx = take(static_cast<size_t>(L.R) * 4);
     L.off_w = take(static_cast<size_t>(L.R) * 4);
     L.off_pos = take(static_cast<size_t>(L.R) * 4);
-    L.off_src = take(static_cast<size_t>(L.Rmax) * 4);
+    const size_t blk_words = static_cast<size_t>(moe_route_blocks(T)) * E;   // per token block, per expert
+    L.off_hist = take(blk_words * 4);
+    L.off_bpad = take(blk_words * 4);
+    L.off_boff = take(blk_words * 4);
+    L.off_pad = take(static_cast<size_t>(2 * E) * 4);
     L.off_band = take(static_cast<size_t>(L.mbmax) * 4);
     L.off_nb = take(4);
     L.off_xp = take(static_cast<size_t>(L.Rmax) * N * 2);
@@ -649,7 +654,10 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
     int32_t* idx = reinterpret_cast<int32_t*>(base + L.off_idx);
     float* w = reinterpret_cast<float*>(base + L.off_w);
     int32_t* pos = reinterpret_cast<int32_t*>(base + L.off_pos);
-    int32_t* src = reinterpret_cast<int32_t*>(base + L.off_src);
+    int32_t* hist = reinterpret_cast<int32_t*>(base + L.off_hist);
+    int32_t* bpad = reinterpret_cast<int32_t*>(base + L.off_bpad);
+    int32_t* boff = reinterpret_cast<int32_t*>(base + L.off_boff);
+    int32_t* padt = reinterpret_cast<int32_t*>(base + L.off_pad);
     int32_t* band = reinterpret_cast<int32_t*>(base + L.off_band);
     int32_t* nb = reinterpret_cast<int32_t*>(base + L.off_nb);
     void* Xp = base + L.off_xp;
@@ -690,11 +698,11 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
     p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
 
     int fail = 0;
-    fail |= launch_moe_route(gate_logits, T, E, top_k, idx, w, s);
-    fail |= launch_moe_plan(idx, T, E, top_k, engine::BM, g_opt_moe_order.load() != 0 ? 1 : 0, pos, src, band, nb,
-                            routing ? routing->perm : nullptr,
+    fail |= launch_moe_route(gate_logits, T, E, top_k, idx, w, hist, s);
+    fail |= launch_moe_plan(hist, T, E, engine::BM, g_opt_moe_order.load() != 0 ? 1 : 0, bpad, boff, band, nb, padt,
                             routing ? routing->expert_offsets : nullptr, s);
-    fail |= launch_moe_gather(X, src, nb, engine::BM, N, Xp, d->sms * 4, s);
+    fail |= launch_moe_scatter(idx, T, E, top_k, bpad, boff, pos, routing ? routing->perm : nullptr, s);
+    fail |= launch_moe_gather(X, pos, T, top_k, padt, E, N, Xp, d->sms * 4, s);
     if (!fail) {
         timing_start(s);
         fail |= launch_engine_grouped(p, d->sms / 2, s);
@@ -704,7 +712,7 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
     delete pp;
     if (fail)
         return TFFN_ERR_CUDA;
-    g_last_launches = 5;
+    g_last_launches = 6;
     if (routing && routing->topk_idx &&
         cudaMemcpyAsync(routing->topk_idx, idx, static_cast<size_t>(L.R) * 4, cudaMemcpyDeviceToDevice, s) !=
             cudaSuccess)

@@ -28,12 +28,16 @@ int launch_decode(const decode::Params& p, int grid, cudaStream_t s);
 int launch_reduce(const reduce::Params& p, int max_pairs, cudaStream_t s);
 int launch_b2b(const reduce::Params& p, int max_pairs, cudaStream_t s);
 
-int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w,
+// Token blocks of the MoE routing (per-block expert counts, per-block scatter).
+int moe_route_blocks(int64_t T);
+int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w, int32_t* blk_hist,
                      cudaStream_t s);
-int launch_moe_plan(const int32_t* idx, int64_t T, int E, int k, int bm, int size_desc, int32_t* pos,
-                    int32_t* row_src, int32_t* band_expert, int32_t* nbands, int32_t* perm_out,
-                    int32_t* offs_out, cudaStream_t s);
-int launch_moe_gather(const void* X, const int32_t* row_src, const int32_t* nbands, int bm, int64_t N,
+int launch_moe_plan(const int32_t* blk_hist, int64_t T, int E, int bm, int size_desc, int32_t* blk_pad,
+                    int32_t* blk_off, int32_t* band_expert, int32_t* nbands, int32_t* pad, int32_t* offs_out,
+                    cudaStream_t s);
+int launch_moe_scatter(const int32_t* idx, int64_t T, int E, int k, const int32_t* blk_pad, const int32_t* blk_off,
+                       int32_t* pos, int32_t* perm_out, cudaStream_t s);
+int launch_moe_gather(const void* X, const int32_t* pos, int64_t T, int k, const int32_t* pad, int E, int64_t N,
                       void* Xp, int grid, cudaStream_t s);
 int launch_moe_combine(const float* Yp, const int32_t* pos, const float* w, int64_t T, int k, int64_t P,
                        void* Y, int grid, cudaStream_t s);

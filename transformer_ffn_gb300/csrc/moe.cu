@@ -18,188 +18,204 @@ namespace tffn {
 namespace moe {
 
 // ------------------------------------------------------------------ routing
+// Tokens are taken in blocks of ROUTE_BLOCK; the block's entries (t, s) are
+// ranked and copied by the same block of scatter_gather_kernel.
+constexpr int ROUTE_BLOCK = 128;
+
 // One thread per token: slot s takes the largest logit not yet taken, the
 // lower expert index winning ties; gate weights are the softmax over the k
-// kept logits.
-__global__ void route_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
-                             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w)
+// kept logits.  Each block also counts its entries per expert (blk_hist).
+__global__ void __launch_bounds__(ROUTE_BLOCK) route_kernel(const float* __restrict__ logits, int64_t T, int E,
+                                                            int k, int32_t* __restrict__ topk_idx,
+                                                            float* __restrict__ topk_w,
+                                                            int32_t* __restrict__ blk_hist)
 {
+    __shared__ int32_t hist[64];
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        hist[e] = 0;
+    __syncthreads();
     const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (t >= T)
-        return;
-    const float* l = logits + t * E;
-    uint64_t taken = 0;
-    float lmax = 0.0f;
-    for (int s = 0; s < k; ++s) {
-        int best = -1;
-        float bv = 0.0f;
-        for (int e = 0; e < E; ++e) {
-            if ((taken >> e) & 1ull)
-                continue;
-            const float v = l[e];
-            if (best < 0 || v > bv) {
-                best = e;
-                bv = v;
+    if (t < T) {
+        const float* l = logits + t * E;
+        uint64_t taken = 0;
+        float lmax = 0.0f;
+        for (int s = 0; s < k; ++s) {
+            int best = -1;
+            float bv = 0.0f;
+            for (int e = 0; e < E; ++e) {
+                if ((taken >> e) & 1ull)
+                    continue;
+                const float v = l[e];
+                if (best < 0 || v > bv) {
+                    best = e;
+                    bv = v;
+                }
             }
+            taken |= 1ull << best;
+            topk_idx[t * k + s] = best;
+            topk_w[t * k + s] = bv;
+            atomicAdd(&hist[best], 1);
+            if (s == 0)
+                lmax = bv;
         }
-        taken |= 1ull << best;
-        topk_idx[t * k + s] = best;
-        topk_w[t * k + s] = bv;
-        if (s == 0)
-            lmax = bv;
+        float sum = 0.0f;
+        for (int s = 0; s < k; ++s)
+            sum += expf(topk_w[t * k + s] - lmax);
+        const float inv = 1.0f / sum;
+        for (int s = 0; s < k; ++s)
+            topk_w[t * k + s] = expf(topk_w[t * k + s] - lmax) * inv;
     }
-    float sum = 0.0f;
-    for (int s = 0; s < k; ++s)
-        sum += expf(topk_w[t * k + s] - lmax);
-    const float inv = 1.0f / sum;
-    for (int s = 0; s < k; ++s)
-        topk_w[t * k + s] = expf(topk_w[t * k + s] - lmax) * inv;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        blk_hist[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
 }
 
 // --------------------------------------------------------------------- plan
-constexpr int PLAN_THREADS = 1024;
-
-// Exclusive scan of one value per thread across the block; returns the
-// thread's exclusive prefix and leaves the block total in *total.
-__device__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_sums, int32_t* total)
+// One small CTA.  From the per-block counts: each expert's padded segment
+// (laid out in expert index order, or, with size_desc, largest row count
+// first -- ties to the lower index -- the schedule order of "Fine-Grained
+// Compute-Communication Overlap for MoE", section 4.4, rule (ii)), the band
+// table, and for every token block the first grouped row of its entries of
+// each expert (blk_pad) and their first position in the unpadded, expert-index
+// order (blk_off, for the public permutation).  pad[2e], pad[2e+1]: first
+// padding row of expert e and how many follow.
+__global__ void plan_kernel(const int32_t* __restrict__ blk_hist, int nblk, int E, int bm, int size_desc,
+                            int32_t* __restrict__ blk_pad, int32_t* __restrict__ blk_off,
+                            int32_t* __restrict__ band_expert, int32_t* __restrict__ nbands,
+                            int32_t* __restrict__ pad, int32_t* __restrict__ offs_out)
 {
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    int32_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x += y;
-    }
-    if (lane == 31)
-        warp_sums[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int32_t s = warp_sums[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int32_t y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o)
-                s += y;
-        }
-        warp_sums[lane] = s;   // inclusive over warps
-    }
-    __syncthreads();
-    const int32_t before = (warp > 0 ? warp_sums[warp - 1] : 0) + (x - v);
-    *total = warp_sums[31];
-    __syncthreads();
-    return before;
-}
-
-// Single CTA.  Entries i = t*k + s are split into contiguous chunks, one per
-// thread, so a per-expert exclusive scan over threads keeps token order.
-// The experts' padded segments are laid out in expert index order, or, with
-// size_desc, largest row count first (ties: lower index first), the schedule
-// order of "Fine-Grained Compute-Communication Overlap for MoE", section 4.4,
-// rule (ii).  The public outputs (perm, offsets) keep expert index order
-// either way: they describe the grouping, not the internal layout.
-__global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(
-    const int32_t* __restrict__ topk_idx, int64_t T, int E, int k, int bm, int size_desc,
-    int32_t* __restrict__ pos, int32_t* __restrict__ row_src, int32_t* __restrict__ band_expert,
-    int32_t* __restrict__ nbands, int32_t* __restrict__ perm_out, int32_t* __restrict__ offs_out)
-{
-    __shared__ int32_t warp_sums[32];
-    __shared__ int32_t s_total[64];
-    __shared__ int32_t s_pad[64];       // first grouped row of expert e's segment
-    __shared__ int32_t s_pad_end[64];   // one past its last (padding included)
-    __shared__ int32_t s_off[65];
-    const int64_t R = T * k;
-    const int64_t chunk = (R + PLAN_THREADS - 1) / PLAN_THREADS;
-    const int64_t i0 = static_cast<int64_t>(threadIdx.x) * chunk;
-    const int64_t i1 = i0 + chunk < R ? i0 + chunk : R;
-
-    int32_t cnt[64];
-    for (int e = 0; e < E; ++e)
-        cnt[e] = 0;
-    for (int64_t i = i0; i < i1; ++i)
-        ++cnt[topk_idx[i]];
-    int32_t start[64];
-    for (int e = 0; e < E; ++e) {
-        int32_t tot;
-        start[e] = block_exclusive_scan(cnt[e], warp_sums, &tot);
-        if (threadIdx.x == 0)
-            s_total[e] = tot;
+    __shared__ int32_t tot[64], s_pad[64], s_end[64], s_off[65];
+    __shared__ int32_t s_nbands;
+    const int e = threadIdx.x;
+    if (e < E) {
+        int32_t c = 0;
+        for (int b = 0; b < nblk; ++b)
+            c += blk_hist[static_cast<int64_t>(b) * E + e];
+        tot[e] = c;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         int32_t order[64];
-        for (int e = 0; e < E; ++e) {
+        for (int x = 0; x < E; ++x) {
             // stable insertion: an expert goes after every earlier one that
             // is at least as large
-            int j = e;
+            int j = x;
             if (size_desc)
-                while (j > 0 && s_total[order[j - 1]] < s_total[e]) {
+                while (j > 0 && tot[order[j - 1]] < tot[x]) {
                     order[j] = order[j - 1];
                     --j;
                 }
-            order[j] = e;
+            order[j] = x;
         }
         int32_t p = 0;
         for (int j = 0; j < E; ++j) {
-            const int e = order[j];
-            s_pad[e] = p;
-            p += (s_total[e] + bm - 1) / bm * bm;
-            s_pad_end[e] = p;
+            const int x = order[j];
+            s_pad[x] = p;
+            p += (tot[x] + bm - 1) / bm * bm;
+            s_end[x] = p;
         }
         int32_t o = 0;
-        for (int e = 0; e < E; ++e) {
-            s_off[e] = o;
-            o += s_total[e];
+        for (int x = 0; x < E; ++x) {
+            s_off[x] = o;
+            o += tot[x];
         }
         s_off[E] = o;
+        s_nbands = p / bm;
         *nbands = p / bm;
     }
     __syncthreads();
-    // Scatter: grouped row of each (token, slot) entry, and its source token.
-    for (int64_t i = i0; i < i1; ++i) {
-        const int e = topk_idx[i];
-        const int32_t within = start[e]++;
-        const int32_t r = s_pad[e] + within;
-        pos[i] = r;
-        row_src[r] = static_cast<int32_t>(i / k);
-        if (perm_out)
-            perm_out[s_off[e] + within] = static_cast<int32_t>(i);
+    if (e < E) {
+        int32_t rp = s_pad[e], ro = s_off[e];
+        for (int b = 0; b < nblk; ++b) {
+            const int64_t at = static_cast<int64_t>(b) * E + e;
+            blk_pad[at] = rp;
+            blk_off[at] = ro;
+            const int32_t c = blk_hist[at];
+            rp += c;
+            ro += c;
+        }
+        pad[2 * e] = s_pad[e] + tot[e];
+        pad[2 * e + 1] = s_end[e] - (s_pad[e] + tot[e]);
     }
-    // Padding rows read no token; bands map to their expert.
-    for (int e = 0; e < E; ++e) {
-        for (int32_t r = s_pad[e] + s_total[e] + threadIdx.x; r < s_pad_end[e]; r += blockDim.x)
-            row_src[r] = -1;
-        for (int32_t b = s_pad[e] / bm + threadIdx.x; b < s_pad_end[e] / bm; b += blockDim.x)
-            band_expert[b] = e;
+    for (int b = threadIdx.x; b < s_nbands; b += blockDim.x) {
+        int x = 0;
+        while (x < E - 1 && !(b * bm >= s_pad[x] && b * bm < s_end[x]))
+            ++x;
+        band_expert[b] = x;
     }
     if (offs_out)
-        for (int e = threadIdx.x; e <= E; e += blockDim.x)
-            offs_out[e] = s_off[e];
+        for (int x = threadIdx.x; x <= E; x += blockDim.x)
+            offs_out[x] = s_off[x];
+}
+
+// ------------------------------------------------------------------ scatter
+// One block per token block.  Warp 0 ranks the block's entries i = t*k + s in
+// order (a warp-wide match of the expert ids of 32 consecutive entries gives
+// each its rank among the equal ones; a running count per expert carries the
+// rank across groups), which keeps (expert, token) order stably.
+__global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int E, int k,
+                                                     const int32_t* __restrict__ blk_pad,
+                                                     const int32_t* __restrict__ blk_off, int32_t* __restrict__ pos,
+                                                     int32_t* __restrict__ perm_out)
+{
+    __shared__ int32_t cnt[64];
+    const int lane = threadIdx.x;
+    const int64_t b = blockIdx.x;
+    const int64_t i0 = b * ROUTE_BLOCK * k;
+    const int64_t R = T * k;
+    const int n_ent = static_cast<int>(i0 + ROUTE_BLOCK * k <= R ? ROUTE_BLOCK * k : R - i0);
+    cnt[lane] = 0;
+    cnt[lane + 32] = 0;
+    __syncwarp();
+    for (int c = 0; c < n_ent; c += 32) {
+        const int j = c + lane;
+        const bool valid = j < n_ent;
+        const int e = valid ? topk_idx[i0 + j] : -1;
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & ((1u << lane) - 1u));
+        const int32_t base = valid ? cnt[e] : 0;
+        if (valid) {
+            pos[i0 + j] = blk_pad[b * E + e] + base + rank;
+            if (perm_out)
+                perm_out[blk_off[b * E + e] + base + rank] = static_cast<int32_t>(i0 + j);
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(same) - 1)
+            cnt[e] = base + __popc(same);
+        __syncwarp();
+    }
 }
 
 // ------------------------------------------------------------------- gather
-// One warp per grouped row: X_perm[r] = X[row_src[r]] (zeros for padding).
-__global__ void gather_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restrict__ row_src,
-                              const int32_t* __restrict__ nbands, int bm, int64_t N,
-                              __nv_bfloat16* __restrict__ Xp)
+// One warp per entry: X_perm[pos[i]] = X[i / k]; then the experts' padding
+// rows (pad[2e] first row, pad[2e+1] count), numbered across experts, are
+// zeroed, one per warp.
+__global__ void gather_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restrict__ pos, int64_t R, int k,
+                              const int32_t* __restrict__ pad, int E, int64_t N, __nv_bfloat16* __restrict__ Xp)
 {
-    const int64_t rows = static_cast<int64_t>(*nbands) * bm;
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    const int64_t nvec = N / 8;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-         r += warps) {
-        const int32_t t = row_src[r];
-        uint4* dst = reinterpret_cast<uint4*>(Xp + r * N);
-        if (t < 0) {
-            for (int64_t c = lane; c < nvec; c += 32)
-                dst[c] = make_uint4(0u, 0u, 0u, 0u);
-        } else {
-            const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(t) * N);
-            for (int64_t c = lane; c < nvec; c += 32)
-                dst[c] = __ldg(src + c);
+    const int64_t w0 = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t nvec = N / 8;   // 16-byte vectors per row
+    for (int64_t i = w0; i < R; i += warps) {
+        const uint4* src = reinterpret_cast<const uint4*>(X + (i / k) * N);
+        uint4* dst = reinterpret_cast<uint4*>(Xp + static_cast<int64_t>(pos[i]) * N);
+        for (int64_t c = lane; c < nvec; c += 32)
+            dst[c] = __ldg(src + c);
+    }
+    int64_t total = 0;
+    for (int e = 0; e < E; ++e)
+        total += pad[2 * e + 1];
+    for (int64_t q = w0; q < total; q += warps) {
+        int e = 0;
+        int64_t rest = q;
+        while (rest >= pad[2 * e + 1]) {
+            rest -= pad[2 * e + 1];
+            ++e;
         }
+        uint4* dst = reinterpret_cast<uint4*>(Xp + (pad[2 * e] + rest) * N);
+        for (int64_t c = lane; c < nvec; c += 32)
+            dst[c] = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -232,28 +248,38 @@ __global__ void combine_kernel(const float* __restrict__ Yp, const int32_t* __re
 
 }  // namespace moe
 
-int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w,
+int moe_route_blocks(int64_t T)
+{
+    return static_cast<int>((T + moe::ROUTE_BLOCK - 1) / moe::ROUTE_BLOCK);
+}
+
+int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w, int32_t* blk_hist,
                      cudaStream_t s)
 {
-    const int threads = 256;
-    const int64_t blocks = (T + threads - 1) / threads;
-    moe::route_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(logits, T, E, k, idx, w);
+    moe::route_kernel<<<moe_route_blocks(T), moe::ROUTE_BLOCK, 0, s>>>(logits, T, E, k, idx, w, blk_hist);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
-int launch_moe_plan(const int32_t* idx, int64_t T, int E, int k, int bm, int size_desc, int32_t* pos,
-                    int32_t* row_src, int32_t* band_expert, int32_t* nbands, int32_t* perm_out,
-                    int32_t* offs_out, cudaStream_t s)
+int launch_moe_plan(const int32_t* blk_hist, int64_t T, int E, int bm, int size_desc, int32_t* blk_pad,
+                    int32_t* blk_off, int32_t* band_expert, int32_t* nbands, int32_t* pad, int32_t* offs_out,
+                    cudaStream_t s)
 {
-    moe::plan_kernel<<<1, moe::PLAN_THREADS, 0, s>>>(idx, T, E, k, bm, size_desc, pos, row_src, band_expert, nbands,
-                                                     perm_out, offs_out);
+    moe::plan_kernel<<<1, 64, 0, s>>>(blk_hist, moe_route_blocks(T), E, bm, size_desc, blk_pad, blk_off,
+                                      band_expert, nbands, pad, offs_out);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
-int launch_moe_gather(const void* X, const int32_t* row_src, const int32_t* nbands, int bm, int64_t N,
+int launch_moe_scatter(const int32_t* idx, int64_t T, int E, int k, const int32_t* blk_pad, const int32_t* blk_off,
+                       int32_t* pos, int32_t* perm_out, cudaStream_t s)
+{
+    moe::scatter_kernel<<<moe_route_blocks(T), 32, 0, s>>>(idx, T, E, k, blk_pad, blk_off, pos, perm_out);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_moe_gather(const void* X, const int32_t* pos, int64_t T, int k, const int32_t* pad, int E, int64_t N,
                       void* Xp, int grid, cudaStream_t s)
 {
-    moe::gather_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), row_src, nbands, bm, N,
+    moe::gather_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), pos, T * k, k, pad, E, N,
                                             static_cast<__nv_bfloat16*>(Xp));
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
