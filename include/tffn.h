@@ -75,7 +75,7 @@ typedef enum {
  * Numerics: products accumulate in fp32; H is rounded to bf16 (round to
  * nearest even) after b1 and act1, as it is stored between the layers; Y is
  * rounded to bf16 after b2 and act2.
- * Paths: M <= 32 streams the weights (split-K, HBM-bound decode shapes);
+ * Paths: M <= 64 streams the weights (split-K, HBM-bound decode shapes);
  * larger M runs the persistent tcgen05 engine (GEMM1 tiles publish ready
  * flags that GEMM2 tiles consume in the same launch).
  */
@@ -99,7 +99,7 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
  *
  * Numerics: products accumulate in fp32; H = act(X W1) * (X W3) is rounded to
  * bf16 (nearest even) where it is stored between the layers; Y is rounded to
- * bf16.  Paths: M <= 32 streams the weights (each layer-1 unit loads the same
+ * bf16.  Paths: M <= 64 streams the weights (each layer-1 unit loads the same
  * 64 columns of W1 and W3); larger M runs the persistent tcgen05 engine, each
  * layer-1 tile pairing 128 columns of W1 with the same 128 columns of W3 in
  * one 256-column accumulator.  Errors and workspace as ffn_forward.

@@ -79,6 +79,9 @@ def test_engine_ragged_shapes(cuda_lib, shape, acts):
     ((8, 4096, 8192, 1024), ("relu", "none")),          # long split-K ranges
     ((16, 4096, 1024, 256), ("gelu_tanh", "none")),     # N > O: more layer-1 k than hidden columns
     ((4, 2048, 136, 4096), ("relu", "none")),           # N > O, narrow ragged hidden, wide output
+    ((48, 512, 1024, 256), ("gelu_tanh", "none")),      # four 16-row tiles (64-row instance)
+    ((64, 1024, 2048, 512), ("relu", "gelu_tanh")),
+    ((33, 136, 520, 264), ("gelu_tanh", "relu")),       # one row past the 32-row instance, ragged
 ])
 def test_decode_path_full(cuda_lib, shape, acts):
     M, N, O, P = shape

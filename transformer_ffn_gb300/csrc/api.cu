@@ -39,7 +39,7 @@ constexpr size_t SYNC_BYTES = size_t(5) << 20;
 static_assert(OFF_DCOUNT + DCOUNT_WORDS * 4 <= SYNC_BYTES, "sync region layout");
 constexpr uint32_t EPOCH_LIMIT = 0x7FFFFFF0u;      // launches before the flag region is cleared
 
-constexpr int64_t DECODE_MAX_M = 32;
+constexpr int64_t DECODE_MAX_M = 64;   // the weight stream wins up to here (measured against the engine)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -263,7 +263,7 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, int sms, bo
     int64_t path = g_opt_path.load();
     if (path == 0)
         path = (M <= DECODE_MAX_M) ? 2 : 1;
-    if (path == 2 && M > DECODE_MAX_M)
+    if (path == 2 && M > decode::MAX_ROWS)
         path = 1;
     if ((path == 4 || path == 5) && glu)
         path = 1;
@@ -395,7 +395,7 @@ static int run_decode(DeviceState& d, uint8_t* base, const DenseLayout& L, const
     if (static_cast<size_t>(p.plan.slices[0]) * 4 > FLAG_WORDS ||
         (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * 4 > DCOUNT_WORDS)
         return TFFN_ERR_UNSUPPORTED;
-    const uint32_t arows = M <= 16 ? 16u : 32u;
+    const uint32_t arows = M <= 16 ? 16u : static_cast<uint32_t>(decode::decode_rows(M));
     // Gated layer 1 loads 64-column boxes of W1 and W3 (128 B per row) whose
     // neighbours belong to other units: no promotion past 128 B, or every
     // weight row would be fetched twice.

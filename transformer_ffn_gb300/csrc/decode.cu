@@ -11,8 +11,8 @@ namespace decode {
 static_assert(SLICE == KC, "a layer-2 unit reads one dense (or two gated) layer-1 slices of H");
 
 struct Aux {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint32_t abort;
     uint32_t epoch;     // this launch's ready-flag value (control block's + 1)
 };
@@ -77,14 +77,15 @@ __device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uin
     const uint32_t cb_chunk = GLU ? static_cast<uint32_t>(cw) * 2 : static_cast<uint32_t>(cw & 1) * 4;
     const uint32_t j = static_cast<uint32_t>(lane >> 3);
     const uint32_t r = static_cast<uint32_t>(lane & 7);
+    constexpr int KB = Geo<MT>::KB;
 #pragma unroll
-    for (int half = 0; half < KC / 64; ++half) {
-        uint32_t a[4][MT][4];
-        uint32_t b[4][2][4];
+    for (int kb0 = 0; kb0 < KC / 16; kb0 += KB) {
+        uint32_t a[KB][MT][4];
+        uint32_t b[KB][2][4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const int ks = half * 4 + kk;
-            const uint32_t abox = a_base + static_cast<uint32_t>(ks >> 2) * A_BOX_BYTES;
+        for (int kk = 0; kk < KB; ++kk) {
+            const int ks = kb0 + kk;
+            const uint32_t abox = a_base + static_cast<uint32_t>(ks >> 2) * Geo<MT>::A_BOX;
             const uint32_t kchunk = static_cast<uint32_t>((ks & 3) * 2) + (j >> 1);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
@@ -100,7 +101,7 @@ __device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uin
             }
         }
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int kk = 0; kk < KB; ++kk)
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr)
 #pragma unroll
@@ -130,8 +131,8 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
 
     if (nparts > 1) {
         float* base = p.partial + pl.part_off[layer] +
-                      (static_cast<int64_t>(slice) * pl.maxp[layer]) * MAX_ROWS * SLICE;
-        float* mine = base + static_cast<int64_t>(part) * MAX_ROWS * SLICE;
+                      (static_cast<int64_t>(slice) * pl.maxp[layer]) * Geo<MT>::ROWS * SLICE;
+        float* mine = base + static_cast<int64_t>(part) * Geo<MT>::ROWS * SLICE;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -155,7 +156,7 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
         __threadfence();
         zero(acc);
         for (int pp = 0; pp < nparts; ++pp) {
-            const float* src = base + static_cast<int64_t>(pp) * MAX_ROWS * SLICE;
+            const float* src = base + static_cast<int64_t>(pp) * Geo<MT>::ROWS * SLICE;
 #pragma unroll
             for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -295,6 +296,8 @@ template <int MT>
 __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const WaitCtx& w, int lane)
 {
     constexpr uint32_t A_BYTES = 2u * (16u * MT) * 64u * 2u;
+    constexpr int STAGES = Geo<MT>::NST;
+    constexpr int STAGE_BYTES = Geo<MT>::STAGE;
     const Plan& pl = p.plan;
     const int64_t G = pl.grid, c = blockIdx.x;
     uint32_t stage = 0, phase = 0;
@@ -325,7 +328,7 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
         const uint32_t fb = ptx::smem_u32(&aux.full[st]);
         const uint32_t sa = ptx::smem_u32(stages + st * STAGE_BYTES) + W_STAGE_BYTES;
         ptx::tma_load_2d(sa, &p.map_a[layer], fb, static_cast<int32_t>(kc * KC), 0);
-        ptx::tma_load_2d(sa + A_BOX_BYTES, &p.map_a[layer], fb, static_cast<int32_t>(kc * KC + 64), 0);
+        ptx::tma_load_2d(sa + Geo<MT>::A_BOX, &p.map_a[layer], fb, static_cast<int32_t>(kc * KC + 64), 0);
     };
     auto advance = [&]() {
         if (++stage == STAGES) {
@@ -415,6 +418,8 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
 template <int MT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_constant__ Params p)
 {
+    constexpr int STAGES = Geo<MT>::NST;
+    constexpr int STAGE_BYTES = Geo<MT>::STAGE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -492,23 +497,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
 
 }  // namespace decode
 
-int launch_decode(const decode::Params& p, int grid, cudaStream_t s)
+namespace {
+
+template <int MT>
+int launch_decode_mt(const decode::Params& p, cudaStream_t s)
 {
-    (void)grid;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(decode::decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 decode::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(decode::decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 decode::SMEM_BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(decode::decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 decode::Geo<MT>::SMEM) != cudaSuccess)
             return -1;
         attr_set = true;
     }
-    if (p.M <= 16)
-        decode::decode_kernel<1><<<p.plan.grid, decode::NUM_THREADS, decode::SMEM_BYTES, s>>>(p);
-    else
-        decode::decode_kernel<2><<<p.plan.grid, decode::NUM_THREADS, decode::SMEM_BYTES, s>>>(p);
+    decode::decode_kernel<MT><<<p.plan.grid, decode::NUM_THREADS, decode::Geo<MT>::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int launch_decode(const decode::Params& p, int grid, cudaStream_t s)
+{
+    (void)grid;
+    if (p.M <= 16)
+        return launch_decode_mt<1>(p, s);
+    if (p.M <= 32)
+        return launch_decode_mt<2>(p, s);
+    return launch_decode_mt<4>(p, s);
 }
 
 }  // namespace tffn

@@ -40,16 +40,34 @@ namespace decode {
 
 constexpr int SLICE = 128;              // output columns per unit
 constexpr int KC = 128;                 // K rows per unit
-constexpr int MAX_ROWS = 32;            // rows handled by this path
-constexpr int STAGES = 5;
+constexpr int MAX_ROWS = 64;            // rows handled by this path
+constexpr int MAX_STAGES = 5;
 constexpr int CONSUMER_WARPS = 4;       // 32 columns each
 constexpr int NUM_THREADS = 32 * (1 + CONSUMER_WARPS);
 constexpr int W_BOX_BYTES = KC * 64 * 2;                 // 16 KiB: KC rows x 64 cols
 constexpr int W_STAGE_BYTES = 2 * W_BOX_BYTES;           // 32 KiB
-constexpr int A_BOX_BYTES = MAX_ROWS * 64 * 2;           // 4 KiB: 32 rows x 64 k
-constexpr int A_STAGE_BYTES = 2 * A_BOX_BYTES;           // 8 KiB
-constexpr int STAGE_BYTES = W_STAGE_BYTES + A_STAGE_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+
+// Geometry of the kernel instance for MT tiles of 16 rows (MT 1 and 2 share
+// one layout; MT 4 covers up to 64 rows): the A (X or H) box slot holds ROWS
+// rows of 64 k; a stage is the W tile plus two A boxes; NST stages fill the
+// shared memory; KB k-steps of fragments are loaded before their MMAs (fewer
+// for more rows: registers).
+template <int MT>
+struct Geo {
+    static constexpr int ROWS = MT <= 2 ? 32 : 16 * MT;
+    static constexpr int A_BOX = ROWS * 64 * 2;
+    static constexpr int STAGE = W_STAGE_BYTES + 2 * A_BOX;
+    static constexpr int NST = MT <= 2 ? 5 : 4;
+    static constexpr int SMEM = NST * STAGE + 1024 + 1024;
+    static constexpr int KB = MT <= 2 ? 4 : 2;
+};
+static_assert(Geo<4>::SMEM <= 232448 && Geo<1>::SMEM <= 232448, "shared memory");
+
+// Rows of a partial-sum block for M rows (the kernel instance's ROWS).
+inline int decode_rows(int64_t M)
+{
+    return M <= 32 ? 32 : 64;
+}
 
 struct Plan {
     int32_t grid;
@@ -77,8 +95,8 @@ __host__ __device__ inline int64_t range_start(int64_t c, int64_t U, int64_t G)
 // owns at least one unit of each layer.
 inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool glu = false)
 {
-    (void)M;
     Plan pl{};
+    const int64_t rows = decode_rows(M);
     const int64_t h_cols = glu ? SLICE / 2 : SLICE;   // hidden columns per layer-1 slice
     pl.h_per_k = static_cast<int32_t>(KC / h_cols);
     pl.slices[0] = static_cast<int32_t>((O + h_cols - 1) / h_cols);
@@ -105,7 +123,7 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool
         }
         pl.maxp[l] = maxp;
         pl.part_off[l] = static_cast<int64_t>(off / 4);
-        off += static_cast<size_t>(pl.slices[l]) * maxp * MAX_ROWS * SLICE * 4;
+        off += static_cast<size_t>(pl.slices[l]) * maxp * rows * SLICE * 4;
     }
     pl.partial_bytes = off;
     return pl;

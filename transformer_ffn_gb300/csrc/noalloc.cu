@@ -94,7 +94,7 @@ extern "C" int ffn_forward_decode_noalloc(const void* X, const void* W1, const v
                                           int64_t P, void* Y, struct CUstream_st* stream)
 {
     using namespace tffn;
-    if (M < 0 || M > decode::MAX_ROWS || !dim8(N) || !dim8(O) || !dim8(P) || !act_valid(act1) ||
+    if (M < 0 || M > 32 || !dim8(N) || !dim8(O) || !dim8(P) || !act_valid(act1) ||
         !act_valid(act2))
         return TFFN_ERR_INVALID_ARG;
     if (M == 0)
