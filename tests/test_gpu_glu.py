@@ -98,7 +98,7 @@ def test_glu_full_size_sampled_rows(cuda_lib):
 
 
 def test_dense_ffn_with_silu_on_both_paths(cuda_lib):
-    # SiLU as the dense FFN's activation, on the weight-streaming path (M <= 32)
+    # SiLU as the dense FFN's activation, on the weight-streaming path (M <= 64)
     # and on the engine
     for M in (16, 200):
         inp = synth.ffn_inputs(M, 256, 512, 128, seed=M, device="cuda")
@@ -110,7 +110,7 @@ def test_dense_ffn_with_silu_on_both_paths(cuda_lib):
         _assert_close(Y.float().cpu().numpy(), want, f"silu M={M}")
 
 
-# ------------------------------------------------ weight-streaming path, M <= 32
+# ------------------------------------------------ weight-streaming path, M <= 64
 
 @pytest.mark.parametrize("M,N,O,P,act", [
     (1, 256, 384, 136, "silu"),
@@ -134,7 +134,7 @@ def test_glu_decode_path_full(cuda_lib, M, N, O, P, act):
 
 def test_glu_decode_deterministic_and_close_to_engine(cuda_lib):
     X, W1, W3, W2 = _inputs(24, 1024, 3072, 1024, seed=12)
-    a = cuda_lib.ffn_glu_forward(X, W1, W3, W2, "silu")      # auto: the weight stream at M <= 32
+    a = cuda_lib.ffn_glu_forward(X, W1, W3, W2, "silu")      # auto: the weight stream at M <= 64
     b = cuda_lib.ffn_glu_forward(X, W1, W3, W2, "silu")
     prev = cuda_lib.set_option(cuda_lib.OPT_PATH, 1)
     try:

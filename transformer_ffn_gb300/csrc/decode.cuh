@@ -1,7 +1,7 @@
 // decode.cuh -- the small-M (decode) path: both layers of the FFN as one
 // persistent launch that streams the weights from HBM exactly once.
 //
-// At M <= 32 rows the FFN is bound by reading W1 and W2 ("kernel fusion"
+// At M <= 64 rows the FFN is bound by reading W1 and W2 ("kernel fusion"
 // page, section "Complexity and constants": a memory-bound kernel takes the
 // bytes it moves divided by the achievable HBM bandwidth, and needs 16-byte
 // accesses to get there).  Work is cut into units of SLICE output columns x KC
