@@ -4,8 +4,9 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl refe
 
 A step is one ffn_forward (or moe_ffn_forward) call over one batch of
 synthetic input resident in HBM.  Timing: W untimed warm-up steps, then K
-steps, each bracketed by CUDA events on the launching stream, with a 256 MiB
-write between steps so that L2 (129 MB) holds nothing of the previous step;
+steps, each bracketed by CUDA events on the launching stream; when a step's
+inputs are under twice the L2 (129 MB), a 256 MiB write between steps so that
+L2 holds nothing of the previous step (larger inputs stream through it);
 a barrier + device synchronisation on both sides of the timed block; the max
 over ranks.  Under torchrun every rank runs its own replica of the workload
 (the FFN has no data-path exchange: weak scaling, no collective but the
@@ -140,6 +141,16 @@ def measured_peaks():
         return 1900.0, 6800.0, "fallback"
 
 
+def sustained_bf16_peak():
+    """cuBLAS bf16 throughput held for seconds under the power cap (context
+    for long runs of a tensor-bound kernel), or None."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return None
+
+
 def kernel_sha(kernel):
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
@@ -167,28 +178,36 @@ def recorded_traffic(config, kernel=None):
 
 # -------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons every 20 ms, each sample stamped,
+    so that the median and the reasons come from the samples taken inside the
+    timed region (mark() brackets it)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
         self.thread = None
+        self.window = [None, None]
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        time.sleep(0.1)   # the first samples arrive before the timed region starts
+
+    def mark(self, which):
+        self.window[0 if which == "start" else 1] = time.time()
 
     def _read(self):
         for line in self.proc.stdout:
@@ -197,7 +216,7 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.05)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -205,24 +224,44 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarize_clocks(self.lines, self.window, self.INTERVAL_MS)
+
+
+def summarize_clocks(lines, window, interval_ms):
+    """Median SM clock, max clock and active throttle reasons of the samples
+    (nvidia-smi csv lines: timestamp, index, clocks.sm, clocks.max.sm, power,
+    reasons.active, hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown,
+    sw_power_cap) taken inside window = [t0, t1] (host epoch seconds, one
+    interval of slack on each side); the sample nearest the window when none
+    falls inside it."""
+    import datetime
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    samples = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            samples.append((ts, float(parts[2]), float(parts[3]),
+                            {n for n, v in zip(names, parts[6:10]) if v.lower() == "active"}))
+        except ValueError:
+            continue
+    if not samples:
+        return None
+    t0, t1 = window
+    slack = interval_ms / 1e3
+    inside = [x for x in samples if t0 is not None and t1 is not None and t0 - slack <= x[0] <= t1 + slack]
+    where = "timed region"
+    if not inside:
+        ref = t0 if t0 is not None else samples[0][0]
+        inside = [min(samples, key=lambda x: abs(x[0] - ref))]
+        where = "nearest sample to the timed region"
+    reasons = set()
+    for x in inside:
+        reasons |= x[3]
+    return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": max(x[2] for x in samples),
+            "reasons": sorted(reasons), "samples": len(inside), "interval_ms": interval_ms, "from": where}
 
 
 # ------------------------------------------------------------------- helpers
@@ -435,11 +474,13 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     sampler.start()
     tffn.timing_begin()
+    sampler.mark("start")
     t0 = time.perf_counter()
     per_step = time_steps(step, args.steps, flush_buf, stream)
     barrier(world)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    sampler.mark("end")
     n_dom, dom_ms = tffn.timing_end()
     clocks = sampler.stop()
     tffn.check()
@@ -458,6 +499,11 @@ def run_gpu(args, world, rank, local):
     else:
         roof = {"bound": "tensor", "achieved": flops(cfg) / dom_s / 1e12, "peak": peak_tf, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    if not is_hbm_bound(cfg) and sustained_bf16_peak():
+        # the burst peak is the denominator; a run of many steps meets the power cap
+        # like the sustained measurement does, so that fraction is given for context
+        roof["sustained_peak"] = sustained_bf16_peak()
+        roof["frac_of_sustained"] = roof["achieved"] / roof["sustained_peak"]
     # the datasheet's dense peaks, for context (the fraction above is the one reported)
     roof["spec_peak"] = SPEC_HBM_GBS if is_hbm_bound(cfg) else SPEC_BF16_TFLOPS
     roof["frac_of_spec"] = roof["achieved"] / roof["spec_peak"]
@@ -613,7 +659,9 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 200 on the GPU, whose steps take 0.05-10 ms, so that the "
+                         "clock samples fall inside the timed region; 20 for the CPU reference arm)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT, choices=sorted(CONFIGS))
     ap.add_argument("--ffn-path", default="auto", choices=sorted(FFN_PATHS),
@@ -627,6 +675,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 20 if args.impl == "reference" else 200
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
     world, rank, local = dist_setup()
