@@ -70,7 +70,8 @@ SPEC_BF16_TFLOPS = 2250.0   # GB300 dense bf16 (NVIDIA's 2:4-sparse figures are 
 SPEC_HBM_GBS = 8000.0       # GB300 HBM3e
 
 # Dominant kernel of each workload (for the ncu traffic record).
-KERNEL = {"tiny": "engine_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
+DECODE_MAX_M = 64   # rows up to which ffn_forward / ffn_glu_forward stream the weights
+KERNEL = {"tiny": "decode_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
           "swiglu": "engine_kernel", "swiglu_decode": "decode_kernel", "moe": "engine_kernel", "moe_swiglu": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
           "decode": "decode_kernel"}
 # Sources a kernel's DRAM traffic depends on: its own code and the host code
@@ -96,6 +97,10 @@ def dominant_kernel(config, ffn_path="auto"):
         return "decode_kernel"
     if ffn_path in ("fused", "two"):
         return "engine_kernel"
+    cfg = CONFIGS[config]
+    if cfg["kind"] in ("ffn", "glu"):
+        # the library's own choice: the weight stream up to 64 rows, the engine above
+        return "decode_kernel" if cfg["M"] <= DECODE_MAX_M else "engine_kernel"
     return KERNEL[config]
 
 
