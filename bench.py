@@ -50,6 +50,10 @@ CONFIGS = {
                          "Y = (SiLU(X W1) * (X W3)) W2, no biases"),
     "swiglu_decode": dict(kind="glu", M=16, N=4096, O=14336, P=4096, act1="silu", act2="none",
                           label="SwiGLU FFN decode (Llama 3 8B shape) M=16 N=4096 O=14336 P=4096"),
+    "batch128": dict(kind="ffn", M=128, N=4096, O=14336, P=4096, act1="gelu_tanh", act2="none",
+                     label="batched decode FFN (Llama 3 8B dims) M=128 N=4096 O=14336 P=4096, GELU-tanh"),
+    "swiglu_batch128": dict(kind="glu", M=128, N=4096, O=14336, P=4096, act1="silu", act2="none",
+                            label="SwiGLU FFN batched decode (Llama 3 8B shape) M=128 N=4096 O=14336 P=4096"),
     "moe_swiglu": dict(kind="moe", glu=True, M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="silu",
                        act2="none",
                        label="MoE FFN with SwiGLU experts (Mixtral-class) T=8192 N=4096 E=8 O=14336 P=4096, "
@@ -64,16 +68,17 @@ CONFIGS = {
                              "stress-skewed router (expert 0 in ~98% of tokens)"),
 }
 DEFAULT = "prefill"
-FFN_PATHS = {"auto": 0, "fused": 1, "decode": 2, "two": 3, "reduce": 4, "b2b": 5}
+FFN_PATHS = {"auto": 0, "fused": 1, "decode": 2, "two": 3, "reduce": 4, "b2b": 5, "stream": 6}
 FLUSH_BYTES = 256 << 20
 SPEC_BF16_TFLOPS = 2250.0   # GB300 dense bf16 (NVIDIA's 2:4-sparse figures are twice this)
 SPEC_HBM_GBS = 8000.0       # GB300 HBM3e
 
 # Dominant kernel of each workload (for the ncu traffic record).
-DECODE_MAX_M = 64   # rows up to which ffn_forward / ffn_glu_forward stream the weights
+DECODE_MAX_M = 64   # rows up to which ffn_forward / ffn_glu_forward stream the weights with mma.sync
+STREAM_MAX_M = 128  # ... and then with tcgen05 MMAs
 KERNEL = {"tiny": "decode_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
           "swiglu": "engine_kernel", "swiglu_decode": "decode_kernel", "moe": "engine_kernel", "moe_swiglu": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",
-          "decode": "decode_kernel"}
+          "decode": "decode_kernel", "batch128": "wstream_kernel", "swiglu_batch128": "wstream_kernel"}
 # Sources a kernel's DRAM traffic depends on: its own code and the host code
 # that builds its tensor maps (box shapes, L2 promotion).
 KERNEL_SOURCES = {
@@ -84,6 +89,7 @@ KERNEL_SOURCES = {
                       "api.cu"],
     "b2b_kernel": ["reduce.cuh", "reduce_params.cuh", "engine.cuh", "common.cuh", "ptx.cuh", "engine_reduce.cu",
                    "api.cu"],
+    "wstream_kernel": ["wstream.cu", "wstream.cuh", "common.cuh", "ptx.cuh", "api.cu"],
 }
 
 
@@ -93,14 +99,18 @@ def dominant_kernel(config, ffn_path="auto"):
         return "reduce_kernel"
     if ffn_path == "b2b" and CONFIGS[config]["kind"] == "ffn":
         return "b2b_kernel"
-    if ffn_path == "decode" and CONFIGS[config]["kind"] == "ffn":
+    if ffn_path == "decode" and CONFIGS[config]["kind"] in ("ffn", "glu"):
         return "decode_kernel"
+    if ffn_path == "stream" and CONFIGS[config]["kind"] in ("ffn", "glu"):
+        return "wstream_kernel"
     if ffn_path in ("fused", "two"):
         return "engine_kernel"
     cfg = CONFIGS[config]
     if cfg["kind"] in ("ffn", "glu"):
         # the library's own choice: the weight stream up to 64 rows, the engine above
-        return "decode_kernel" if cfg["M"] <= DECODE_MAX_M else "engine_kernel"
+        if cfg["M"] <= DECODE_MAX_M:
+            return "decode_kernel"
+        return "wstream_kernel" if cfg["M"] <= STREAM_MAX_M else "engine_kernel"
     return KERNEL[config]
 
 
@@ -122,7 +132,8 @@ def weight_bytes(cfg):
 
 
 def is_hbm_bound(cfg):
-    return cfg["kind"] in ("ffn", "glu") and cfg["M"] <= 32
+    # the weight streams: M up to 128 rows, below the ridge (2 M FLOP per weight byte pair)
+    return cfg["kind"] in ("ffn", "glu") and cfg["M"] <= STREAM_MAX_M
 
 
 def metric_of(cfg):
@@ -672,7 +683,7 @@ def main():
     ap.add_argument("--ffn-path", default="auto", choices=sorted(FFN_PATHS),
                     help="dense FFN path: auto, fused (engine), decode, two (two launches), "
                          "reduce (the reduce-add form of the fused-FFN page, section Step 1), "
-                         "b2b (back-to-back, H on chip)")
+                         "b2b (back-to-back, H on chip), stream (tensor-core weight stream)")
     ap.add_argument("--moe-order", type=int, default=1, choices=(0, 1),
                     help="MoE grouped-layout segment order: 0 expert index, 1 largest expert first")
     ap.add_argument("--impl", default="tffn", choices=["tffn", "reference"])

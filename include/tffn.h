@@ -75,9 +75,11 @@ typedef enum {
  * Numerics: products accumulate in fp32; H is rounded to bf16 (round to
  * nearest even) after b1 and act1, as it is stored between the layers; Y is
  * rounded to bf16 after b2 and act2.
- * Paths: M <= 64 streams the weights (split-K, HBM-bound decode shapes);
- * larger M runs the persistent tcgen05 engine (GEMM1 tiles publish ready
- * flags that GEMM2 tiles consume in the same launch).
+ * Paths: M <= 64 streams the weights with mma.sync (split-K, HBM-bound
+ * decode shapes); 65 <= M <= 128 streams them with tcgen05 MMAs (the weights
+ * as the MMA's M side, still HBM-bound); larger M runs the persistent tcgen05
+ * engine (GEMM1 tiles publish ready flags that GEMM2 tiles consume in the
+ * same launch).
  */
 int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, const void* b2,
                 int act1, int act2, int64_t M, int64_t N, int64_t O, int64_t P, void* Y,
@@ -99,10 +101,12 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
  *
  * Numerics: products accumulate in fp32; H = act(X W1) * (X W3) is rounded to
  * bf16 (nearest even) where it is stored between the layers; Y is rounded to
- * bf16.  Paths: M <= 64 streams the weights (each layer-1 unit loads the same
- * 64 columns of W1 and W3); larger M runs the persistent tcgen05 engine, each
- * layer-1 tile pairing 128 columns of W1 with the same 128 columns of W3 in
- * one 256-column accumulator.  Errors and workspace as ffn_forward.
+ * bf16.  Paths: M <= 64 streams the weights with mma.sync (each layer-1 unit
+ * loads the same 64 columns of W1 and W3); 65 <= M <= 128 streams them with
+ * tcgen05 MMAs (gate and linear products in two tensor-memory accumulators);
+ * larger M runs the persistent tcgen05 engine, each layer-1 tile pairing 128
+ * columns of W1 with the same 128 columns of W3 in one 256-column
+ * accumulator.  Errors and workspace as ffn_forward.
  */
 int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W2, int act, int64_t M,
                     int64_t N, int64_t O, int64_t P, void* Y, struct CUstream_st* stream);
@@ -227,8 +231,11 @@ const char* tffn_status_string(int status);
  *                         fp32 Y; results vary in the last bits run to run),
  *                         5 back-to-back (each task walks the hidden tiles of
  *                         one band for one Y tile, H only in shared memory,
- *                         products summed in tensor memory; for small FFNs);
- *                         4 and 5 apply to ffn_forward only
+ *                         products summed in tensor memory; for small FFNs),
+ *                         6 the tensor-core weight stream (up to 256 rows;
+ *                         the weights as the MMA's M side); 4 and 5
+ *                         apply to ffn_forward only; other values are refused
+ *                         (-1, option unchanged)
  *   TFFN_OPT_WAIT_LIMIT_MS  device wait limit in ms (default 4000)
  *   TFFN_OPT_SKIP_FLAG    test fault injection: the engine never publishes
  *                         the ready flag of this GEMM1 tile index (-1 = off);

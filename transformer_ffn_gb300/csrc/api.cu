@@ -13,6 +13,7 @@
 
 #include "../../include/tffn.h"
 #include "decode.cuh"
+#include "wstream.cuh"
 #include "engine.cuh"
 #include "launch.h"
 #include "reduce_params.cuh"
@@ -39,7 +40,8 @@ constexpr size_t SYNC_BYTES = size_t(5) << 20;
 static_assert(OFF_DCOUNT + DCOUNT_WORDS * 4 <= SYNC_BYTES, "sync region layout");
 constexpr uint32_t EPOCH_LIMIT = 0x7FFFFFF0u;      // launches before the flag region is cleared
 
-constexpr int64_t DECODE_MAX_M = 64;   // the weight stream wins up to here (measured against the engine)
+constexpr int64_t DECODE_MAX_M = 64;   // the mma.sync weight stream wins up to here (measured against the engine)
+constexpr int64_t STREAM_MAX_M = 128;  // then the tensor-core weight stream (measured against the engine)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -246,11 +248,11 @@ uint64_t wait_limit_ns()
 // ------------------------------------------------------------------ layouts
 struct DenseLayout {
     int path = 0;          // 1 engine fused, 2 decode, 3 engine two launches, 4 reduce-add form,
-                           // 5 back-to-back (H on chip)
+                           // 5 back-to-back (H on chip), 6 tensor-core weight stream
     int64_t m_blocks = 0;
     int32_t n1 = 0, n2 = 0;
     size_t off_h = 0;      // engine: H [m_blocks*BM x O]; decode: H [M x O]
-    size_t off_part = 0;   // decode: split-K partial sums
+    size_t off_part = 0;   // decode and tensor-core stream: split-K partial sums
     size_t total = 0;
 };
 
@@ -262,8 +264,10 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, int sms, bo
     DenseLayout L;
     int64_t path = g_opt_path.load();
     if (path == 0)
-        path = (M <= DECODE_MAX_M) ? 2 : 1;
+        path = (M <= DECODE_MAX_M) ? 2 : (M <= STREAM_MAX_M ? 6 : 1);
     if (path == 2 && M > decode::MAX_ROWS)
+        path = 1;
+    if (path == 6 && M > wstream::MAX_ROWS)
         path = 1;
     if ((path == 4 || path == 5) && glu)
         path = 1;
@@ -291,6 +295,12 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, int sms, bo
     }
     if (L.path == 2) {
         const decode::Plan pl = decode::make_plan(M, N, O, P, sms, glu);
+        L.off_part = align_up(L.off_h + static_cast<size_t>(M) * O * 2, 256);
+        L.total = L.off_part + pl.partial_bytes;
+        return L;
+    }
+    if (L.path == 6) {
+        const wstream::Plan pl = wstream::make_plan(M, N, O, P, sms, glu);
         L.off_part = align_up(L.off_h + static_cast<size_t>(M) * O * 2, 256);
         L.total = L.off_part + pl.partial_bytes;
         return L;
@@ -414,6 +424,49 @@ static int run_decode(DeviceState& d, uint8_t* base, const DenseLayout& L, const
     return TFFN_OK;
 }
 
+// The tensor-core weight stream (dense, or gated when W3 is given).
+static int run_wstream(DeviceState& d, uint8_t* base, const DenseLayout& L, const void* X, const void* W1,
+                       const void* W3, const void* b1, const void* W2, const void* b2, int act1, int act2,
+                       int64_t M, int64_t N, int64_t O, int64_t P, void* Y, cudaStream_t s)
+{
+    int rc = count_launch(d, base, s);
+    if (rc != TFFN_OK)
+        return rc;
+    const bool glu = W3 != nullptr;
+    wstream::Params p{};
+    p.b1 = static_cast<const __nv_bfloat16*>(b1);
+    p.b2 = static_cast<const __nv_bfloat16*>(b2);
+    p.Y = static_cast<__nv_bfloat16*>(Y);
+    p.H = reinterpret_cast<__nv_bfloat16*>(base + L.off_h);
+    p.partial = reinterpret_cast<float*>(base + L.off_part);
+    p.counters = reinterpret_cast<uint32_t*>(base + OFF_DCOUNT);
+    p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+    p.ctrl = reinterpret_cast<DevCtrl*>(base);
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.O = static_cast<int32_t>(O);
+    p.P = static_cast<int32_t>(P);
+    p.act1 = act1;
+    p.act2 = act2;
+    p.glu = glu ? 1 : 0;
+    p.wait_limit_ns = wait_limit_ns();
+    p.plan = wstream::make_plan(M, N, O, P, d.sms, glu);
+    if (static_cast<size_t>(p.plan.slices[0]) * wstream::EPI_WARPS > FLAG_WORDS ||
+        2 * (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * wstream::EPI_WARPS > DCOUNT_WORDS)
+        return TFFN_ERR_UNSUPPORTED;
+    const uint32_t rows = static_cast<uint32_t>(p.plan.rows);
+    if (make_map(&p.map_w[0], W1, O, N, 64, wstream::KC) || make_map(&p.map_w[1], W2, P, O, 64, wstream::KC) ||
+        make_map(&p.map_x[0], X, N, M, 64, rows) || make_map(&p.map_x[1], p.H, O, M, 64, rows) ||
+        (glu && make_map(&p.map_w3, W3, O, N, 64, wstream::KC)))
+        return TFFN_ERR_INVALID_ARG;
+    timing_start(s);
+    if (launch_wstream(p, s) != 0)
+        return TFFN_ERR_CUDA;
+    timing_stop(s);
+    g_last_launches = 1;
+    return TFFN_OK;
+}
+
 // Launch the dense engine as the layout says: one fused launch, or layer 1
 // and layer 2 as two launches.
 static int run_dense_engine(DeviceState& d, uint8_t* base, const DenseLayout& L, engine::Params<1>& p,
@@ -492,6 +545,8 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
 
     if (L.path == 2)
         return run_decode(*d, base, L, X, W1, nullptr, b1, W2, b2, act1, act2, M, N, O, P, Y, s);
+    if (L.path == 6)
+        return run_wstream(*d, base, L, X, W1, nullptr, b1, W2, b2, act1, act2, M, N, O, P, Y, s);
 
     if (L.path == 4 || L.path == 5) {
         reduce::Params rp;
@@ -587,6 +642,8 @@ int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W
         return rc;
     if (L.path == 2)
         return run_decode(*d, base, L, X, W1, W3, nullptr, W2, nullptr, act, TFFN_ACT_NONE, M, N, O, P, Y, s);
+    if (L.path == 6)
+        return run_wstream(*d, base, L, X, W1, W3, nullptr, W2, nullptr, act, TFFN_ACT_NONE, M, N, O, P, Y, s);
 
     engine::Params<1> p;
     std::memset(&p, 0, sizeof(p));
@@ -830,7 +887,7 @@ const char* tffn_status_string(int status)
 int64_t tffn_set_option(int option, int64_t value)
 {
     switch (option) {
-    case TFFN_OPT_PATH: return g_opt_path.exchange(value);
+    case TFFN_OPT_PATH: return (value < 0 || value > 6) ? -1 : g_opt_path.exchange(value);
     case TFFN_OPT_WAIT_LIMIT_MS: return g_opt_wait_ms.exchange(value);
     case TFFN_OPT_SKIP_FLAG: return g_opt_skip.exchange(value);
     case TFFN_OPT_GROUP_M: return g_opt_group.exchange(value);

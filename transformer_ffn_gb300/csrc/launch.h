@@ -17,6 +17,9 @@ struct Params;
 namespace reduce {
 struct Params;
 }
+namespace wstream {
+struct Params;
+}
 
 constexpr int MOE_MAX_E = 64;
 
@@ -25,6 +28,7 @@ constexpr int MOE_MAX_E = 64;
 int launch_engine_dense(const engine::Params<1>& p, int max_pairs, cudaStream_t s);
 int launch_engine_grouped(const engine::Params<MOE_MAX_E>& p, int max_pairs, cudaStream_t s);
 int launch_decode(const decode::Params& p, int grid, cudaStream_t s);
+int launch_wstream(const wstream::Params& p, cudaStream_t s);
 int launch_reduce(const reduce::Params& p, int max_pairs, cudaStream_t s);
 int launch_b2b(const reduce::Params& p, int max_pairs, cudaStream_t s);
 

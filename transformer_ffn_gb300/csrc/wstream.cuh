@@ -1,0 +1,170 @@
+// wstream.cuh -- the medium-batch weight stream: both FFN layers as one
+// persistent launch that reads every weight byte once, on the tcgen05 tensor
+// cores with the weights as the MMA's M side ("swap-AB").
+//
+// From 65 to 256 rows the FFN is still bound by the weight bytes (2 M FLOP per
+// weight byte pair: M below the ~287 FLOP/byte ridge of a GB300), but the
+// row-band engine has too few tiles to fill the GPU and mma.sync has too
+// little throughput to keep up with HBM.  Here a unit is KC = 64 rows of K for
+// one slice of 256 output columns: each 128-column half of W (MN-major) is
+// the A operand (M = 128) of one MMA, the K chunk of X or H (NB token rows,
+// K-major) the B operand (N = NB) of both, and the products accumulate in
+// tensor memory, one lane per output column and one column per token.  Units are
+// spread over the CTAs as contiguous ranges (Stream-K, equal weight bytes per
+// CTA).  A slice split across CTAs leaves fp32 partial sums in fixed places;
+// once the slice's arrival counter shows every part ("Kernel fusion and
+// tensor parallelism", section "Step 1": per-tile counters complete the
+// tile), each contributing CTA sums its share of the slice's rows over all
+// parts in part order, so the result does not depend on timing.
+// A finished layer-1 slice of H publishes ready flags; a layer-2 range waits
+// for the H slices it reads, with its first W2 stages already loaded.
+//
+// Gated layer 1 (H = act(X W1) * (X W3)): the unit's two tiles are the same
+// 128 columns of W1 and of W3, so the two accumulators hold the gate and the
+// linear product and one thread has both values of its column.
+//
+// CTA layout (192 threads): warp 0 issues the TMA copies; warp 1 allocates
+// tensor memory and one of its threads issues the MMAs; warps 2-5 drain the
+// accumulators (warp w reads tensor-memory lanes 32 (w % 4) .. + 31).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace tffn {
+namespace wstream {
+
+constexpr int SLICE = 128;              // output columns of one MMA (its M); a unit has two
+constexpr int KC = 64;                  // K rows per unit: one 128-byte swizzle row of B
+constexpr int W_BOX = 64 * KC * 2;      // 8 KiB: 64 columns x KC rows of W
+constexpr int EPI_WARPS = 4;
+constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
+constexpr int MAX_STAGES = 8;
+constexpr int MAX_ROWS = 256;           // rows (tokens) handled by this path
+
+// Geometry of the instance for at most NB token rows (NB a multiple of 32, up
+// to 256).  Every unit carries two 128-column W tiles (four boxes, 32 KiB):
+// the two halves of a 256-column output slice, or for the gated layer 1 the
+// same 128 columns of W1 and W3; with the NB x KC tile of X or H this is a
+// stage, and as many stages as fit 200 KiB are in flight (the weight bytes in
+// flight per SM set the streaming rate).  A run's accumulator is two NB-column
+// blocks of tensor memory; two of them (double buffering) up to NB = 128, one
+// at NB = 256.
+template <int NB>
+struct Geo {
+    static constexpr int W_BYTES = 4 * W_BOX;
+    static constexpr int X_BYTES = NB * KC * 2;
+    static constexpr int STAGE = W_BYTES + X_BYTES;
+    static constexpr int NST0 = (200 * 1024) / STAGE;
+    static constexpr int NST = NST0 > MAX_STAGES ? MAX_STAGES : NST0;
+    static constexpr int ACC_COLS = 2 * NB;
+    static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
+    static constexpr int TMEM_COLS = NBUF * ACC_COLS;
+    static constexpr int AUX = 1024;
+    static constexpr int SMEM = NST * STAGE + AUX + 1024;
+    static_assert(SMEM <= 232448, "shared memory");
+    static_assert(NB % 32 == 0 && NB <= 256, "token rows");
+    static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "tensor-memory allocation");
+    static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
+};
+
+// Token rows of the instance that serves M rows.
+inline int stream_rows(int64_t M)
+{
+    return M <= 128 ? 128 : 256;
+}
+
+struct Plan {
+    int32_t grid;
+    int32_t rows;           // NB of the instance
+    int32_t h_cols;         // hidden columns of a layer-1 slice: 256, or 128 gated
+    int32_t slices[2];      // output slices per layer (256 columns; gated layer 1: 128)
+    int32_t kch[2];         // K chunks (KC rows) per slice
+    int64_t units[2];       // slices * kch
+    int32_t maxp[2];        // most CTAs sharing one slice
+    int64_t part_off[2];    // float offset of each layer's partial sums
+    size_t partial_bytes;
+};
+
+// CTA that owns unit u when U units are spread over G CTAs (U >= G).
+__host__ __device__ inline int64_t owner_of(int64_t u, int64_t U, int64_t G)
+{
+    return ((u + 1) * G + U - 1) / U - 1;
+}
+
+__host__ __device__ inline int64_t range_start(int64_t c, int64_t U, int64_t G)
+{
+    return c * U / G;
+}
+
+// Floats of one part's partial sums: two halves x 128 columns x NB rows.
+__host__ __device__ inline int64_t part_floats(int rows)
+{
+    return static_cast<int64_t>(2) * SLICE * rows;
+}
+
+// grid is the CTA count the caller wants; it is lowered so that every CTA
+// owns at least one unit of each layer.
+inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool glu)
+{
+    Plan pl{};
+    pl.rows = stream_rows(M);
+    pl.h_cols = glu ? SLICE : 2 * SLICE;
+    pl.slices[0] = static_cast<int32_t>((O + pl.h_cols - 1) / pl.h_cols);
+    pl.kch[0] = static_cast<int32_t>((N + KC - 1) / KC);
+    pl.slices[1] = static_cast<int32_t>((P + 2 * SLICE - 1) / (2 * SLICE));
+    pl.kch[1] = static_cast<int32_t>((O + KC - 1) / KC);
+    int64_t g = grid;
+    for (int l = 0; l < 2; ++l) {
+        pl.units[l] = static_cast<int64_t>(pl.slices[l]) * pl.kch[l];
+        if (pl.units[l] < g)
+            g = pl.units[l];
+    }
+    if (g < 1)
+        g = 1;
+    pl.grid = static_cast<int32_t>(g);
+    int64_t off = 0;
+    for (int l = 0; l < 2; ++l) {
+        int32_t maxp = 1;
+        for (int64_t s = 0; s < pl.slices[l]; ++s) {
+            const int64_t a = owner_of(s * pl.kch[l], pl.units[l], g);
+            const int64_t b = owner_of((s + 1) * pl.kch[l] - 1, pl.units[l], g);
+            if (b - a + 1 > maxp)
+                maxp = static_cast<int32_t>(b - a + 1);
+        }
+        pl.maxp[l] = maxp;
+        pl.part_off[l] = off;
+        if (maxp > 1)
+            off += static_cast<int64_t>(pl.slices[l]) * maxp * part_floats(pl.rows);
+    }
+    pl.partial_bytes = static_cast<size_t>(off) * 4;
+    return pl;
+}
+
+struct Params {
+    CUtensorMap map_w[2];      // W1 {O, N}, W2 {P, O}; box {64, KC}
+    CUtensorMap map_w3;        // gated form: W3 {O, N}; box {64, KC}
+    CUtensorMap map_x[2];      // X {N, M}, H {O, M}; box {64, NB} (rows past M read as zeros)
+    const __nv_bfloat16* b1;
+    const __nv_bfloat16* b2;
+    __nv_bfloat16* Y;          // [M x P]
+    __nv_bfloat16* H;          // [M x O]
+    float* partial;
+    uint32_t* counters;        // arrival counters [slices0 * 4] then [slices1 * 4] (one per epilogue
+                               // warp), then the done counters in the same layout
+    uint32_t* flags;           // [slices0 * 4]: H slice ready, one word per epilogue warp (= epoch)
+    DevCtrl* ctrl;
+    int32_t M, N, O, P;
+    int32_t act1, act2;
+    int32_t glu;
+    uint64_t wait_limit_ns;
+    Plan plan;
+};
+
+}  // namespace wstream
+}  // namespace tffn
