@@ -325,18 +325,43 @@ __device__ __forceinline__ int64_t part_index(int a, int ch, int col)
     return ((static_cast<int64_t>(a) * (NB / CH) + ch) * (CH / 4) * SLICE + col) * 4;
 }
 
+// store_chunk with the activation chosen at run time, once per chunk: the
+// dense activations and SwiGLU's SiLU compiled in, the rarer gated forms
+// (GeGLU, ReGLU, bilinear) through the run-time activation.
+template <bool GATED>
+__device__ __forceinline__ void store_any(int act, __nv_bfloat16* out, int ncols, int M, int64_t gcol, float bias,
+                                          float (&v)[CH], const float (&lin)[CH], int t0, int lane)
+{
+    if constexpr (GATED) {
+        if (act == TFFN_ACT_SILU)
+            store_chunk<TFFN_ACT_SILU, true>(out, ncols, M, gcol, bias, v, lin, t0, lane, act);
+        else
+            store_chunk<ACT_RUNTIME, true>(out, ncols, M, gcol, bias, v, lin, t0, lane, act);
+    } else {
+        switch (act) {
+        case TFFN_ACT_RELU: store_chunk<TFFN_ACT_RELU, false>(out, ncols, M, gcol, bias, v, lin, t0, lane, act); break;
+        case TFFN_ACT_GELU_TANH:
+            store_chunk<TFFN_ACT_GELU_TANH, false>(out, ncols, M, gcol, bias, v, lin, t0, lane, act);
+            break;
+        case TFFN_ACT_SILU: store_chunk<TFFN_ACT_SILU, false>(out, ncols, M, gcol, bias, v, lin, t0, lane, act); break;
+        default: store_chunk<TFFN_ACT_NONE, false>(out, ncols, M, gcol, bias, v, lin, t0, lane, act); break;
+        }
+    }
+}
+
 // acc[4i .. 4i+3] = sum over parts pp = 0 .. nparts-1, in that order, of the
-// float4 at src + pp * pf + i * SLICE * 4; two parts' loads in flight.
+// float4 at src + pp * pf + i * SLICE * 4; F parts' loads in flight.
+template <int F>
 __device__ __forceinline__ void sum_parts(float (&acc)[CH], const float* src, int64_t pf, int nparts)
 {
 #pragma unroll
     for (int i = 0; i < CH; ++i)
         acc[i] = 0.0f;
 #pragma unroll 1
-    for (int pp = 0; pp < nparts; pp += 2) {
-        float4 x[2][CH / 4];
+    for (int pp = 0; pp < nparts; pp += F) {
+        float4 x[F][CH / 4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < F; ++j)
             if (pp + j < nparts) {
                 const float4* sj = reinterpret_cast<const float4*>(src + static_cast<int64_t>(pp + j) * pf);
 #pragma unroll
@@ -344,7 +369,7 @@ __device__ __forceinline__ void sum_parts(float (&acc)[CH], const float* src, in
                     x[j][i] = __ldcg(sj + i * SLICE);
             }
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < F; ++j)
             if (pp + j < nparts) {
 #pragma unroll
                 for (int i = 0; i < CH / 4; ++i) {
@@ -418,7 +443,7 @@ __device__ __forceinline__ void publish_h(const Params& p, const Aux& aux, int64
 // part's partial sums go to their fixed place and the slice's arrival counter
 // counts them.  Gated: the two halves are the gate and the linear product of
 // the same column.
-template <int NB, int ACT, bool GATED>
+template <int NB, bool GATED>
 __device__ void drain_run(const Params& p, Aux& aux, uint32_t tmem_base, int layer, int64_t slice, uint32_t buf, int q,
                           int lane)
 {
@@ -442,8 +467,8 @@ __device__ void drain_run(const Params& p, Aux& aux, uint32_t tmem_base, int lay
                 tmem_chunk(tb + a * NB + ch * CH, v);
                 if (GATED)
                     tmem_chunk(tb + NB + ch * CH, lin);
-                store_chunk<ACT, GATED>(out, ncols, p.M, c.gcol[a], c.bias[a], v, lin, ch * CH, lane,
-                                        layer == 0 ? p.act1 : p.act2);
+                store_any<GATED>(layer == 0 ? p.act1 : p.act2, out, ncols, p.M, c.gcol[a], c.bias[a], v, lin,
+                                 ch * CH, lane);
             }
         ptx::tc_fence_before();
         __syncwarp();
@@ -478,7 +503,7 @@ __device__ void drain_run(const Params& p, Aux& aux, uint32_t tmem_base, int lay
 // sums its share of the slice's chunks (chunk items part, part + nparts, ...)
 // over all parts in part order and writes them.  The CTA whose share finishes
 // last resets the slice's counters and, in layer 1, publishes the H slice.
-template <int NB, int ACT, bool GATED>
+template <int NB, bool GATED>
 __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int layer, int64_t slice, int q, int lane)
 {
     const Plan& pl = p.plan;
@@ -507,11 +532,12 @@ __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int la
 #pragma unroll 1
     for (int it = ri.part; it < items; it += ri.nparts) {
         const int a = it / NCH, ch = it % NCH;
-        sum_parts(v, base + part_index<NB>(a, ch, col), pf, ri.nparts);
+        // four parts in flight (two per accumulator when gated: the registers)
+        sum_parts<GATED ? 2 : 4>(v, base + part_index<NB>(a, ch, col), pf, ri.nparts);
         if (GATED)
-            sum_parts(lin, base + part_index<NB>(1, ch, col), pf, ri.nparts);
-        store_chunk<ACT, GATED>(out, ncols, p.M, c.gcol[a], c.bias[a], v, lin, ch * CH, lane,
-                                layer == 0 ? p.act1 : p.act2);
+            sum_parts<2>(lin, base + part_index<NB>(1, ch, col), pf, ri.nparts);
+        store_any<GATED>(layer == 0 ? p.act1 : p.act2, out, ncols, p.M, c.gcol[a], c.bias[a], v, lin, ch * CH,
+                         lane);
     }
     if (layer == 0)
         ptx::fence_proxy_async_global();
@@ -535,35 +561,24 @@ __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int la
 // The activation of a run, resolved once; the gated FFN's layer 2 has no bias
 // and no activation (ffn_glu_forward), so the gated instance only needs the
 // gated layer-1 variants and that one.
+// The gated FFN's layer 1 is the gated variant; its layer 2 (no bias, no
+// activation) and every dense layer the plain one.
 template <int NB, bool GLU, int PHASE>
 __device__ __forceinline__ bool run_phase(const Params& p, Aux& aux, const WaitCtx& w, uint32_t tmem_base, int layer,
                                           int64_t slice, uint32_t buf, int q, int lane)
 {
-#define TFFN_WS_CALL(ACT, GATED)                                                          \
-    do {                                                                                  \
-        if (PHASE == 1)                                                                   \
-            drain_run<NB, ACT, GATED>(p, aux, tmem_base, layer, slice, buf, q, lane);     \
-        else                                                                              \
-            return reduce_share<NB, ACT, GATED>(p, aux, w, layer, slice, q, lane);        \
-        return true;                                                                      \
-    } while (0)
-    if constexpr (GLU) {
-        if (layer == 1)
-            TFFN_WS_CALL(TFFN_ACT_NONE, false);
-        // SwiGLU compiled for its activation; GeGLU, ReGLU and the bilinear
-        // form share one variant that reads the activation at run time
-        if (p.act1 == TFFN_ACT_SILU)
-            TFFN_WS_CALL(TFFN_ACT_SILU, true);
-        TFFN_WS_CALL(ACT_RUNTIME, true);
-    } else {
-        switch (layer == 0 ? p.act1 : p.act2) {
-        case TFFN_ACT_RELU: TFFN_WS_CALL(TFFN_ACT_RELU, false);
-        case TFFN_ACT_GELU_TANH: TFFN_WS_CALL(TFFN_ACT_GELU_TANH, false);
-        case TFFN_ACT_SILU: TFFN_WS_CALL(TFFN_ACT_SILU, false);
-        default: TFFN_WS_CALL(TFFN_ACT_NONE, false);
-        }
+    if (GLU && layer == 0) {
+        if (PHASE == 1)
+            drain_run<NB, GLU>(p, aux, tmem_base, layer, slice, buf, q, lane);
+        else
+            return reduce_share<NB, GLU>(p, aux, w, layer, slice, q, lane);
+        return true;
     }
-#undef TFFN_WS_CALL
+    if (PHASE == 1)
+        drain_run<NB, false>(p, aux, tmem_base, layer, slice, buf, q, lane);
+    else
+        return reduce_share<NB, false>(p, aux, w, layer, slice, q, lane);
+    return true;
 }
 
 // Per layer: drain every run as its accumulator completes (phase 1), then sum
