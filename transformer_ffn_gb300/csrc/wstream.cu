@@ -529,8 +529,20 @@ __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int la
 #pragma unroll
     for (int i = 0; i < CH; ++i)
         lin[i] = 0.0f;
+    // This part's block of the slice's items: a CTA with two split slices in
+    // this layer has two shares to sum, so its blocks are half as long.
+    int64_t wsum = 0, wmine = 0;
+    const int64_t first_cta = static_cast<int64_t>(blockIdx.x) - ri.part;
+    for (int j = 0; j < ri.nparts; ++j) {
+        const int64_t wj = pl.split[layer][first_cta + j] > 1 ? 1 : 2;
+        if (j < ri.part)
+            wmine += wj;
+        wsum += wj;
+    }
+    const int it0 = static_cast<int>(items * wmine / wsum);
+    const int it1 = static_cast<int>(items * (wmine + (pl.split[layer][blockIdx.x] > 1 ? 1 : 2)) / wsum);
 #pragma unroll 1
-    for (int it = ri.part; it < items; it += ri.nparts) {
+    for (int it = it0; it < it1; ++it) {
         const int a = it / NCH, ch = it % NCH;
         // four parts in flight (two per accumulator when gated: the registers)
         sum_parts<GATED ? 2 : 4>(v, base + part_index<NB>(a, ch, col), pf, ri.nparts);

@@ -46,6 +46,7 @@ constexpr int EPI_WARPS = 4;
 constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_ROWS = 256;           // rows (tokens) handled by this path
+constexpr int MAX_GRID = 256;           // CTAs of one launch (one per SM)
 
 // Geometry of the instance for at most NB token rows (NB a multiple of 32, up
 // to 256).  Every unit carries two 128-column W tiles (four boxes, 32 KiB):
@@ -89,6 +90,7 @@ struct Plan {
     int32_t maxp[2];        // most CTAs sharing one slice
     int64_t part_off[2];    // float offset of each layer's partial sums
     size_t partial_bytes;
+    uint8_t split[2][MAX_GRID];   // per CTA: its split slices (shared with other CTAs) per layer
 };
 
 // CTA that owns unit u when U units are spread over G CTAs (U >= G).
@@ -119,7 +121,7 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool
     pl.kch[0] = static_cast<int32_t>((N + KC - 1) / KC);
     pl.slices[1] = static_cast<int32_t>((P + 2 * SLICE - 1) / (2 * SLICE));
     pl.kch[1] = static_cast<int32_t>((O + KC - 1) / KC);
-    int64_t g = grid;
+    int64_t g = grid < MAX_GRID ? grid : MAX_GRID;
     for (int l = 0; l < 2; ++l) {
         pl.units[l] = static_cast<int64_t>(pl.slices[l]) * pl.kch[l];
         if (pl.units[l] < g)
@@ -143,6 +145,16 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool
             off += static_cast<int64_t>(pl.slices[l]) * maxp * part_floats(pl.rows);
     }
     pl.partial_bytes = static_cast<size_t>(off) * 4;
+    for (int l = 0; l < 2; ++l) {
+        const int64_t U = pl.units[l], kch = pl.kch[l];
+        for (int64_t c = 0; c < g; ++c) {
+            const int64_t u0 = range_start(c, U, g), u1 = range_start(c + 1, U, g);
+            int n = 0;
+            for (int64_t sl = u0 / kch; sl <= (u1 - 1) / kch; ++sl)
+                n += owner_of(sl * kch, U, g) != owner_of((sl + 1) * kch - 1, U, g) ? 1 : 0;
+            pl.split[l][c] = static_cast<uint8_t>(n < 255 ? n : 255);
+        }
+    }
     return pl;
 }
 
