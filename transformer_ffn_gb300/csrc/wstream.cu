@@ -503,7 +503,7 @@ __device__ void drain_run(const Params& p, Aux& aux, uint32_t tmem_base, int lay
 // sums its share of the slice's chunks (chunk items part, part + nparts, ...)
 // over all parts in part order and writes them.  The CTA whose share finishes
 // last resets the slice's counters and, in layer 1, publishes the H slice.
-template <int NB, bool GATED>
+template <int NB, bool GATED, bool PIPE>
 __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int layer, int64_t slice, int q, int lane)
 {
     const Plan& pl = p.plan;
@@ -541,15 +541,68 @@ __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int la
     }
     const int it0 = static_cast<int>(items * wmine / wsum);
     const int it1 = static_cast<int>(items * (wmine + (pl.split[layer][blockIdx.x] > 1 ? 1 : 2)) / wsum);
+    const int act = layer == 0 ? p.act1 : p.act2;
+    if constexpr (GATED || !PIPE) {
+        // the gated instance (gate and linear sums, both kernels' layers) keeps
+        // the plain loop: the registers
 #pragma unroll 1
-    for (int it = it0; it < it1; ++it) {
-        const int a = it / NCH, ch = it % NCH;
-        // four parts in flight (two per accumulator when gated: the registers)
-        sum_parts<GATED ? 2 : 4>(v, base + part_index<NB>(a, ch, col), pf, ri.nparts);
-        if (GATED)
-            sum_parts<2>(lin, base + part_index<NB>(1, ch, col), pf, ri.nparts);
-        store_any<GATED>(layer == 0 ? p.act1 : p.act2, out, ncols, p.M, c.gcol[a], c.bias[a], v, lin, ch * CH,
-                         lane);
+        for (int it = it0; it < it1; ++it) {
+            const int a = GATED ? 0 : it / NCH, ch = it % NCH;
+            sum_parts<2>(v, base + part_index<NB>(a, ch, col), pf, ri.nparts);
+            if (GATED)
+                sum_parts<2>(lin, base + part_index<NB>(1, ch, col), pf, ri.nparts);
+            store_any<GATED>(act, out, ncols, p.M, c.gcol[a], c.bias[a], v, lin, ch * CH, lane);
+        }
+    } else {
+        // Items in a two-deep pipeline: the first four parts of item it + 1
+        // are loading while item it is summed and stored.
+        float4 xa[4][CH / 4], xb[4][CH / 4];
+        auto load4 = [&](float4 (&x)[4][CH / 4], int it, int pp0) {
+            const float* src = base + part_index<NB>(it / NCH, it % NCH, col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (pp0 + j < ri.nparts) {
+                    const float4* sj = reinterpret_cast<const float4*>(src + static_cast<int64_t>(pp0 + j) * pf);
+#pragma unroll
+                    for (int i = 0; i < CH / 4; ++i)
+                        x[j][i] = __ldcg(sj + i * SLICE);
+                }
+        };
+        auto add4 = [&](const float4 (&x)[4][CH / 4], int pp0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (pp0 + j < ri.nparts) {
+#pragma unroll
+                    for (int i = 0; i < CH / 4; ++i) {
+                        v[4 * i] += x[j][i].x;
+                        v[4 * i + 1] += x[j][i].y;
+                        v[4 * i + 2] += x[j][i].z;
+                        v[4 * i + 3] += x[j][i].w;
+                    }
+                }
+        };
+        auto item = [&](float4 (&cur)[4][CH / 4], float4 (&nxt)[4][CH / 4], int it) {
+            if (it + 1 < it1)
+                load4(nxt, it + 1, 0);
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+                v[i] = 0.0f;
+            add4(cur, 0);
+            for (int pp = 4; pp < ri.nparts; pp += 4) {   // parts past the first four (part order kept)
+                load4(cur, it, pp);
+                add4(cur, pp);
+            }
+            const int a = it / NCH;
+            store_any<false>(act, out, ncols, p.M, c.gcol[a], c.bias[a], v, lin, (it % NCH) * CH, lane);
+        };
+        if (it0 < it1)
+            load4(xa, it0, 0);
+#pragma unroll 1
+        for (int it = it0; it < it1; it += 2) {
+            item(xa, xb, it);
+            if (it + 1 < it1)
+                item(xb, xa, it + 1);
+        }
     }
     if (layer == 0)
         ptx::fence_proxy_async_global();
@@ -583,13 +636,13 @@ __device__ __forceinline__ bool run_phase(const Params& p, Aux& aux, const WaitC
         if (PHASE == 1)
             drain_run<NB, GLU>(p, aux, tmem_base, layer, slice, buf, q, lane);
         else
-            return reduce_share<NB, GLU>(p, aux, w, layer, slice, q, lane);
+            return reduce_share<NB, GLU, false>(p, aux, w, layer, slice, q, lane);
         return true;
     }
     if (PHASE == 1)
         drain_run<NB, false>(p, aux, tmem_base, layer, slice, buf, q, lane);
     else
-        return reduce_share<NB, false>(p, aux, w, layer, slice, q, lane);
+        return reduce_share<NB, false, !GLU>(p, aux, w, layer, slice, q, lane);
     return true;
 }
 
