@@ -74,7 +74,7 @@ SPEC_BF16_TFLOPS = 2250.0   # GB300 dense bf16 (NVIDIA's 2:4-sparse figures are 
 SPEC_HBM_GBS = 8000.0       # GB300 HBM3e
 
 # Dominant kernel of each workload (for the ncu traffic record).
-DECODE_MAX_M = 64   # rows up to which ffn_forward / ffn_glu_forward stream the weights with mma.sync
+DECODE_MAX_M = 32   # rows up to which ffn_forward / ffn_glu_forward stream the weights with mma.sync
 STREAM_MAX_M = 128  # ... and then with tcgen05 MMAs
 KERNEL = {"tiny": "decode_kernel", "prefill": "engine_kernel", "large": "engine_kernel",
           "swiglu": "engine_kernel", "swiglu_decode": "decode_kernel", "moe": "engine_kernel", "moe_swiglu": "engine_kernel", "moe_moderate": "engine_kernel", "moe_stress": "engine_kernel",

@@ -75,8 +75,8 @@ typedef enum {
  * Numerics: products accumulate in fp32; H is rounded to bf16 (round to
  * nearest even) after b1 and act1, as it is stored between the layers; Y is
  * rounded to bf16 after b2 and act2.
- * Paths: M <= 64 streams the weights with mma.sync (split-K, HBM-bound
- * decode shapes); 65 <= M <= 128 streams them with tcgen05 MMAs (the weights
+ * Paths: M <= 32 streams the weights with mma.sync (split-K, HBM-bound
+ * decode shapes); 33 <= M <= 128 streams them with tcgen05 MMAs (the weights
  * as the MMA's M side, still HBM-bound); larger M runs the persistent tcgen05
  * engine (GEMM1 tiles publish ready flags that GEMM2 tiles consume in the
  * same launch).
@@ -101,8 +101,8 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
  *
  * Numerics: products accumulate in fp32; H = act(X W1) * (X W3) is rounded to
  * bf16 (nearest even) where it is stored between the layers; Y is rounded to
- * bf16.  Paths: M <= 64 streams the weights with mma.sync (each layer-1 unit
- * loads the same 64 columns of W1 and W3); 65 <= M <= 128 streams them with
+ * bf16.  Paths: M <= 32 streams the weights with mma.sync (each layer-1 unit
+ * loads the same 64 columns of W1 and W3); 33 <= M <= 128 streams them with
  * tcgen05 MMAs (gate and linear products in two tensor-memory accumulators);
  * larger M runs the persistent tcgen05 engine, each layer-1 tile pairing 128
  * columns of W1 with the same 128 columns of W3 in one 256-column

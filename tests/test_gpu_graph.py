@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("shape,path", [((300, 256, 1024, 512), 1), ((16, 512, 1024, 256), 2),
-                                        ((520, 128, 768, 264), 1)])
+                                        ((520, 128, 768, 264), 1), ((100, 512, 2048, 512), 6)])
 def test_replayed_ffn_matches_eager(cuda_lib, shape, path):
     tffn = cuda_lib
     M, N, O, P = shape

@@ -54,6 +54,8 @@ def lib_path(cuda_lib):
     (3, 300, 256, 1152, 320),       # engine as two launches
     (4, 300, 256, 1152, 320),       # reduce-add form (fp32 Y accumulator)
     (5, 300, 256, 1152, 320),       # back-to-back form
+    (0, 100, 1024, 2048, 520),      # tensor-core weight stream (split-slice partial sums)
+    (6, 200, 512, 1152, 264),       # the same at 256 rows
 ])
 def test_dense_with_exact_caller_workspace(lib_path, path, M, N, O, P):
     lib_path.set_option(lib_path.OPT_PATH, path)
@@ -71,7 +73,7 @@ def test_dense_with_exact_caller_workspace(lib_path, path, M, N, O, P):
     _assert_close(Y.float().cpu().numpy(), want, f"path {path}")
 
 
-@pytest.mark.parametrize("M", [16, 300])
+@pytest.mark.parametrize("M", [16, 100, 300])
 def test_glu_with_exact_caller_workspace(lib_path, M):
     N, O, P = 1024, 2560, 512
     g = synth.glu_inputs(M, N, O, P, seed=M, device="cuda")

@@ -60,7 +60,10 @@ def _glu_oracle(g, act, rows=None):
     ((129, 256, 384, 136), ("gelu_tanh", "relu")),      # 256-row instance, one row past 128
     ((256, 1024, 2048, 512), ("relu", "none")),         # full 256 rows
     ((200, 64, 128, 64), ("none", "none")),             # one K chunk, one slice per layer
-    ((1, 256, 264, 72), ("gelu_tanh", "none")),         # a single row through the 128-row instance
+    ((1, 256, 264, 72), ("gelu_tanh", "none")),         # a single row through the 32-row instance
+    ((16, 512, 1024, 256), ("relu", "none")),           # decode-sized batch, 32-row instance
+    ((48, 136, 520, 264), ("gelu_tanh", "relu")),       # 64-row instance, ragged
+    ((32, 4096, 1024, 256), ("gelu_tanh", "none")),     # N > O at 32 rows
 ])
 def test_stream_dense_full(cuda_lib, shape, acts):
     M, N, O, P = shape
@@ -83,6 +86,8 @@ def test_stream_dense_no_bias(cuda_lib):
     (100, 2048, 256, 512, "silu"),       # N > O
     (65, 64, 128, 64, "relu"),           # ReGLU, one slice
     (200, 256, 640, 392, "silu"),        # 256-row instance (one accumulator buffer), ragged P
+    (16, 512, 1024, 256, "silu"),        # 32-row instance
+    (40, 136, 328, 200, "gelu_tanh"),    # 64-row instance, ragged
 ])
 def test_stream_glu_full(cuda_lib, M, N, O, P, act):
     g = synth.glu_inputs(M, N, O, P, seed=M + N, device="cuda")

@@ -40,8 +40,8 @@ constexpr size_t SYNC_BYTES = size_t(5) << 20;
 static_assert(OFF_DCOUNT + DCOUNT_WORDS * 4 <= SYNC_BYTES, "sync region layout");
 constexpr uint32_t EPOCH_LIMIT = 0x7FFFFFF0u;      // launches before the flag region is cleared
 
-constexpr int64_t DECODE_MAX_M = 64;   // the mma.sync weight stream wins up to here (measured against the engine)
-constexpr int64_t STREAM_MAX_M = 128;  // then the tensor-core weight stream (measured against the engine)
+constexpr int64_t DECODE_MAX_M = 32;   // the mma.sync weight stream wins up to here (measured)
+constexpr int64_t STREAM_MAX_M = 128;  // then the tensor-core weight stream, then the engine (measured)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

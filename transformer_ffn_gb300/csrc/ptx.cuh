@@ -194,6 +194,13 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v)
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Release-add without a result: one thread publishes what its warp (after a
+// __syncwarp) or CTA (after a barrier) wrote before it.
+__device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v)
 {
     uint32_t old;

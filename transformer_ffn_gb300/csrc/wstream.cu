@@ -431,11 +431,9 @@ __device__ __forceinline__ Cols cols_of(const Params& p, int layer, int64_t slic
 __device__ __forceinline__ void publish_h(const Params& p, const Aux& aux, int64_t slice, int q, int lane)
 {
     ptx::fence_proxy_async_global();
-    __syncwarp();
-    if (lane == 0) {
-        __threadfence();
+    __syncwarp();   // the warp's stores, then one release by lane 0
+    if (lane == 0)
         ptx::st_release_gpu(p.flags + slice * EPI_WARPS + q, aux.epoch);
-    }
 }
 
 // Phase 1 of a run (this thread: column col of each 128-column half, NB token
@@ -491,12 +489,12 @@ __device__ void drain_run(const Params& p, Aux& aux, uint32_t tmem_base, int lay
         }
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0)
+    if (lane == 0) {
         ptx::mbar_arrive(ptx::smem_u32(&aux.tmem_empty[buf]));
-    __threadfence();
-    __syncwarp();
-    if (lane == 0)
-        atomicAdd(arrive_counter(p, layer, slice, q), 1u);
+        // the warp's partial sums are published by this one release (the
+        // __syncwarp above orders them before it)
+        ptx::red_release_add_gpu(arrive_counter(p, layer, slice, q), 1u);
+    }
 }
 
 // Phase 2 of a split run: once every part of the slice has arrived, this CTA
@@ -517,7 +515,7 @@ __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int la
         ok = wait_flag(w, arrive, static_cast<uint32_t>(ri.nparts), SITE_SLICE_FLAG, static_cast<uint32_t>(slice));
     if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0)
         return false;
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    __syncwarp();   // lane 0's acquire covers the warp's reads of the parts
     const Cols c = cols_of<GATED>(p, layer, slice, col);
     const int ncols = layer == 0 ? p.O : p.P;
     __nv_bfloat16* out = layer == 0 ? p.H : p.Y;
@@ -606,13 +604,12 @@ __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int la
     }
     if (layer == 0)
         ptx::fence_proxy_async_global();
-    __threadfence();
     __syncwarp();
     if (lane == 0) {
         uint32_t* done = done_counter(p, layer, slice, q);
-        if (atomicAdd(done, 1u) == static_cast<uint32_t>(ri.nparts - 1)) {
+        // acquire-release: the last share also sees every other share's stores
+        if (ptx::atom_add_acq_rel_gpu(done, 1u) == static_cast<uint32_t>(ri.nparts - 1)) {
             // every share is written (and every CTA is past its wait)
-            __threadfence();
             *arrive = 0u;
             *done = 0u;
             if (layer == 0)
@@ -769,6 +766,10 @@ int launch_instance(const wstream::Params& p, cudaStream_t s)
 
 int launch_wstream(const wstream::Params& p, cudaStream_t s)
 {
+    if (p.plan.rows == 32)
+        return p.glu ? launch_instance<32, true>(p, s) : launch_instance<32, false>(p, s);
+    if (p.plan.rows == 64)
+        return p.glu ? launch_instance<64, true>(p, s) : launch_instance<64, false>(p, s);
     if (p.plan.rows == 128)
         return p.glu ? launch_instance<128, true>(p, s) : launch_instance<128, false>(p, s);
     if (p.plan.rows == 256)

@@ -77,7 +77,7 @@ struct Geo {
 // Token rows of the instance that serves M rows.
 inline int stream_rows(int64_t M)
 {
-    return M <= 128 ? 128 : 256;
+    return M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256));
 }
 
 struct Plan {
