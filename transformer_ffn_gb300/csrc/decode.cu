@@ -144,16 +144,17 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
                 if (r1 < M)
                     *reinterpret_cast<float2*>(mine + r1 * SLICE + col) = make_float2(acc.c[m][n][2], acc.c[m][n][3]);
             }
-        __threadfence();
+        // One acquire-release add by lane 0 after a __syncwarp publishes the
+        // warp's partial and, for the last part, acquires everyone else's.
         __syncwarp();
         uint32_t* cnt = p.counters + (layer == 0 ? 0 : pl.slices[0] * 4) + slice * 4 + cw;
         uint32_t old = 0;
         if (lane == 0)
-            old = atomicAdd(cnt, 1u);
+            old = ptx::atom_add_acq_rel_gpu(cnt, 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
         if (old != static_cast<uint32_t>(nparts - 1))
             return;
-        __threadfence();
+        __syncwarp();
         zero(acc);
         for (int pp = 0; pp < nparts; ++pp) {
             const float* src = base + static_cast<int64_t>(pp) * Geo<MT>::ROWS * SLICE;
@@ -200,11 +201,9 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
             }
         }
         ptx::fence_proxy_async_global();
-        __syncwarp();
-        if (lane == 0) {
-            __threadfence();
+        __syncwarp();   // the warp's stores, then one release by lane 0
+        if (lane == 0)
             ptx::st_release_gpu(p.flags + slice * CONSUMER_WARPS + cw, epoch);
-        }
         return;
     }
 
@@ -239,11 +238,9 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
         // Publish this warp's quarter of the H slice: stamp its flag word with
         // the call's epoch (release, gpu scope).
         ptx::fence_proxy_async_global();
-        __syncwarp();
-        if (lane == 0) {
-            __threadfence();
+        __syncwarp();   // the warp's stores, then one release by lane 0
+        if (lane == 0)
             ptx::st_release_gpu(p.flags + slice * CONSUMER_WARPS + cw, epoch);
-        }
     }
 }
 
