@@ -30,6 +30,7 @@ enum WaitSite : uint32_t {
     SITE_H_SMEM = 11,        // reduce-add form: MMA waiting for the H tile in shared memory
     SITE_H_FREE = 12,        // reduce-add form: epilogue waiting for the H tile's readers
     SITE_BIAS = 13,          // engine epilogue: the CTA's shared bias slice
+    SITE_PARTS = 14,         // weight streams: a slice's reducer waiting for its split-K parts
 };
 
 // Control block at the start of the workspace (256 bytes).

@@ -114,11 +114,61 @@ __device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uin
     }
 }
 
+// Adds parts [1, nparts) of this warp's columns, in part order, to acc (which
+// holds part 0); F parts' loads are in flight at a time.
+template <int MT, int F>
+__device__ __forceinline__ void add_parts(Acc<MT>& acc, const float* base, int nparts, int cw, int lane, int M)
+{
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll 1
+    for (int pp = 1; pp < nparts; pp += F) {
+        float2 v[F][MT][4][2];
+#pragma unroll
+        for (int j = 0; j < F; ++j) {
+            const float* src = base + static_cast<int64_t>(pp + j) * Geo<MT>::ROWS * SLICE;
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    const int col = cw * 32 + n * 8 + 2 * q;
+                    const int r0 = m * 16 + g, r1 = r0 + 8;
+                    const bool in = pp + j < nparts;
+                    v[j][m][n][0] = (in && r0 < M) ? __ldcg(reinterpret_cast<const float2*>(src + r0 * SLICE + col))
+                                                   : make_float2(0.f, 0.f);
+                    v[j][m][n][1] = (in && r1 < M) ? __ldcg(reinterpret_cast<const float2*>(src + r1 * SLICE + col))
+                                                   : make_float2(0.f, 0.f);
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < F; ++j) {
+            if (pp + j >= nparts)
+                break;
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    acc.c[m][n][0] += v[j][m][n][0].x;
+                    acc.c[m][n][1] += v[j][m][n][0].y;
+                    acc.c[m][n][2] += v[j][m][n][1].x;
+                    acc.c[m][n][3] += v[j][m][n][1].y;
+                }
+        }
+    }
+}
+
 // Finish this warp's 32 columns of one slice: direct epilogue when one CTA
-// owns the whole K range, else store the partial and let the last arriver sum
-// the parts in part order.
+// owns the whole K range.  A split slice's parts are its CTAs' runs in CTA
+// order; part 0 is the run that ends its CTA's range (the slice continues in
+// the next CTA), so it is normally finished last, and its CTA reduces: it
+// waits until the slice's counter shows the other nparts - 1 parts, adds them
+// in part order to its own registers, and writes the output.  Every other
+// part stores its partial and leaves the counter increment in `pending`: the
+// caller publishes it (one release by lane 0) after its next stage, when the
+// stores have drained, instead of stalling the warp on them now.
+// Returns false on abort or timeout.
 template <int MT>
-__device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, int cw, int lane, uint32_t epoch)
+__device__ bool flush(const Params& p, const WaitCtx& w, int layer, int64_t slice, Acc<MT>& acc, int cw, int lane,
+                      uint32_t epoch, uint32_t*& pending)
 {
     const Plan& pl = p.plan;
     const int64_t U = pl.units[layer], G = pl.grid, kch = pl.kch[layer];
@@ -130,54 +180,36 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
     const int M = p.M;
 
     if (nparts > 1) {
-        float* base = p.partial + pl.part_off[layer] +
-                      (static_cast<int64_t>(slice) * pl.maxp[layer]) * Geo<MT>::ROWS * SLICE;
-        float* mine = base + static_cast<int64_t>(part) * Geo<MT>::ROWS * SLICE;
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const int col = cw * 32 + n * 8 + 2 * q;
-                const int r0 = m * 16 + g, r1 = r0 + 8;
-                if (r0 < M)
-                    *reinterpret_cast<float2*>(mine + r0 * SLICE + col) = make_float2(acc.c[m][n][0], acc.c[m][n][1]);
-                if (r1 < M)
-                    *reinterpret_cast<float2*>(mine + r1 * SLICE + col) = make_float2(acc.c[m][n][2], acc.c[m][n][3]);
-            }
-        // One acquire-release add by lane 0 after a __syncwarp publishes the
-        // warp's partial and, for the last part, acquires everyone else's.
-        __syncwarp();
+        const float* base = p.partial + pl.part_off[layer] +
+                            (static_cast<int64_t>(slice) * pl.maxp[layer]) * Geo<MT>::ROWS * SLICE;
         uint32_t* cnt = p.counters + (layer == 0 ? 0 : pl.slices[0] * 4) + slice * 4 + cw;
-        uint32_t old = 0;
-        if (lane == 0)
-            old = ptx::atom_add_acq_rel_gpu(cnt, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old != static_cast<uint32_t>(nparts - 1))
-            return;
-        __syncwarp();
-        zero(acc);
-        for (int pp = 0; pp < nparts; ++pp) {
-            const float* src = base + static_cast<int64_t>(pp) * Geo<MT>::ROWS * SLICE;
+        if (part != 0) {
+            float* mine = const_cast<float*>(base) + static_cast<int64_t>(part) * Geo<MT>::ROWS * SLICE;
 #pragma unroll
             for (int m = 0; m < MT; ++m)
 #pragma unroll
                 for (int n = 0; n < 4; ++n) {
                     const int col = cw * 32 + n * 8 + 2 * q;
                     const int r0 = m * 16 + g, r1 = r0 + 8;
-                    if (r0 < M) {
-                        const float2 v = __ldcg(reinterpret_cast<const float2*>(src + r0 * SLICE + col));
-                        acc.c[m][n][0] += v.x;
-                        acc.c[m][n][1] += v.y;
-                    }
-                    if (r1 < M) {
-                        const float2 v = __ldcg(reinterpret_cast<const float2*>(src + r1 * SLICE + col));
-                        acc.c[m][n][2] += v.x;
-                        acc.c[m][n][3] += v.y;
-                    }
+                    if (r0 < M)
+                        *reinterpret_cast<float2*>(mine + r0 * SLICE + col) =
+                            make_float2(acc.c[m][n][0], acc.c[m][n][1]);
+                    if (r1 < M)
+                        *reinterpret_cast<float2*>(mine + r1 * SLICE + col) =
+                            make_float2(acc.c[m][n][2], acc.c[m][n][3]);
                 }
+            pending = cnt;
+            return true;
         }
+        bool ok = true;
         if (lane == 0)
-            *cnt = 0u;   // every part has arrived: ready for the next call
+            ok = wait_flag(w, cnt, static_cast<uint32_t>(nparts - 1), SITE_PARTS, static_cast<uint32_t>(slice));
+        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0)
+            return false;
+        __syncwarp();   // lane 0's acquire covers the warp's reads of the parts
+        add_parts<MT, (MT == 1 ? 4 : (MT == 2 ? 2 : 1))>(acc, base, nparts, cw, lane, M);
+        if (lane == 0)
+            *cnt = 0u;   // every other part has arrived: ready for the next call
     }
 
     if (layer == 0 && p.glu) {
@@ -204,7 +236,7 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
         __syncwarp();   // the warp's stores, then one release by lane 0
         if (lane == 0)
             ptx::st_release_gpu(p.flags + slice * CONSUMER_WARPS + cw, epoch);
-        return;
+        return true;
     }
 
     // Epilogue: bias, activation, bf16.
@@ -242,6 +274,7 @@ __device__ void flush(const Params& p, int layer, int64_t slice, Acc<MT>& acc, i
         if (lane == 0)
             ptx::st_release_gpu(p.flags + slice * CONSUMER_WARPS + cw, epoch);
     }
+    return true;
 }
 
 // Wait, with the whole warp, until every layer-1 slice of H read by the
@@ -447,6 +480,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
         uint32_t stage = 0, phase = 0;
         Acc<MT> acc;
         bool ok = true;
+        uint32_t* pending = nullptr;   // a stored part whose counter increment is still to be published
+        auto publish = [&]() {
+            if (pending != nullptr) {
+                __syncwarp();   // the warp's partial stores, then one release by lane 0
+                if (lane == 0)
+                    ptx::red_release_add_gpu(pending, 1u);
+                pending = nullptr;
+            }
+        };
         for (int layer = 0; layer < 2 && ok; ++layer) {
             const int64_t U = pl.units[layer], kch = pl.kch[layer];
             const int64_t u0 = range_start(c, U, G), u1 = range_start(c + 1, U, G);
@@ -454,8 +496,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
             for (int64_t u = u0; u < u1; ++u) {
                 const int64_t slice = u / kch;
                 if (slice != cur) {
-                    if (cur >= 0)
-                        flush<MT>(p, layer, cur, acc, cw, lane, aux.epoch);
+                    if (cur >= 0 && !flush<MT>(p, w, layer, cur, acc, cw, lane, aux.epoch, pending)) {
+                        ok = false;
+                        break;
+                    }
                     zero(acc);
                     cur = slice;
                 }
@@ -474,9 +518,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
                     stage = 0;
                     phase ^= 1u;
                 }
+                publish();   // a part flushed before this stage: its stores have had a stage to drain
             }
             if (ok && cur >= 0)
-                flush<MT>(p, layer, cur, acc, cw, lane, aux.epoch);
+                ok = flush<MT>(p, w, layer, cur, acc, cw, lane, aux.epoch, pending);
+            publish();
         }
     }
     __syncwarp();
