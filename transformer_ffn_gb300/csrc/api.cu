@@ -451,7 +451,9 @@ static int run_wstream(DeviceState& d, uint8_t* base, const DenseLayout& L, cons
     p.glu = glu ? 1 : 0;
     p.wait_limit_ns = wait_limit_ns();
     p.plan = wstream::make_plan(M, N, O, P, d.sms, glu);
-    if (static_cast<size_t>(p.plan.slices[0]) * wstream::EPI_WARPS > FLAG_WORDS ||
+    const size_t flag_words = p.plan.win ? static_cast<size_t>(p.plan.nblk) * 2
+                                         : static_cast<size_t>(p.plan.slices[0]) * wstream::EPI_WARPS;
+    if (flag_words > FLAG_WORDS ||
         2 * (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * wstream::EPI_WARPS > DCOUNT_WORDS)
         return TFFN_ERR_UNSUPPORTED;
     const uint32_t rows = static_cast<uint32_t>(p.plan.rows);

@@ -47,21 +47,24 @@ constexpr int NUM_THREADS = 32 * (1 + CONSUMER_WARPS);
 constexpr int W_BOX_BYTES = KC * 64 * 2;                 // 16 KiB: KC rows x 64 cols
 constexpr int W_STAGE_BYTES = 2 * W_BOX_BYTES;           // 32 KiB
 
-// Geometry of the kernel instance for MT tiles of 16 rows (MT 1 and 2 share
-// one layout; MT 4 covers up to 64 rows): the A (X or H) box slot holds ROWS
-// rows of 64 k; a stage is the W tile plus two A boxes; NST stages fill the
-// shared memory; KB k-steps of fragments are loaded before their MMAs (fewer
-// for more rows: registers).
+// Geometry of the kernel instance for MT tiles of 16 rows (up to 64 rows):
+// the A (X or H) box slot holds ROWS = 16 MT rows of 64 k; a stage is the W
+// tile plus two A boxes; NST stages are in flight (measured on the 16-row
+// instance: 4, 5 and the former 5 stages of 32-row slots stream alike at
+// ~6.35 TB/s, 6 stages are 2 % slower, so it keeps 4 and leaves the rest of
+// the shared memory to L1); KB k-steps of fragments are loaded before their
+// MMAs (fewer for more rows: registers).
 template <int MT>
 struct Geo {
-    static constexpr int ROWS = MT <= 2 ? 32 : 16 * MT;
+    static constexpr int ROWS = 16 * MT;
     static constexpr int A_BOX = ROWS * 64 * 2;
     static constexpr int STAGE = W_STAGE_BYTES + 2 * A_BOX;
-    static constexpr int NST = MT <= 2 ? 5 : 4;
+    static constexpr int NST = MT == 1 ? 4 : (MT == 2 ? 5 : 4);
     static constexpr int SMEM = NST * STAGE + 1024 + 1024;
     static constexpr int KB = MT <= 2 ? 4 : 2;
 };
-static_assert(Geo<4>::SMEM <= 232448 && Geo<1>::SMEM <= 232448, "shared memory");
+static_assert(Geo<4>::SMEM <= 232448 && Geo<2>::SMEM <= 232448 && Geo<1>::SMEM <= 232448, "shared memory");
+static_assert(Geo<1>::NST <= MAX_STAGES && Geo<2>::NST <= MAX_STAGES && Geo<4>::NST <= MAX_STAGES, "stages");
 
 // Rows of a partial-sum block for M rows (the kernel instance's ROWS).
 inline int decode_rows(int64_t M)

@@ -12,6 +12,8 @@ namespace wstream {
 struct Aux {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
+    uint64_t full1[MAX_STAGES];     // window layer 1: its own ring geometry
+    uint64_t empty1[MAX_STAGES];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
@@ -44,27 +46,43 @@ __device__ __forceinline__ bool run_last(const Range& r, int64_t u)
     return u + 1 == r.u1 || (u + 1) % r.kch == 0;
 }
 
+// Window layer 1: the 64-column hidden blocks [b0, b1) this CTA owns.
+struct Blocks {
+    int32_t b0, b1;
+};
+
+__device__ __forceinline__ Blocks blocks_of(const Plan& pl)
+{
+    const int64_t c = blockIdx.x, G = pl.grid, n = pl.nblk;
+    return Blocks{static_cast<int32_t>(c * n / G), static_cast<int32_t>((c + 1) * n / G)};
+}
+
 // Wait, with the whole warp, until every H slice read by the K chunks
 // [k0, k0 + count) (cyclic over kch) is ready: all four words equal the
 // epoch.  A K chunk of KC rows lies in H slice kc * KC / h_cols.
+// With the window layer 1 a K chunk is one 64-column block of H, whose two
+// words (its two epilogue warps) must equal the epoch.
 __device__ bool wait_h(const WaitCtx& w, const uint32_t* flags, uint32_t epoch, int64_t k0, int64_t count, int64_t kch,
-                       int64_t h_slices, int64_t h_cols, int lane)
+                       int64_t h_slices, int64_t h_cols, bool win, int lane)
 {
     const uint64_t t0 = ptx::globaltimer();
     for (;;) {
         bool mine = true;
         for (int64_t i = lane; i < count && mine; i += 32) {
-            const int64_t hs = ((k0 + i) % kch) * KC / h_cols;
+            const int64_t kc = (k0 + i) % kch;
+            const int64_t hs = win ? kc : kc * KC / h_cols;
             if (hs >= h_slices)
                 continue;
-            const uint32_t* f = flags + hs * EPI_WARPS;
+            const int nw = win ? 2 : EPI_WARPS;
+            const uint32_t* f = flags + hs * nw;
             uint32_t v[EPI_WARPS];
 #pragma unroll
             for (int q = 0; q < EPI_WARPS; ++q)
-                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v[q]) : "l"(f + q) : "memory");
+                if (q < nw)
+                    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v[q]) : "l"(f + q) : "memory");
 #pragma unroll
             for (int q = 0; q < EPI_WARPS; ++q)
-                mine = mine && (v[q] == epoch);
+                mine = mine && (q >= nw || v[q] == epoch);
         }
         if (__all_sync(0xffffffffu, mine))
             break;
@@ -133,7 +151,57 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
     };
 
     // ---- layer 1
-    if (lane == 0) {
+    if (lane == 0 && pl.win) {
+        // The window: every K chunk of this CTA's 128 hidden columns (W1, and
+        // W3 when gated) with the X chunk, in the layer-1 ring.
+        constexpr int N1 = GLU ? Gm::NST : Gm::NST1;
+        constexpr int S1 = GLU ? Gm::STAGE : Gm::STAGE1;
+        constexpr uint32_t bytes1 = static_cast<uint32_t>((GLU ? 4 : 2) * W_BOX + Gm::X_BYTES);
+        const Blocks bk = blocks_of(pl);
+        uint32_t st1 = 0, ph1 = 0;
+        int32_t last1[N1];
+        for (int s = 0; s < N1; ++s)
+            last1[s] = -1;
+        if (bk.b1 > bk.b0) {
+            const int32_t col0 = bk.b0 * 64;
+            for (int64_t kc = 0; kc < pl.kch[0]; ++kc) {
+                ok = wait_mbar(w, ptx::smem_u32(&aux.empty1[st1]), ph1 ^ 1u, SITE_SMEM_EMPTY);
+                if (!ok)
+                    break;
+                const uint32_t fb = ptx::smem_u32(&aux.full1[st1]);
+                const uint32_t sw = ptx::smem_u32(stages + st1 * S1);
+                const int32_t row = static_cast<int32_t>(kc * KC);
+                ptx::mbar_arrive_expect_tx(fb, bytes1);
+                ptx::tma_load_2d_hint(sw, &p.map_w[0], fb, col0, row, evict_first);
+                ptx::tma_load_2d_hint(sw + W_BOX, &p.map_w[0], fb, col0 + 64, row, evict_first);
+                if (GLU) {
+                    ptx::tma_load_2d_hint(sw + 2 * W_BOX, &p.map_w3, fb, col0, row, evict_first);
+                    ptx::tma_load_2d_hint(sw + 3 * W_BOX, &p.map_w3, fb, col0 + 64, row, evict_first);
+                }
+                ptx::tma_load_2d(sw + (GLU ? 4 : 2) * W_BOX, &p.map_x[0], fb, row, 0);
+                last1[st1] = static_cast<int32_t>(ph1);
+                if (++st1 == N1) {
+                    st1 = 0;
+                    ph1 ^= 1u;
+                }
+            }
+        }
+        // Layer 2's ring reuses this memory: every layer-1 stage consumed
+        // first (or, after a failure, at least landed).
+        for (int s = 0; s < N1; ++s) {
+            if (last1[s] < 0)
+                continue;
+            if (ok) {
+                ok = wait_mbar(w, ptx::smem_u32(&aux.empty1[s]), static_cast<uint32_t>(last1[s]), SITE_SMEM_EMPTY);
+            }
+            if (!ok) {
+                const uint64_t t0 = ptx::globaltimer();
+                while (!ptx::mbar_try_wait(ptx::smem_u32(&aux.full1[s]), static_cast<uint32_t>(last1[s])))
+                    if (ptx::globaltimer() - t0 > p.wait_limit_ns)
+                        break;
+            }
+        }
+    } else if (lane == 0) {
         const Range r = range_of(pl, 0);
         for (int64_t u = r.u0; u < r.u1; ++u) {
             ok = wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY);
@@ -170,7 +238,8 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
         if (npre_done >= 0) {
             const int64_t count = (r.u1 - r.u0) < r.kch ? (r.u1 - r.u0) : r.kch;
             const bool ready =
-                wait_h(w, p.flags, aux.epoch, r.u0 % r.kch, count, r.kch, pl.slices[0], pl.h_cols, lane);
+                wait_h(w, p.flags, aux.epoch, r.u0 % r.kch, count, r.kch, pl.win ? pl.nblk : pl.slices[0], pl.h_cols,
+                       pl.win != 0, lane);
             if (lane == 0) {
                 ptx::fence_proxy_async_global();
                 // the prefetched stages expect their H bytes: issue them even
@@ -223,6 +292,48 @@ __device__ void run_mma(const Params& p, Aux& aux, uint8_t* stages, const WaitCt
     uint32_t stage = 0, phase = 0, iter = 0;
     bool ok = true;
     for (int layer = 0; layer < 2 && ok; ++layer) {
+        if (layer == 0 && pl.win) {
+            // the window: one run over all K chunks, in the layer-1 ring
+            constexpr int N1 = GLU ? Gm::NST : Gm::NST1;
+            constexpr int S1 = GLU ? Gm::STAGE : Gm::STAGE1;
+            const Blocks bk = blocks_of(pl);
+            if (bk.b1 <= bk.b0)
+                continue;
+            const uint32_t buf = iter % Gm::NBUF;
+            ok = wait_mbar(w, ptx::smem_u32(&aux.tmem_empty[buf]), ((iter / Gm::NBUF) & 1u) ^ 1u, SITE_TMEM_EMPTY);
+            if (!ok)
+                break;
+            ptx::tc_fence_after();
+            const uint32_t d = tmem_base + buf * Gm::ACC_COLS;
+            uint32_t st1 = 0, ph1 = 0;
+            for (int64_t kc = 0; kc < pl.kch[0]; ++kc) {
+                ok = wait_mbar(w, ptx::smem_u32(&aux.full1[st1]), ph1, SITE_SMEM_FULL);
+                if (!ok)
+                    break;
+                ptx::tc_fence_after();
+                const uint32_t sw = ptx::smem_u32(stages + st1 * S1);
+                const uint64_t adesc = ptx::sdesc_sw128(sw, W_BOX, 1024);
+                const uint64_t adesc1 = ptx::sdesc_sw128(sw + 2 * W_BOX, W_BOX, 1024);
+                const uint64_t bdesc = ptx::sdesc_sw128(sw + (GLU ? 4 : 2) * W_BOX, 16, 1024);
+#pragma unroll
+                for (int k = 0; k < KC / 16; ++k) {
+                    const uint64_t bk16 = bdesc + static_cast<uint64_t>((k * 32) >> 4);
+                    const uint32_t acc = (kc == 0 && k == 0) ? 0u : 1u;
+                    ptx::umma_bf16(d, adesc + static_cast<uint64_t>((k * 2048) >> 4), bk16, idesc, acc);
+                    if (GLU)
+                        ptx::umma_bf16(d + NB, adesc1 + static_cast<uint64_t>((k * 2048) >> 4), bk16, idesc, acc);
+                }
+                ptx::umma_commit(ptx::smem_u32(&aux.empty1[st1]));
+                if (++st1 == N1) {
+                    st1 = 0;
+                    ph1 ^= 1u;
+                }
+            }
+            if (ok)
+                ptx::umma_commit(ptx::smem_u32(&aux.tmem_full[buf]));
+            ++iter;
+            continue;
+        }
         const Range r = range_of(pl, layer);
         for (int64_t u = r.u0; u < r.u1; ++u) {
             const bool first = run_first(r, u);
@@ -643,6 +754,44 @@ __device__ __forceinline__ bool run_phase(const Params& p, Aux& aux, const WaitC
     return true;
 }
 
+// Window layer 1: the CTA's 128-column tile of H over all of K.  Warp q
+// holds columns 32q .. 32q + 31 of the window, in block b0 + q / 2; the warps
+// of an owned block write it (act(v + bias), or act(gate) * linear) and
+// publish its ready word, the others only release the accumulator.
+template <int NB, bool GATED>
+__device__ void drain_window(const Params& p, Aux& aux, uint32_t tmem_base, Blocks bk, uint32_t buf, int q, int lane)
+{
+    using Gm = Geo<NB>;
+    const int32_t block = bk.b0 + q / 2;
+    const bool owned = block < bk.b1;
+    const int64_t gcol = static_cast<int64_t>(bk.b0) * 64 + q * 32 + lane;
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Gm::ACC_COLS;
+    if (owned) {
+        const float bias = (!GATED && p.b1 != nullptr && gcol < p.O) ? __bfloat162float(p.b1[gcol]) : 0.0f;
+        float v[CH], lin[CH];
+#pragma unroll
+        for (int i = 0; i < CH; ++i)
+            lin[i] = 0.0f;
+#pragma unroll 1
+        for (int ch = 0; ch < NB / CH; ++ch) {
+            tmem_chunk(tb + ch * CH, v);
+            if (GATED)
+                tmem_chunk(tb + NB + ch * CH, lin);
+            store_any<GATED>(p.act1, p.H, p.O, p.M, gcol, bias, v, lin, ch * CH, lane);
+        }
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0)
+        ptx::mbar_arrive(ptx::smem_u32(&aux.tmem_empty[buf]));
+    if (owned) {
+        ptx::fence_proxy_async_global();
+        __syncwarp();   // the warp's stores, then one release by lane 0
+        if (lane == 0)
+            ptx::st_release_gpu(p.flags + block * 2 + (q & 1), aux.epoch);
+    }
+}
+
 // Per layer: drain every run as its accumulator completes (phase 1), then sum
 // this CTA's shares of the split slices (phase 2).  A CTA stores all of its
 // parts before it waits on anyone else's, so the waits cannot form a chain.
@@ -653,6 +802,18 @@ __device__ void run_epilogue(const Params& p, Aux& aux, const WaitCtx& w, uint32
     const Plan& pl = p.plan;
     uint32_t iter = 0;
     for (int layer = 0; layer < 2; ++layer) {
+        if (layer == 0 && pl.win) {
+            const Blocks bk = blocks_of(pl);
+            if (bk.b1 <= bk.b0)
+                continue;
+            const uint32_t buf = iter % Geo<NB>::NBUF;
+            if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_full[buf]), (iter / Geo<NB>::NBUF) & 1u, SITE_TMEM_FULL))
+                return;
+            ptx::tc_fence_after();
+            drain_window<NB, GLU>(p, aux, tmem_base, bk, buf, q, lane);
+            ++iter;
+            continue;
+        }
         const Range r = range_of(pl, layer);
         for (int64_t u = r.u0; u < r.u1; ++u) {
             if (!run_last(r, u))
@@ -680,14 +841,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) wstream_kernel(const __grid_co
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Aux& aux = *reinterpret_cast<Aux*>(stages + Gm::NST * Gm::STAGE);
+    Aux& aux = *reinterpret_cast<Aux*>(stages + Gm::RING);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < Gm::NST; ++s) {
+        for (int s = 0; s < MAX_STAGES; ++s) {
             ptx::mbar_init(ptx::smem_u32(&aux.full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&aux.empty[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&aux.full1[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&aux.empty1[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&aux.tmem_full[b]), 1);

@@ -63,12 +63,19 @@ struct Geo {
     static constexpr int STAGE = W_BYTES + X_BYTES;
     static constexpr int NST0 = (200 * 1024) / STAGE;
     static constexpr int NST = NST0 > MAX_STAGES ? MAX_STAGES : NST0;
+    // Window layer 1 (see Plan::win): a dense stage is one 128-column tile
+    // and the X tile, in a ring of its own geometry over the same memory.
+    static constexpr int STAGE1 = 2 * W_BOX + X_BYTES;
+    static constexpr int NST1_0 = (200 * 1024) / STAGE1;
+    static constexpr int NST1 = NST1_0 > MAX_STAGES ? MAX_STAGES : NST1_0;
+    static constexpr int RING = NST * STAGE > NST1 * STAGE1 ? NST * STAGE : NST1 * STAGE1;
     static constexpr int ACC_COLS = 2 * NB;
     static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
     static constexpr int TMEM_COLS = NBUF * ACC_COLS;
     static constexpr int AUX = 1024;
-    static constexpr int SMEM = NST * STAGE + AUX + 1024;
+    static constexpr int SMEM = RING + AUX + 1024;
     static_assert(SMEM <= 232448, "shared memory");
+    static_assert(STAGE1 % 1024 == 0, "window stages stay 1024-byte aligned");
     static_assert(NB % 32 == 0 && NB <= 256, "token rows");
     static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "tensor-memory allocation");
     static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
@@ -83,6 +90,15 @@ inline int stream_rows(int64_t M)
 struct Plan {
     int32_t grid;
     int32_t rows;           // NB of the instance
+    // Window layer 1: CTA c owns the 64-column hidden blocks
+    // [c * nblk / grid, (c + 1) * nblk / grid) (one or two) and computes them
+    // over the whole of K as one 128-column tile (the second block of a
+    // one-block CTA is its neighbour's, computed and dropped): no split
+    // slices, so H is final when a CTA's stream ends.  Used up to 128 rows
+    // when every CTA owns at most two blocks; otherwise layer 1 is a
+    // Stream-K over 256-column slices like layer 2.
+    int32_t win;
+    int32_t nblk;           // 64-column hidden blocks (window layer 1)
     int32_t h_cols;         // hidden columns of a layer-1 slice: 256, or 128 gated
     int32_t slices[2];      // output slices per layer (256 columns; gated layer 1: 128)
     int32_t kch[2];         // K chunks (KC rows) per slice
@@ -122,16 +138,19 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool
     pl.slices[1] = static_cast<int32_t>((P + 2 * SLICE - 1) / (2 * SLICE));
     pl.kch[1] = static_cast<int32_t>((O + KC - 1) / KC);
     int64_t g = grid < MAX_GRID ? grid : MAX_GRID;
-    for (int l = 0; l < 2; ++l) {
+    for (int l = 0; l < 2; ++l)
         pl.units[l] = static_cast<int64_t>(pl.slices[l]) * pl.kch[l];
-        if (pl.units[l] < g)
-            g = pl.units[l];
-    }
+    if (pl.units[1] < g)
+        g = pl.units[1];
     if (g < 1)
         g = 1;
+    pl.nblk = static_cast<int32_t>((O + 63) / 64);
+    pl.win = (pl.rows <= 128 && pl.nblk <= 2 * g) ? 1 : 0;
+    if (!pl.win && pl.units[0] < g)
+        g = pl.units[0];
     pl.grid = static_cast<int32_t>(g);
     int64_t off = 0;
-    for (int l = 0; l < 2; ++l) {
+    for (int l = pl.win ? 1 : 0; l < 2; ++l) {
         int32_t maxp = 1;
         for (int64_t s = 0; s < pl.slices[l]; ++s) {
             const int64_t a = owner_of(s * pl.kch[l], pl.units[l], g);
@@ -145,7 +164,7 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool
             off += static_cast<int64_t>(pl.slices[l]) * maxp * part_floats(pl.rows);
     }
     pl.partial_bytes = static_cast<size_t>(off) * 4;
-    for (int l = 0; l < 2; ++l) {
+    for (int l = pl.win ? 1 : 0; l < 2; ++l) {
         const int64_t U = pl.units[l], kch = pl.kch[l];
         for (int64_t c = 0; c < g; ++c) {
             const int64_t u0 = range_start(c, U, g), u1 = range_start(c + 1, U, g);
@@ -169,7 +188,8 @@ struct Params {
     float* partial;
     uint32_t* counters;        // arrival counters [slices0 * 4] then [slices1 * 4] (one per epilogue
                                // warp), then the done counters in the same layout
-    uint32_t* flags;           // [slices0 * 4]: H slice ready, one word per epilogue warp (= epoch)
+    uint32_t* flags;           // H ready (= epoch): [slices0 * 4], one word per slice and epilogue warp;
+                               // window layer 1: [nblk * 2], one per 64-column block and warp
     DevCtrl* ctrl;
     int32_t M, N, O, P;
     int32_t act1, act2;
