@@ -17,6 +17,7 @@ struct Aux {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
+    uint64_t xfer[EPI_WARPS];       // per epilogue warp: bulk loads of layer-2 parts
     uint32_t tmem_base;
     uint32_t abort;
     uint32_t epoch;     // this launch's ready-flag value (control block's + 1)
@@ -429,16 +430,6 @@ __device__ __forceinline__ void tmem_chunk(uint32_t taddr, float (&v)[CH])
         v[i] = __uint_as_float(r[i]);
 }
 
-// Partial sums of one part, in an order where each store instruction of a
-// warp covers 512 contiguous bytes: float4 i (i < CH / 4) of chunk ch (CH
-// rows) of half a for column col sits at float offset
-// (((a * NB / CH + ch) * CH / 4 + i) * SLICE + col) * 4.
-template <int NB>
-__device__ __forceinline__ int64_t part_index(int a, int ch, int col)
-{
-    return ((static_cast<int64_t>(a) * (NB / CH) + ch) * (CH / 4) * SLICE + col) * 4;
-}
-
 // store_chunk with the activation chosen at run time, once per chunk: the
 // dense activations and SwiGLU's SiLU compiled in, the rarer gated forms
 // (GeGLU, ReGLU, bilinear) through the run-time activation.
@@ -464,7 +455,8 @@ __device__ __forceinline__ void store_any(int act, __nv_bfloat16* out, int ncols
 }
 
 // acc[4i .. 4i+3] = sum over parts pp = 0 .. nparts-1, in that order, of the
-// float4 at src + pp * pf + i * SLICE * 4; F parts' loads in flight.
+// float4 at src + pp * pf + i * 32 * 4 (src: this lane's float4 of its
+// segment); F parts' loads in flight.
 template <int F>
 __device__ __forceinline__ void sum_parts(float (&acc)[CH], const float* src, int64_t pf, int nparts)
 {
@@ -480,7 +472,7 @@ __device__ __forceinline__ void sum_parts(float (&acc)[CH], const float* src, in
                 const float4* sj = reinterpret_cast<const float4*>(src + static_cast<int64_t>(pp + j) * pf);
 #pragma unroll
                 for (int i = 0; i < CH / 4; ++i)
-                    x[j][i] = __ldcg(sj + i * SLICE);
+                    x[j][i] = __ldcg(sj + i * 32);
             }
 #pragma unroll
         for (int j = 0; j < F; ++j)
@@ -596,10 +588,10 @@ __device__ void drain_run(const Params& p, Aux& aux, uint32_t tmem_base, int lay
 #pragma unroll 1
         for (int ch = 0; ch < NB / CH; ++ch) {
             tmem_chunk(tb + a * NB + ch * CH, v);
-            float4* dst = reinterpret_cast<float4*>(mine + part_index<NB>(a, ch, col));
+            float4* dst = reinterpret_cast<float4*>(mine + seg_off<NB>(q, a, ch)) + lane;
 #pragma unroll
             for (int i = 0; i < CH / 4; ++i)
-                dst[i * SLICE] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                dst[i * 32] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
     ptx::tc_fence_before();
     __syncwarp();
@@ -615,8 +607,19 @@ __device__ void drain_run(const Params& p, Aux& aux, uint32_t tmem_base, int lay
 // sums its share of the slice's chunks (chunk items part, part + nparts, ...)
 // over all parts in part order and writes them.  The CTA whose share finishes
 // last resets the slice's counters and, in layer 1, publishes the H slice.
+// Wait for a warp's bulk loads after a failed wait (abort elsewhere): the
+// copies still land in this CTA's shared memory, so it may not leave first.
+__device__ void settle_xfer(const Params& p, uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (ptx::globaltimer() - t0 > p.wait_limit_ns)
+            break;
+}
+
 template <int NB, bool GATED, bool PIPE>
-__device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int layer, int64_t slice, int q, int lane)
+__device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, uint8_t* ring, uint32_t& xphase, int layer,
+                             int64_t slice, int q, int lane)
 {
     const Plan& pl = p.plan;
     const int col = q * 32 + lane;
@@ -654,15 +657,80 @@ __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int la
     const int it0 = static_cast<int>(items * wmine / wsum);
     const int it1 = static_cast<int>(items * (wmine + (pl.split[layer][blockIdx.x] > 1 ? 1 : 2)) / wsum);
     const int act = layer == 0 ? p.act1 : p.act2;
-    if constexpr (GATED || !PIPE) {
+    if (!GATED && !PIPE && layer == 1) {
+        // Layer 2 ends the kernel: the ring is idle, and each warp fetches its
+        // segments of the parts with bulk copies into its quarter of it, as
+        // many items (all their parts) at a time as fit, then sums from there.
+        // (Used by the gated instance, whose registers leave no room for the
+        // two-deep register pipeline below; for the dense instance that
+        // pipeline measured faster.)
+        constexpr int NCHK = NB / CH;
+        const int nparts = ri.nparts;
+        uint8_t* reg = ring + q * Geo<NB>::WREG;
+        const uint32_t bar = ptx::smem_u32(&aux.xfer[q]);
+        const int pcap = Geo<NB>::WSEGS;
+        const int ipb = nparts <= pcap ? pcap / nparts : 1;
+        if (lane == 0)
+            ptx::fence_proxy_async_global();   // the acquired parts, before the copies read them
+#pragma unroll 1
+        for (int ib = it0; ib < it1; ib += ipb) {
+            const int n = (it1 - ib) < ipb ? (it1 - ib) : ipb;
+#pragma unroll 1
+            for (int p0 = 0; p0 < nparts; p0 += pcap) {   // several rounds only when one item's parts do not fit
+                const int p1 = (nparts - p0) < pcap ? nparts : p0 + pcap;
+                const int np = p1 - p0;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * np) * 2048u);
+                    for (int j = 0; j < n; ++j)
+                        for (int pp = p0; pp < p1; ++pp)
+                            ptx::bulk_load(ptx::smem_u32(reg + (j * np + (pp - p0)) * 2048),
+                                           base + static_cast<int64_t>(pp) * pf +
+                                               seg_off<NB>(q, (ib + j) / NCHK, (ib + j) % NCHK),
+                                           2048u, bar);
+                }
+                if (!wait_mbar(w, bar, xphase, SITE_PARTS)) {
+                    if (lane == 0)
+                        settle_xfer(p, bar, xphase);
+                    __syncwarp();
+                    return false;
+                }
+                xphase ^= 1u;
+#pragma unroll 1
+                for (int j = 0; j < n; ++j) {
+                    const int it = ib + j;
+                    if (p0 == 0) {
+#pragma unroll
+                        for (int i = 0; i < CH; ++i)
+                            v[i] = 0.0f;
+                    }
+#pragma unroll 1
+                    for (int pp = 0; pp < np; ++pp) {
+                        const float4* sv = reinterpret_cast<const float4*>(reg + (j * np + pp) * 2048) + lane;
+#pragma unroll
+                        for (int i = 0; i < CH / 4; ++i) {
+                            const float4 x = sv[i * 32];
+                            v[4 * i] += x.x;
+                            v[4 * i + 1] += x.y;
+                            v[4 * i + 2] += x.z;
+                            v[4 * i + 3] += x.w;
+                        }
+                    }
+                    if (p1 == nparts)
+                        store_any<false>(act, out, ncols, p.M, c.gcol[it / NCHK], c.bias[it / NCHK], v, lin,
+                                         (it % NCHK) * CH, lane);
+                }
+                __syncwarp();   // every lane has read the region before lane 0 refills it
+            }
+        }
+    } else if constexpr (GATED || !PIPE) {
         // the gated instance (gate and linear sums, both kernels' layers) keeps
         // the plain loop: the registers
 #pragma unroll 1
         for (int it = it0; it < it1; ++it) {
             const int a = GATED ? 0 : it / NCH, ch = it % NCH;
-            sum_parts<2>(v, base + part_index<NB>(a, ch, col), pf, ri.nparts);
+            sum_parts<2>(v, base + seg_off<NB>(q, a, ch) + lane * 4, pf, ri.nparts);
             if (GATED)
-                sum_parts<2>(lin, base + part_index<NB>(1, ch, col), pf, ri.nparts);
+                sum_parts<2>(lin, base + seg_off<NB>(q, 1, ch) + lane * 4, pf, ri.nparts);
             store_any<GATED>(act, out, ncols, p.M, c.gcol[a], c.bias[a], v, lin, ch * CH, lane);
         }
     } else {
@@ -670,14 +738,14 @@ __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int la
         // are loading while item it is summed and stored.
         float4 xa[4][CH / 4], xb[4][CH / 4];
         auto load4 = [&](float4 (&x)[4][CH / 4], int it, int pp0) {
-            const float* src = base + part_index<NB>(it / NCH, it % NCH, col);
+            const float* src = base + seg_off<NB>(q, it / NCH, it % NCH) + lane * 4;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 if (pp0 + j < ri.nparts) {
                     const float4* sj = reinterpret_cast<const float4*>(src + static_cast<int64_t>(pp0 + j) * pf);
 #pragma unroll
                     for (int i = 0; i < CH / 4; ++i)
-                        x[j][i] = __ldcg(sj + i * SLICE);
+                        x[j][i] = __ldcg(sj + i * 32);
                 }
         };
         auto add4 = [&](const float4 (&x)[4][CH / 4], int pp0) {
@@ -740,20 +808,20 @@ __device__ bool reduce_share(const Params& p, Aux& aux, const WaitCtx& w, int la
 // The gated FFN's layer 1 is the gated variant; its layer 2 (no bias, no
 // activation) and every dense layer the plain one.
 template <int NB, bool GLU, int PHASE>
-__device__ __forceinline__ bool run_phase(const Params& p, Aux& aux, const WaitCtx& w, uint32_t tmem_base, int layer,
-                                          int64_t slice, uint32_t buf, int q, int lane)
+__device__ __forceinline__ bool run_phase(const Params& p, Aux& aux, const WaitCtx& w, uint8_t* ring, uint32_t& xphase,
+                                          uint32_t tmem_base, int layer, int64_t slice, uint32_t buf, int q, int lane)
 {
     if (GLU && layer == 0) {
         if (PHASE == 1)
             drain_run<NB, GLU>(p, aux, tmem_base, layer, slice, buf, q, lane);
         else
-            return reduce_share<NB, GLU, false>(p, aux, w, layer, slice, q, lane);
+            return reduce_share<NB, GLU, false>(p, aux, w, ring, xphase, layer, slice, q, lane);
         return true;
     }
     if (PHASE == 1)
         drain_run<NB, false>(p, aux, tmem_base, layer, slice, buf, q, lane);
     else
-        return reduce_share<NB, false, !GLU>(p, aux, w, layer, slice, q, lane);
+        return reduce_share<NB, false, !GLU>(p, aux, w, ring, xphase, layer, slice, q, lane);
     return true;
 }
 
@@ -799,11 +867,12 @@ __device__ void drain_window(const Params& p, Aux& aux, uint32_t tmem_base, Bloc
 // this CTA's shares of the split slices (phase 2).  A CTA stores all of its
 // parts before it waits on anyone else's, so the waits cannot form a chain.
 template <int NB, bool GLU>
-__device__ void run_epilogue(const Params& p, Aux& aux, const WaitCtx& w, uint32_t tmem_base, int warp, int lane)
+__device__ void run_epilogue(const Params& p, Aux& aux, const WaitCtx& w, uint8_t* ring, uint32_t tmem_base, int warp,
+                             int lane)
 {
     const int q = warp & 3;   // tensor-memory lanes 32q .. 32q + 31
     const Plan& pl = p.plan;
-    uint32_t iter = 0;
+    uint32_t iter = 0, xphase = 0;
     for (int layer = 0; layer < 2; ++layer) {
         if (layer == 0 && pl.win) {
             const Blocks bk = blocks_of(pl);
@@ -825,13 +894,13 @@ __device__ void run_epilogue(const Params& p, Aux& aux, const WaitCtx& w, uint32
             if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_full[buf]), (iter / Geo<NB>::NBUF) & 1u, SITE_TMEM_FULL))
                 return;
             ptx::tc_fence_after();
-            run_phase<NB, GLU, 1>(p, aux, w, tmem_base, layer, u / r.kch, buf, q, lane);
+            run_phase<NB, GLU, 1>(p, aux, w, ring, xphase, tmem_base, layer, u / r.kch, buf, q, lane);
             ++iter;
         }
         for (int64_t u = r.u0; u < r.u1; ++u) {
             if (!run_last(r, u))
                 continue;
-            if (!run_phase<NB, GLU, 2>(p, aux, w, tmem_base, layer, u / r.kch, 0, q, lane))
+            if (!run_phase<NB, GLU, 2>(p, aux, w, ring, xphase, tmem_base, layer, u / r.kch, 0, q, lane))
                 return;
         }
     }
@@ -860,6 +929,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) wstream_kernel(const __grid_co
             ptx::mbar_init(ptx::smem_u32(&aux.tmem_empty[b]), EPI_WARPS);
         }
         ptx::mbar_init(ptx::smem_u32(&aux.drain), 1);
+        for (int q = 0; q < EPI_WARPS; ++q)
+            ptx::mbar_init(ptx::smem_u32(&aux.xfer[q]), 1);
         aux.abort = 0u;
         // device-side epoch: every CTA reads it before any can finish
         aux.epoch = *reinterpret_cast<volatile uint32_t*>(&p.ctrl->epoch) + 1u;
@@ -889,7 +960,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) wstream_kernel(const __grid_co
         if (lane == 0)
             run_mma<NB, GLU>(p, aux, stages, w, tmem_base);
     } else {
-        run_epilogue<NB, GLU>(p, aux, w, tmem_base, warp, lane);
+        run_epilogue<NB, GLU>(p, aux, w, stages, tmem_base, warp, lane);
     }
     __syncwarp();
     ptx::tc_fence_before();

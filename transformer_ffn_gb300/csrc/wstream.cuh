@@ -74,6 +74,10 @@ struct Geo {
     static constexpr int TMEM_COLS = NBUF * ACC_COLS;
     static constexpr int AUX = 1024;
     static constexpr int SMEM = RING + AUX + 1024;
+    // At the end of layer 2 the ring is idle; each epilogue warp then loads
+    // the parts it sums into its quarter of it (whole 2 KiB segments).
+    static constexpr int WREG = (RING / EPI_WARPS) & ~2047;
+    static constexpr int WSEGS = WREG / 2048;
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(STAGE1 % 1024 == 0, "window stages stay 1024-byte aligned");
     static_assert(NB % 32 == 0 && NB <= 256, "token rows");
@@ -124,6 +128,20 @@ __host__ __device__ inline int64_t range_start(int64_t c, int64_t U, int64_t G)
 __host__ __device__ inline int64_t part_floats(int rows)
 {
     return static_cast<int64_t>(2) * SLICE * rows;
+}
+
+// Layout of one part, by epilogue warp: warp q's 32 columns of half a, rows
+// [16 ch, 16 ch + 16), form one 2 KiB segment at float offset seg_off(q, a,
+// ch); in it, float4 i of lane l (rows 4i .. 4i+3 of column 32 q + l) sits
+// at float (i * 32 + l) * 4.  A warp's data of one item is contiguous, so a
+// warp can fetch it with one bulk copy; a warp store instruction covers 512
+// contiguous bytes.
+constexpr int SEG_FLOATS = 512;
+
+template <int NB>
+__host__ __device__ inline int64_t seg_off(int q, int a, int ch)
+{
+    return ((static_cast<int64_t>(q) * 2 + a) * (NB / 16) + ch) * SEG_FLOATS;
 }
 
 // grid is the CTA count the caller wants; it is lowered so that every CTA
