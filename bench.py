@@ -107,7 +107,8 @@ def dominant_kernel(config, ffn_path="auto"):
         return "engine_kernel"
     cfg = CONFIGS[config]
     if cfg["kind"] in ("ffn", "glu"):
-        # the library's own choice: the weight stream up to 64 rows, the engine above
+        # the library's own choice (for the workloads defined here): the mma.sync
+        # stream up to 32 rows, the tensor-core stream to 128, the engine above
         if cfg["M"] <= DECODE_MAX_M:
             return "decode_kernel"
         return "wstream_kernel" if cfg["M"] <= STREAM_MAX_M else "engine_kernel"

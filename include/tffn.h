@@ -77,9 +77,10 @@ typedef enum {
  * rounded to bf16 after b2 and act2.
  * Paths: M <= 32 streams the weights with mma.sync (split-K, HBM-bound
  * decode shapes); 33 <= M <= 128 streams them with tcgen05 MMAs (the weights
- * as the MMA's M side, still HBM-bound); larger M runs the persistent tcgen05
- * engine (GEMM1 tiles publish ready flags that GEMM2 tiles consume in the
- * same launch).
+ * as the MMA's M side, still HBM-bound), and so do 129 <= M <= 256 when every
+ * CTA's share of the hidden width fits one 128-column window (O up to 128
+ * times the SM count); larger M runs the persistent tcgen05 engine (GEMM1
+ * tiles publish ready flags that GEMM2 tiles consume in the same launch).
  */
 int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, const void* b2,
                 int act1, int act2, int64_t M, int64_t N, int64_t O, int64_t P, void* Y,
@@ -102,9 +103,10 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
  * Numerics: products accumulate in fp32; H = act(X W1) * (X W3) is rounded to
  * bf16 (nearest even) where it is stored between the layers; Y is rounded to
  * bf16.  Paths: M <= 32 streams the weights with mma.sync (each layer-1 unit
- * loads the same 64 columns of W1 and W3); 33 <= M <= 128 streams them with
- * tcgen05 MMAs (gate and linear products in two tensor-memory accumulators);
- * larger M runs the persistent tcgen05 engine, each layer-1 tile pairing 128
+ * loads the same 64 columns of W1 and W3); 33 <= M <= 128 (up to 256 under
+ * the same window condition as ffn_forward) streams them with tcgen05 MMAs
+ * (gate and linear products in two tensor-memory accumulators); larger M
+ * runs the persistent tcgen05 engine, each layer-1 tile pairing 128
  * columns of W1 with the same 128 columns of W3 in one 256-column
  * accumulator.  Errors and workspace as ffn_forward.
  */

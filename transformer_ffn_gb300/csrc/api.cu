@@ -41,7 +41,8 @@ static_assert(OFF_DCOUNT + DCOUNT_WORDS * 4 <= SYNC_BYTES, "sync region layout")
 constexpr uint32_t EPOCH_LIMIT = 0x7FFFFFF0u;      // launches before the flag region is cleared
 
 constexpr int64_t DECODE_MAX_M = 32;   // the mma.sync weight stream wins up to here (measured)
-constexpr int64_t STREAM_MAX_M = 128;  // then the tensor-core weight stream, then the engine (measured)
+constexpr int64_t STREAM_MAX_M = 128;  // then the tensor-core weight stream, then the engine (measured);
+                                       // up to 256 rows while its window layer 1 applies
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -263,8 +264,16 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, int sms, bo
 {
     DenseLayout L;
     int64_t path = g_opt_path.load();
-    if (path == 0)
-        path = (M <= DECODE_MAX_M) ? 2 : (M <= STREAM_MAX_M ? 6 : 1);
+    if (path == 0) {
+        if (M <= DECODE_MAX_M)
+            path = 2;
+        else if (M <= STREAM_MAX_M)
+            path = 6;
+        else if (M <= wstream::MAX_ROWS && wstream::make_plan(M, N, O, P, sms, glu).win)
+            path = 6;   // on the Llama 3 8B shape at 256 rows: 87 us against 125 us on the engine
+        else
+            path = 1;
+    }
     if (path == 2 && M > decode::MAX_ROWS)
         path = 1;
     if (path == 6 && M > wstream::MAX_ROWS)
