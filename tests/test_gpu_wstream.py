@@ -1,8 +1,9 @@
 """Parity of the tensor-core weight stream (TFFN_OPT_PATH = 6: up to 256 rows;
 the weights as the MMA's M side) with the CPU oracle, through the
 C ABI: |y - y_ref| <= 1e-2 + 1e-2 |y_ref| elementwise.  Small shapes in full
-(several slices, split-K parts and ragged tails), the Llama 3 8B shapes on
-sampled rows."""
+(several slices, split-K parts and ragged tails; layer 1 as per-CTA windows
+and, for hidden widths past two blocks per CTA, as split slices), the Llama 3
+8B shapes on sampled rows."""
 import numpy as np
 import pytest
 import torch
@@ -70,6 +71,40 @@ def test_stream_dense_full(cuda_lib, shape, acts):
     inp = synth.ffn_inputs(M, N, O, P, seed=31 + sum(shape), device="cuda")
     Y = _dense(cuda_lib, inp, *acts)
     _assert_close(Y.float().cpu().numpy(), _dense_oracle(inp, *acts), f"stream {shape}")
+
+
+@pytest.mark.parametrize("shape,glu", [
+    ((64, 512, 20480, 512), False),     # 320 hidden blocks > 2 per CTA: Stream-K layer 1, not windows
+    ((100, 256, 20480, 264), True),     # the same for the gated form, ragged P
+])
+def test_stream_wide_hidden_uses_split_layer1(cuda_lib, shape, glu):
+    M, N, O, P = shape
+    if glu:
+        g = synth.glu_inputs(M, N, O, P, seed=M + 3, device="cuda")
+        Y = _glu(cuda_lib, g, "silu")
+        _assert_close(Y.float().cpu().numpy(), _glu_oracle(g, "silu"), f"wide hidden glu {shape}")
+    else:
+        inp = synth.ffn_inputs(M, N, O, P, seed=M + 5, device="cuda")
+        Y = _dense(cuda_lib, inp, "gelu_tanh", "none")
+        _assert_close(Y.float().cpu().numpy(), _dense_oracle(inp, "gelu_tanh", "none"), f"wide hidden {shape}")
+
+
+@pytest.mark.parametrize("M,glu", [(200, False), (160, True)])
+def test_stream_is_the_default_to_256_rows(cuda_lib, M, glu):
+    # 129-256 rows take the stream automatically while its window layer 1
+    # applies; the result matches the oracle and the forced stream bit for bit
+    N, O, P = 512, 2048, 512
+    if glu:
+        g = synth.glu_inputs(M, N, O, P, seed=9, device="cuda")
+        auto = _glu(cuda_lib, g, "silu", path=0)
+        forced = _glu(cuda_lib, g, "silu")
+        _assert_close(auto.float().cpu().numpy(), _glu_oracle(g, "silu"), "auto glu")
+    else:
+        inp = synth.ffn_inputs(M, N, O, P, seed=9, device="cuda")
+        auto = _dense(cuda_lib, inp, "gelu_tanh", "none", path=0)
+        forced = _dense(cuda_lib, inp, "gelu_tanh", "none")
+        _assert_close(auto.float().cpu().numpy(), _dense_oracle(inp, "gelu_tanh", "none"), "auto dense")
+    assert torch.equal(auto, forced)
 
 
 def test_stream_dense_no_bias(cuda_lib):

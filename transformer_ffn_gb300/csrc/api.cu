@@ -420,10 +420,14 @@ static int run_decode(DeviceState& d, uint8_t* base, const DenseLayout& L, const
     // weight row would be fetched twice.
     const CUtensorMapL2promotion w1_promo =
         glu ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
-    if (make_map(&p.map_w[0], W1, O, N, 64, decode::KC, w1_promo) ||
+    // the gated window reads 128 adjacent columns of W1 and of W3 per row
+    // (two boxes each): 256-byte promotion, boxes of KC1 rows
+    const uint32_t w1_rows = p.plan.win ? static_cast<uint32_t>(decode::KC1) : static_cast<uint32_t>(decode::KC);
+    const CUtensorMapL2promotion w1p = p.plan.win ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : w1_promo;
+    if (make_map(&p.map_w[0], W1, O, N, 64, w1_rows, w1p) ||
         make_map(&p.map_w[1], W2, P, O, 64, decode::KC) || make_map(&p.map_a[0], X, N, M, 64, arows) ||
         make_map(&p.map_a[1], p.H, O, M, 64, arows) ||
-        (glu && make_map(&p.map_w3, W3, O, N, 64, decode::KC, w1_promo)))
+        (glu && make_map(&p.map_w3, W3, O, N, 64, w1_rows, w1p)))
         return TFFN_ERR_INVALID_ARG;
     timing_start(s);
     if (launch_decode(p, p.plan.grid, s) != 0)

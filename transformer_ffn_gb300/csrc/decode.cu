@@ -114,6 +114,99 @@ __device__ __forceinline__ void compute_stage(Acc<MT>& acc, uint32_t w_base, uin
     }
 }
 
+// Gated window layer 1: accumulators of this warp's 32 hidden columns, n8
+// tiles 0-3 the gate (X W1) and 4-7 the linear product (X W3) of the same
+// columns.
+template <int MT>
+struct AccW {
+    float c[MT][8][4];
+};
+
+// One KC1-deep stage of the window: W1 boxes 0-1 (128 columns) then W3 boxes
+// 2-3, each KC1 rows x 64 columns, 128-byte swizzled; warp cw takes columns
+// [32cw, 32cw + 32) of W1 and of W3.
+template <int MT>
+__device__ __forceinline__ void compute_stage_win(AccW<MT>& acc, uint32_t w_base, uint32_t a_base, int cw, int lane)
+{
+    constexpr uint32_t BOX = KC1 * 128;
+    const uint32_t g_box = w_base + static_cast<uint32_t>(cw >> 1) * BOX;
+    const uint32_t l_box = g_box + 2 * BOX;
+    const uint32_t cb = static_cast<uint32_t>(cw & 1) * 4;
+    const uint32_t j = static_cast<uint32_t>(lane >> 3);
+    const uint32_t r = static_cast<uint32_t>(lane & 7);
+    constexpr int KB = Geo<MT>::KB;
+#pragma unroll
+    for (int kb0 = 0; kb0 < KC1 / 16; kb0 += KB) {
+        uint32_t a[KB][MT][4];
+        uint32_t b[KB][4][4];   // gate cols 0-15, gate 16-31, linear 0-15, linear 16-31
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk) {
+            const int ks = kb0 + kk;
+            const uint32_t kchunk = static_cast<uint32_t>((ks & 3) * 2) + (j >> 1);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const uint32_t row = static_cast<uint32_t>(m * 16) + (j & 1u) * 8u + r;
+                ldsm_x4(a_base + sw128(row, kchunk), a[kk][m][0], a[kk][m][1], a[kk][m][2], a[kk][m][3]);
+            }
+            const uint32_t krow = static_cast<uint32_t>(ks * 16) + (j & 1u) * 8u + r;
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const uint32_t nchunk = cb + static_cast<uint32_t>(pr * 2) + (j >> 1);
+                ldsm_x4_t(g_box + sw128(krow, nchunk), b[kk][pr][0], b[kk][pr][1], b[kk][pr][2], b[kk][pr][3]);
+                ldsm_x4_t(l_box + sw128(krow, nchunk), b[kk][2 + pr][0], b[kk][2 + pr][1], b[kk][2 + pr][2],
+                          b[kk][2 + pr][3]);
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk)
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    mma_bf16_16816(acc.c[m][t * 2 + 0], a[kk][m][0], a[kk][m][1], a[kk][m][2], a[kk][m][3],
+                                   b[kk][t][0], b[kk][t][1]);
+                    mma_bf16_16816(acc.c[m][t * 2 + 1], a[kk][m][0], a[kk][m][1], a[kk][m][2], a[kk][m][3],
+                                   b[kk][t][2], b[kk][t][3]);
+                }
+    }
+}
+
+// The window's H: warp cw's 32 columns lie in block b0 + cw / 2; when the CTA
+// owns that block the warp writes act(gate) * linear (bf16) and stamps the
+// block's word for its half.
+template <int MT>
+__device__ void flush_win(const Params& p, int32_t b0, int32_t b1, const AccW<MT>& acc, int cw, int lane,
+                          uint32_t epoch)
+{
+    const int32_t block = b0 + (cw >> 1);
+    if (block >= b1)
+        return;
+    const int g = lane >> 2, q = lane & 3;
+    const int M = p.M;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+        const int col = b0 * 64 + cw * 32 + n * 8 + 2 * q;
+        if (col >= p.O)
+            continue;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const int r0 = m * 16 + g, r1 = r0 + 8;
+            if (r0 < M)
+                *reinterpret_cast<uint32_t*>(p.H + static_cast<int64_t>(r0) * p.O + col) =
+                    pack_bf16x2(act_apply(p.act1, acc.c[m][n][0]) * acc.c[m][n + 4][0],
+                                act_apply(p.act1, acc.c[m][n][1]) * acc.c[m][n + 4][1]);
+            if (r1 < M)
+                *reinterpret_cast<uint32_t*>(p.H + static_cast<int64_t>(r1) * p.O + col) =
+                    pack_bf16x2(act_apply(p.act1, acc.c[m][n][2]) * acc.c[m][n + 4][2],
+                                act_apply(p.act1, acc.c[m][n][3]) * acc.c[m][n + 4][3]);
+        }
+    }
+    ptx::fence_proxy_async_global();
+    __syncwarp();   // the warp's stores, then one release by lane 0
+    if (lane == 0)
+        ptx::st_release_gpu(p.flags + block * 2 + (cw & 1), epoch);
+}
+
 // Adds parts [1, nparts) of this warp's columns, in part order, to acc (which
 // holds part 0); F parts' loads are in flight at a time.
 template <int MT, int F>
@@ -283,8 +376,9 @@ __device__ bool flush(const Params& p, const WaitCtx& w, int layer, int64_t slic
 // the lanes, then an acquire fence in every lane: one pass over many flags
 // instead of one serialised acquire per unit.
 __device__ bool wait_h_window(const WaitCtx& w, const uint32_t* flags, uint32_t epoch, int64_t k0, int64_t count,
-                              int64_t kch, int h_per_k, int64_t h_slices, int lane)
+                              int64_t kch, int h_per_k, int64_t h_slices, bool win, int lane)
 {
+    const int nw = win ? 2 : CONSUMER_WARPS;   // ready words per slice (window: per block)
     const uint64_t t0 = ptx::globaltimer();
     for (;;) {
         bool mine = true;
@@ -292,14 +386,14 @@ __device__ bool wait_h_window(const WaitCtx& w, const uint32_t* flags, uint32_t 
             const int64_t hs = ((k0 + i / h_per_k) % kch) * h_per_k + i % h_per_k;
             if (hs >= h_slices)
                 continue;   // past the last hidden column: nothing to wait for
-            const uint32_t* f = flags + hs * CONSUMER_WARPS;
-            uint32_t v[CONSUMER_WARPS];
+            const uint32_t* f = flags + hs * nw;
 #pragma unroll
             for (int q = 0; q < CONSUMER_WARPS; ++q)
-                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v[q]) : "l"(f + q) : "memory");
-#pragma unroll
-            for (int q = 0; q < CONSUMER_WARPS; ++q)
-                mine = mine && (v[q] == epoch);
+                if (q < nw) {
+                    uint32_t v;
+                    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f + q) : "memory");
+                    mine = mine && (v == epoch);
+                }
         }
         if (__all_sync(0xffffffffu, mine))
             break;
@@ -368,7 +462,32 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
     };
 
     // ---- layer 1
-    if (lane == 0) {
+    if (lane == 0 && pl.win) {
+        // gated window: W1 and W3 boxes of the CTA's 128 hidden columns and
+        // one A box per KC1-row chunk
+        constexpr uint32_t BOX = KC1 * 128;
+        constexpr uint32_t A1_BYTES = (16u * MT) * 64u * 2u;
+        const int32_t b0 = static_cast<int32_t>(c * pl.nblk / G), b1 = static_cast<int32_t>((c + 1) * pl.nblk / G);
+        if (b1 > b0) {
+            const int32_t col0 = b0 * 64;
+            for (int64_t kc = 0; kc < pl.kch[0]; ++kc) {
+                ok = wait_mbar(w, ptx::smem_u32(&aux.empty[stage]), phase ^ 1u, SITE_SMEM_EMPTY);
+                if (!ok)
+                    break;
+                const uint32_t fb = ptx::smem_u32(&aux.full[stage]);
+                const uint32_t sw = ptx::smem_u32(stages + stage * STAGE_BYTES);
+                const int32_t row = static_cast<int32_t>(kc * KC1);
+                ptx::mbar_arrive_expect_tx(fb, 4 * BOX + A1_BYTES);
+                ptx::tma_load_2d(sw, &p.map_w[0], fb, col0, row);
+                ptx::tma_load_2d(sw + BOX, &p.map_w[0], fb, col0 + 64, row);
+                ptx::tma_load_2d(sw + 2 * BOX, &p.map_w3, fb, col0, row);
+                ptx::tma_load_2d(sw + 3 * BOX, &p.map_w3, fb, col0 + 64, row);
+                ptx::tma_load_2d(sw + W_STAGE_BYTES, &p.map_a[0], fb, row, 0);
+                last_phase[stage] = static_cast<int32_t>(phase);
+                advance();
+            }
+        }
+    } else if (lane == 0) {
         const int64_t U = pl.units[0], kch = pl.kch[0];
         const int64_t u0 = range_start(c, U, G), u1 = range_start(c + 1, U, G);
         for (int64_t u = u0; u < u1; ++u) {
@@ -407,7 +526,7 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
         if (npre_done >= 0) {
             const int64_t count = (u1 - u0) < kch ? (u1 - u0) : kch;
             const bool ready = wait_h_window(w, p.flags, aux.epoch, u0 % kch, count, kch, pl.h_per_k, pl.slices[0],
-                                             lane);
+                                             pl.win != 0, lane);
             if (lane == 0) {
                 ptx::fence_proxy_async_global();
                 // the prefetched stages expect their H bytes: issue them even
@@ -490,6 +609,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) decode_kernel(const __grid_con
             }
         };
         for (int layer = 0; layer < 2 && ok; ++layer) {
+            if constexpr (MT <= 2) {
+                if (layer == 0 && pl.win) {
+                    const int32_t b0 = static_cast<int32_t>(c * pl.nblk / G);
+                    const int32_t b1 = static_cast<int32_t>((c + 1) * pl.nblk / G);
+                    if (b1 <= b0)
+                        continue;
+                    AccW<MT> aw;
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+#pragma unroll
+                        for (int n = 0; n < 8; ++n)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                aw.c[m][n][i] = 0.0f;
+                    for (int64_t kc = 0; kc < pl.kch[0]; ++kc) {
+                        ok = wait_mbar(w, ptx::smem_u32(&aux.full[stage]), phase, SITE_STAGE);
+                        if (!ok)
+                            break;
+                        const uint32_t sw = ptx::smem_u32(stages + stage * STAGE_BYTES);
+                        compute_stage_win<MT>(aw, sw, sw + W_STAGE_BYTES, cw, lane);
+                        __syncwarp();
+                        if (lane == 0)
+                            ptx::mbar_arrive(ptx::smem_u32(&aux.empty[stage]));
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (ok)
+                        flush_win<MT>(p, b0, b1, aw, cw, lane, aux.epoch);
+                    continue;
+                }
+            }
             const int64_t U = pl.units[layer], kch = pl.kch[layer];
             const int64_t u0 = range_start(c, U, G), u1 = range_start(c + 1, U, G);
             int64_t cur = -1;

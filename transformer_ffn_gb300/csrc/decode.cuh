@@ -44,6 +44,7 @@ constexpr int MAX_ROWS = 64;            // rows handled by this path
 constexpr int MAX_STAGES = 5;
 constexpr int CONSUMER_WARPS = 4;       // 32 columns each
 constexpr int NUM_THREADS = 32 * (1 + CONSUMER_WARPS);
+constexpr int KC1 = 64;                 // K rows per stage of the gated window layer 1
 constexpr int W_BOX_BYTES = KC * 64 * 2;                 // 16 KiB: KC rows x 64 cols
 constexpr int W_STAGE_BYTES = 2 * W_BOX_BYTES;           // 32 KiB
 
@@ -74,6 +75,14 @@ inline int decode_rows(int64_t M)
 
 struct Plan {
     int32_t grid;
+    // Gated window layer 1 (up to 32 rows): CTA c owns the 64-column hidden
+    // blocks [c * nblk / grid, (c + 1) * nblk / grid) (one or two) and
+    // computes the 128 columns of W1 and of W3 from its first block over all
+    // of K in 64-row chunks (the second block of a one-block CTA is its
+    // neighbour's, computed and dropped): no split slices in layer 1, H final
+    // when the CTA's stream ends, one ready word per block and owning warp.
+    int32_t win;
+    int32_t nblk;
     int32_t h_per_k;        // layer-1 slices of H per layer-2 K chunk (1; 2 for the gated form)
     int32_t slices[2];      // output slices per layer
     int32_t kch[2];         // K chunks per slice
@@ -107,16 +116,27 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool
     pl.slices[1] = static_cast<int32_t>((P + SLICE - 1) / SLICE);
     pl.kch[1] = static_cast<int32_t>((O + KC - 1) / KC);
     int64_t g = grid;
-    for (int l = 0; l < 2; ++l) {
+    for (int l = 0; l < 2; ++l)
         pl.units[l] = static_cast<int64_t>(pl.slices[l]) * pl.kch[l];
-        if (pl.units[l] < g)
-            g = pl.units[l];
-    }
+    if (pl.units[1] < g)
+        g = pl.units[1];
     if (g < 1)
         g = 1;
+    pl.nblk = static_cast<int32_t>((O + 63) / 64);
+    pl.win = (glu && M <= 32 && pl.nblk <= 2 * g) ? 1 : 0;
+    if (pl.win) {
+        pl.kch[0] = static_cast<int32_t>((N + KC1 - 1) / KC1);   // window chunks of KC1 rows
+    } else if (pl.units[0] < g) {
+        g = pl.units[0];
+    }
     pl.grid = static_cast<int32_t>(g);
     size_t off = 0;
     for (int l = 0; l < 2; ++l) {
+        if (l == 0 && pl.win) {
+            pl.maxp[0] = 1;
+            pl.part_off[0] = 0;
+            continue;
+        }
         int32_t maxp = 1;
         for (int64_t s = 0; s < pl.slices[l]; ++s) {
             const int64_t a = owner_of(s * pl.kch[l], pl.units[l], g);
@@ -133,9 +153,9 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool
 }
 
 struct Params {
-    CUtensorMap map_w[2];      // W1 {O, N}, W2 {P, O}; box {64, KC}
+    CUtensorMap map_w[2];      // W1 {O, N}, W2 {P, O}; box {64, KC} (gated window: W1 box {64, KC1})
     CUtensorMap map_a[2];      // X {N, M}, H {O, M}; box {64, 16 * m_tiles}
-    CUtensorMap map_w3;        // gated form: W3 {O, N}; box {64, KC}
+    CUtensorMap map_w3;        // gated form: W3 {O, N}; box {64, KC} (window: {64, KC1})
     const __nv_bfloat16* X;
     const __nv_bfloat16* W1;
     const __nv_bfloat16* b1;
@@ -146,6 +166,7 @@ struct Params {
     float* partial;
     uint32_t* counters;        // [slices0 * 4] then [slices1 * 4]
     uint32_t* flags;           // [slices0 * 4]: one word per consumer warp, = epoch when ready
+                               // (gated window: [nblk * 2], one per block and owning warp)
     DevCtrl* ctrl;
     int32_t M, N, O, P;
     int32_t act1, act2;
