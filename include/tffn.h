@@ -79,7 +79,8 @@ typedef enum {
  * decode shapes); 33 <= M <= 128 streams them with tcgen05 MMAs (the weights
  * as the MMA's M side, still HBM-bound), and so do 129 <= M <= 256 when every
  * CTA's share of the hidden width fits one 128-column window (O up to 128
- * times the SM count); larger M runs the persistent tcgen05 engine (GEMM1
+ * times the SM count, two 64-column blocks per CTA); larger M runs the
+ * persistent tcgen05 engine (GEMM1
  * tiles publish ready flags that GEMM2 tiles consume in the same launch).
  */
 int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, const void* b2,

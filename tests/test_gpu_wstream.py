@@ -74,10 +74,11 @@ def test_stream_dense_full(cuda_lib, shape, acts):
 
 
 @pytest.mark.parametrize("shape,glu", [
-    ((64, 512, 20480, 512), False),     # 320 hidden blocks > 2 per CTA: Stream-K layer 1, not windows
-    ((100, 256, 20480, 264), True),     # the same for the gated form, ragged P
+    ((64, 512, 20480, 512), False),     # 320 hidden blocks, 2-3 per CTA: four-block windows (two tiles)
+    ((48, 256, 40960, 264), False),     # 640 blocks, more than 4 per CTA: Stream-K layer 1, ragged P
+    ((100, 256, 20480, 264), True),     # gated past 2 blocks per CTA: Stream-K layer 1, ragged P
 ])
-def test_stream_wide_hidden_uses_split_layer1(cuda_lib, shape, glu):
+def test_stream_wide_hidden(cuda_lib, shape, glu):
     M, N, O, P = shape
     if glu:
         g = synth.glu_inputs(M, N, O, P, seed=M + 3, device="cuda")

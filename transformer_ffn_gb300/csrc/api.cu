@@ -269,8 +269,9 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, int sms, bo
             path = 2;
         else if (M <= STREAM_MAX_M)
             path = 6;
-        else if (M <= wstream::MAX_ROWS && wstream::make_plan(M, N, O, P, sms, glu).win)
-            path = 6;   // on the Llama 3 8B shape at 256 rows: 87 us against 125 us on the engine
+        else if (M <= wstream::MAX_ROWS && wstream::make_plan(M, N, O, P, sms, glu).win == 1)
+            path = 6;   // on the Llama 3 8B shape at 256 rows: 87 us against 125 us on the engine (with
+                        // four-block windows, (8192, 28672, 8192) at 256 rows: 247 us against 236)
         else
             path = 1;
     }

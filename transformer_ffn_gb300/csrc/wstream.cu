@@ -107,7 +107,7 @@ __device__ bool wait_h(const WaitCtx& w, const uint32_t* flags, uint32_t epoch, 
 // Layer 1 streams W1 (and W3) with X; layer 2 first loads the W2 part of its
 // first stages (W2 does not depend on H), waits once for every H slice its
 // range reads, then streams W2 with H.
-template <int NB, bool GLU>
+template <int NB, bool GLU, bool W2>
 __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const WaitCtx& w, int lane)
 {
     using Gm = Geo<NB>;
@@ -153,11 +153,13 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
 
     // ---- layer 1
     if (lane == 0 && pl.win) {
-        // The window: every K chunk of this CTA's 128 hidden columns (W1, and
-        // W3 when gated) with the X chunk, in the layer-1 ring.
-        constexpr int N1 = GLU ? Gm::NST : Gm::NST1;
-        constexpr int S1 = GLU ? Gm::STAGE : Gm::STAGE1;
-        constexpr uint32_t bytes1 = static_cast<uint32_t>((GLU ? 4 : 2) * W_BOX + Gm::X_BYTES);
+        // The window: every K chunk of this CTA's window (W1's 128 columns,
+        // and W3's same 128 when gated, or W1's 256 for a four-block window)
+        // with the X chunk, in the layer-1 ring.
+        constexpr bool two = GLU || W2;   // two 128-column tiles per stage
+        constexpr int N1 = two ? Gm::NST : Gm::NST1;
+        constexpr int S1 = two ? Gm::STAGE : Gm::STAGE1;
+        constexpr uint32_t bytes1 = static_cast<uint32_t>((two ? 4 : 2) * W_BOX + Gm::X_BYTES);
         const Blocks bk = blocks_of(pl);
         uint32_t st1 = 0, ph1 = 0;
         int32_t last1[N1];
@@ -178,11 +180,13 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
                 ptx::mbar_arrive_expect_tx(fb, bytes1);
                 ptx::tma_load_2d_hint(sw, &p.map_w[0], fb, col0, row, evict_first);
                 ptx::tma_load_2d_hint(sw + W_BOX, &p.map_w[0], fb, col0 + 64, row, evict_first);
-                if (GLU) {
-                    ptx::tma_load_2d_hint(sw + 2 * W_BOX, &p.map_w3, fb, col0, row, evict_first);
-                    ptx::tma_load_2d_hint(sw + 3 * W_BOX, &p.map_w3, fb, col0 + 64, row, evict_first);
+                if (two) {
+                    const CUtensorMap* m1 = GLU ? &p.map_w3 : &p.map_w[0];
+                    const int32_t col1 = GLU ? col0 : col0 + 128;
+                    ptx::tma_load_2d_hint(sw + 2 * W_BOX, m1, fb, col1, row, evict_first);
+                    ptx::tma_load_2d_hint(sw + 3 * W_BOX, m1, fb, col1 + 64, row, evict_first);
                 }
-                ptx::tma_load_2d(sw + (GLU ? 4 : 2) * W_BOX, &p.map_x[0], fb, row, 0);
+                ptx::tma_load_2d(sw + (two ? 4 : 2) * W_BOX, &p.map_x[0], fb, row, 0);
                 last1[st1] = static_cast<int32_t>(ph1);
                 if (++st1 == N1) {
                     st1 = 0;
@@ -287,7 +291,7 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* stages, const W
 // 1 KiB apart; a 16-deep k step advances 2 KiB), B the K-major X tile (rows
 // of 128 bytes; a k step advances 32 bytes), shared by both tiles, whose
 // products go to the two NB-column halves of the run's buffer.
-template <int NB, bool GLU>
+template <int NB, bool GLU, bool W2>
 __device__ void run_mma(const Params& p, Aux& aux, uint8_t* stages, const WaitCtx& w, uint32_t tmem_base)
 {
     using Gm = Geo<NB>;
@@ -298,8 +302,9 @@ __device__ void run_mma(const Params& p, Aux& aux, uint8_t* stages, const WaitCt
     for (int layer = 0; layer < 2 && ok; ++layer) {
         if (layer == 0 && pl.win) {
             // the window: one run over all K chunks, in the layer-1 ring
-            constexpr int N1 = GLU ? Gm::NST : Gm::NST1;
-            constexpr int S1 = GLU ? Gm::STAGE : Gm::STAGE1;
+            constexpr bool two = GLU || W2;
+            constexpr int N1 = two ? Gm::NST : Gm::NST1;
+            constexpr int S1 = two ? Gm::STAGE : Gm::STAGE1;
             const Blocks bk = blocks_of(pl);
             if (bk.b1 <= bk.b0)
                 continue;
@@ -318,13 +323,13 @@ __device__ void run_mma(const Params& p, Aux& aux, uint8_t* stages, const WaitCt
                 const uint32_t sw = ptx::smem_u32(stages + st1 * S1);
                 const uint64_t adesc = ptx::sdesc_sw128(sw, W_BOX, 1024);
                 const uint64_t adesc1 = ptx::sdesc_sw128(sw + 2 * W_BOX, W_BOX, 1024);
-                const uint64_t bdesc = ptx::sdesc_sw128(sw + (GLU ? 4 : 2) * W_BOX, 16, 1024);
+                const uint64_t bdesc = ptx::sdesc_sw128(sw + (two ? 4 : 2) * W_BOX, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < KC / 16; ++k) {
                     const uint64_t bk16 = bdesc + static_cast<uint64_t>((k * 32) >> 4);
                     const uint32_t acc = (kc == 0 && k == 0) ? 0u : 1u;
                     ptx::umma_bf16(d, adesc + static_cast<uint64_t>((k * 2048) >> 4), bk16, idesc, acc);
-                    if (GLU)
+                    if (two)
                         ptx::umma_bf16(d + NB, adesc1 + static_cast<uint64_t>((k * 2048) >> 4), bk16, idesc, acc);
                 }
                 ptx::umma_commit(ptx::smem_u32(&aux.empty1[st1]));
@@ -825,19 +830,24 @@ __device__ __forceinline__ bool run_phase(const Params& p, Aux& aux, const WaitC
     return true;
 }
 
-// Window layer 1: the CTA's 128-column tile of H over all of K.  Warp q
-// holds columns 32q .. 32q + 31 of the window, in block b0 + q / 2; the warps
-// of an owned block write it (act(v + bias), or act(gate) * linear) and
-// publish its ready word, the others only release the accumulator.
-template <int NB, bool GATED>
+// Window layer 1: the CTA's window of H over all of K, one 128-column tile
+// (or, for a four-block window, two: tensor-memory columns [0, NB) and
+// [NB, 2 NB)).  Warp q holds columns 32q .. 32q + 31 of each tile, in block
+// (the tile's first block) + q / 2; the warps of an owned block write it
+// (act(v + bias), or act(gate) * linear) and publish its ready word, the
+// others only release the accumulator.
+template <int NB, bool GATED, bool W2>
 __device__ void drain_window(const Params& p, Aux& aux, uint32_t tmem_base, Blocks bk, uint32_t buf, int q, int lane)
 {
     using Gm = Geo<NB>;
-    const int32_t block = bk.b0 + q / 2;
-    const bool owned = block < bk.b1;
-    const int64_t gcol = static_cast<int64_t>(bk.b0) * 64 + q * 32 + lane;
+    constexpr int ntile = (!GATED && W2) ? 2 : 1;
     const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Gm::ACC_COLS;
-    if (owned) {
+#pragma unroll 1
+    for (int t = 0; t < ntile; ++t) {
+        const int32_t block = bk.b0 + 2 * t + q / 2;
+        if (block >= bk.b1)
+            continue;
+        const int64_t gcol = static_cast<int64_t>(bk.b0) * 64 + t * 128 + q * 32 + lane;
         const float bias = (!GATED && p.b1 != nullptr && gcol < p.O) ? __bfloat162float(p.b1[gcol]) : 0.0f;
         float v[CH], lin[CH];
 #pragma unroll
@@ -845,7 +855,7 @@ __device__ void drain_window(const Params& p, Aux& aux, uint32_t tmem_base, Bloc
             lin[i] = 0.0f;
 #pragma unroll 1
         for (int ch = 0; ch < NB / CH; ++ch) {
-            tmem_chunk(tb + ch * CH, v);
+            tmem_chunk(tb + t * NB + ch * CH, v);
             if (GATED)
                 tmem_chunk(tb + NB + ch * CH, lin);
             store_any<GATED>(p.act1, p.H, p.O, p.M, gcol, bias, v, lin, ch * CH, lane);
@@ -855,9 +865,17 @@ __device__ void drain_window(const Params& p, Aux& aux, uint32_t tmem_base, Bloc
     __syncwarp();
     if (lane == 0)
         ptx::mbar_arrive(ptx::smem_u32(&aux.tmem_empty[buf]));
-    if (owned) {
-        ptx::fence_proxy_async_global();
-        __syncwarp();   // the warp's stores, then one release by lane 0
+    bool fenced = false;
+#pragma unroll 1
+    for (int t = 0; t < ntile; ++t) {
+        const int32_t block = bk.b0 + 2 * t + q / 2;
+        if (block >= bk.b1)
+            continue;
+        if (!fenced) {
+            ptx::fence_proxy_async_global();
+            __syncwarp();   // the warp's stores, then one release by lane 0 per block
+            fenced = true;
+        }
         if (lane == 0)
             ptx::st_release_gpu(p.flags + block * 2 + (q & 1), aux.epoch);
     }
@@ -866,7 +884,7 @@ __device__ void drain_window(const Params& p, Aux& aux, uint32_t tmem_base, Bloc
 // Per layer: drain every run as its accumulator completes (phase 1), then sum
 // this CTA's shares of the split slices (phase 2).  A CTA stores all of its
 // parts before it waits on anyone else's, so the waits cannot form a chain.
-template <int NB, bool GLU>
+template <int NB, bool GLU, bool W2>
 __device__ void run_epilogue(const Params& p, Aux& aux, const WaitCtx& w, uint8_t* ring, uint32_t tmem_base, int warp,
                              int lane)
 {
@@ -882,7 +900,7 @@ __device__ void run_epilogue(const Params& p, Aux& aux, const WaitCtx& w, uint8_
             if (!wait_mbar(w, ptx::smem_u32(&aux.tmem_full[buf]), (iter / Geo<NB>::NBUF) & 1u, SITE_TMEM_FULL))
                 return;
             ptx::tc_fence_after();
-            drain_window<NB, GLU>(p, aux, tmem_base, bk, buf, q, lane);
+            drain_window<NB, GLU, W2>(p, aux, tmem_base, bk, buf, q, lane);
             ++iter;
             continue;
         }
@@ -906,7 +924,7 @@ __device__ void run_epilogue(const Params& p, Aux& aux, const WaitCtx& w, uint8_
     }
 }
 
-template <int NB, bool GLU>
+template <int NB, bool GLU, bool W2>
 __global__ void __launch_bounds__(NUM_THREADS, 1) wstream_kernel(const __grid_constant__ Params p)
 {
     using Gm = Geo<NB>;
@@ -955,12 +973,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) wstream_kernel(const __grid_co
     const WaitCtx w{&aux.abort, p.ctrl, p.wait_limit_ns, 0u};
 
     if (warp == 0) {
-        run_producer<NB, GLU>(p, aux, stages, w, lane);
+        run_producer<NB, GLU, W2>(p, aux, stages, w, lane);
     } else if (warp == 1) {
         if (lane == 0)
-            run_mma<NB, GLU>(p, aux, stages, w, tmem_base);
+            run_mma<NB, GLU, W2>(p, aux, stages, w, tmem_base);
     } else {
-        run_epilogue<NB, GLU>(p, aux, w, stages, tmem_base, warp, lane);
+        run_epilogue<NB, GLU, W2>(p, aux, w, stages, tmem_base, warp, lane);
     }
     __syncwarp();
     ptx::tc_fence_before();
@@ -984,18 +1002,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) wstream_kernel(const __grid_co
 
 namespace {
 
-template <int NB, bool GLU>
+template <int NB, bool GLU, bool W2>
 int launch_instance(const wstream::Params& p, cudaStream_t s)
 {
     using Gm = wstream::Geo<NB>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(wstream::wstream_kernel<NB, GLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(wstream::wstream_kernel<NB, GLU, W2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Gm::SMEM) != cudaSuccess)
             return -1;
         attr_set = true;
     }
-    wstream::wstream_kernel<NB, GLU><<<p.plan.grid, wstream::NUM_THREADS, Gm::SMEM, s>>>(p);
+    wstream::wstream_kernel<NB, GLU, W2><<<p.plan.grid, wstream::NUM_THREADS, Gm::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -1004,13 +1022,17 @@ int launch_instance(const wstream::Params& p, cudaStream_t s)
 int launch_wstream(const wstream::Params& p, cudaStream_t s)
 {
     if (p.plan.rows == 32)
-        return p.glu ? launch_instance<32, true>(p, s) : launch_instance<32, false>(p, s);
+        return p.glu ? launch_instance<32, true, false>(p, s)
+                     : (p.plan.win == 2 ? launch_instance<32, false, true>(p, s) : launch_instance<32, false, false>(p, s));
     if (p.plan.rows == 64)
-        return p.glu ? launch_instance<64, true>(p, s) : launch_instance<64, false>(p, s);
+        return p.glu ? launch_instance<64, true, false>(p, s)
+                     : (p.plan.win == 2 ? launch_instance<64, false, true>(p, s) : launch_instance<64, false, false>(p, s));
     if (p.plan.rows == 128)
-        return p.glu ? launch_instance<128, true>(p, s) : launch_instance<128, false>(p, s);
+        return p.glu ? launch_instance<128, true, false>(p, s)
+                     : (p.plan.win == 2 ? launch_instance<128, false, true>(p, s) : launch_instance<128, false, false>(p, s));
     if (p.plan.rows == 256)
-        return p.glu ? launch_instance<256, true>(p, s) : launch_instance<256, false>(p, s);
+        return p.glu ? launch_instance<256, true, false>(p, s)
+                     : (p.plan.win == 2 ? launch_instance<256, false, true>(p, s) : launch_instance<256, false, false>(p, s));
     return -1;
 }
 

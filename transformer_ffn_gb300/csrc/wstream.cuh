@@ -98,9 +98,11 @@ struct Plan {
     // [c * nblk / grid, (c + 1) * nblk / grid) (one or two) and computes them
     // over the whole of K as one 128-column tile (the second block of a
     // one-block CTA is its neighbour's, computed and dropped): no split
-    // slices, so H is final when a CTA's stream ends.  Used whenever every
-    // CTA owns at most two blocks (hidden width up to 128 x CTAs); otherwise
-    // layer 1 is a Stream-K over 256-column slices like layer 2.
+    // slices, so H is final when a CTA's stream ends.  win = 1 when every
+    // CTA owns at most two blocks (hidden width up to 128 x CTAs); win = 2
+    // (dense) up to four, the window then two 128-column tiles (256
+    // columns, the stage geometry of layer 2); otherwise (win = 0) layer 1
+    // is a Stream-K over 256-column slices like layer 2.
     int32_t win;
     int32_t nblk;           // 64-column hidden blocks (window layer 1)
     int32_t h_cols;         // hidden columns of a layer-1 slice: 256, or 128 gated
@@ -163,7 +165,7 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool
     if (g < 1)
         g = 1;
     pl.nblk = static_cast<int32_t>((O + 63) / 64);
-    pl.win = pl.nblk <= 2 * g ? 1 : 0;
+    pl.win = pl.nblk <= 2 * g ? 1 : ((!glu && pl.nblk <= 4 * g) ? 2 : 0);
     if (!pl.win && pl.units[0] < g)
         g = pl.units[0];
     pl.grid = static_cast<int32_t>(g);
