@@ -21,6 +21,7 @@ timed region, and the CPU oracle timed on a bounded sample of the workload
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -168,11 +169,19 @@ def sustained_bf16_peak():
         return None
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace runs collapsed, so that
+    a record taken on a kernel stays valid across comment-only edits."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_sha(kernel):
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "transformer_ffn_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "transformer_ffn_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -32,3 +32,9 @@ def test_clock_summary_short_region_takes_the_nearest_sample():
 
 def test_clock_summary_ignores_malformed_lines():
     assert bench.summarize_clocks(["", "garbage", "a, b"], [0.0, 1.0], 20) is None
+
+
+def test_kernel_hash_ignores_comments_only():
+    code = "int a = 1; // a comment\n/* block\n comment */ float b;"
+    assert bench._code_only(code) == bench._code_only("int a = 1;\nfloat   b;")
+    assert bench._code_only(code) != bench._code_only("int a = 2; float b;")

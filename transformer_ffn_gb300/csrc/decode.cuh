@@ -7,19 +7,22 @@
 // accesses to get there).  Work is cut into units of SLICE output columns x KC
 // rows of K; CTA c of G owns the contiguous unit range [c*U/G, (c+1)*U/G) of
 // each layer (Stream-K style: every CTA gets the same amount of weight bytes).
-// A slice whose K range is split across CTAs is finished by the last CTA to
-// arrive on the slice's counter, which sums the parts in part order, so the
-// result does not depend on arrival order ("Kernel fusion and tensor
-// parallelism", section "Step 1": a per-tile counter, the last contributor
-// marks the tile ready; the accumulation of partial tiles with completion
-// flags that Stream-K uses).  A finished layer-1 slice of H publishes a ready
-// flag; layer-2 units wait on the flag of the H slice they read.
+// A slice whose K range is split across CTAs is finished by the CTA holding
+// its part 0 (the run that ends that CTA's range, normally the last part to
+// be done): once the slice's counter shows the other parts it adds them in
+// part order to its own, so the result does not depend on arrival order
+// ("Kernel fusion and tensor parallelism", section "Step 1": a per-tile
+// counter completes the tile; the accumulation of partial tiles with
+// completion flags that Stream-K uses).  A finished layer-1 slice of H
+// publishes a ready flag; layer-2 units wait on the flags of the H slices
+// they read.
 //
-// Gated FFN (H = act(X W1) * (X W3)): a layer-1 unit covers 64 hidden
-// columns; its stage holds the W1 box and the W3 box of those columns, and
-// each consumer warp takes 16 columns of each, so every thread ends with the
-// gate and linear fragments of the same H elements.  A layer-2 K chunk then
-// reads two layer-1 slices of H.
+// Gated FFN (H = act(X W1) * (X W3)), up to 32 rows: layer 1 is a window
+// instead (Plan::win): each CTA owns one or two 64-column hidden blocks and
+// streams 128 adjacent columns of W1 and of W3 over all of K, each consumer
+// warp taking 32 columns of each, so every thread ends with the gate and
+// linear fragments of the same H elements; no split, one ready word per block
+// and owning warp.  A layer-2 K chunk reads two 64-column blocks of H.
 //
 // Layout per CTA: warp 0 issues TMA copies (W tile [KC x SLICE] as two
 // 128-byte-swizzled boxes, plus the [rows x KC] tile of X or H); warps 1..4

@@ -2,26 +2,36 @@
 // persistent launch that reads every weight byte once, on the tcgen05 tensor
 // cores with the weights as the MMA's M side ("swap-AB").
 //
-// From 65 to 256 rows the FFN is still bound by the weight bytes (2 M FLOP per
+// From 33 to 256 rows the FFN is still bound by the weight bytes (2 M FLOP per
 // weight byte pair: M below the ~287 FLOP/byte ridge of a GB300), but the
 // row-band engine has too few tiles to fill the GPU and mma.sync has too
-// little throughput to keep up with HBM.  Here a unit is KC = 64 rows of K for
-// one slice of 256 output columns: each 128-column half of W (MN-major) is
-// the A operand (M = 128) of one MMA, the K chunk of X or H (NB token rows,
-// K-major) the B operand (N = NB) of both, and the products accumulate in
-// tensor memory, one lane per output column and one column per token.  Units are
+// little throughput to keep up with HBM.  A 128-column tile of W (MN-major)
+// is the A operand (M = 128) of an MMA, the K chunk of X or H (NB token rows,
+// K-major) its B operand (N = NB), and the products accumulate in tensor
+// memory, one lane per output column and one column per token.
+//
+// Layer 1 has many output columns and a short K, so it is not split: each
+// CTA owns one or two (up to four) 64-column hidden blocks and computes a
+// window of 128 (256) columns over all of K (Plan::win; the window's blocks
+// it does not own are its neighbour's, computed and dropped).  Its H is
+// final when the CTA's stream ends; the owning warps store it and stamp one
+// ready word per block.
+//
+// Layer 2 has few output columns and a long K: a unit is KC = 64 rows of K
+// for a slice of 256 output columns (two tiles sharing the H chunk), units
 // spread over the CTAs as contiguous ranges (Stream-K, equal weight bytes per
 // CTA).  A slice split across CTAs leaves fp32 partial sums in fixed places;
 // once the slice's arrival counter shows every part ("Kernel fusion and
 // tensor parallelism", section "Step 1": per-tile counters complete the
 // tile), each contributing CTA sums its share of the slice's rows over all
-// parts in part order, so the result does not depend on timing.
-// A finished layer-1 slice of H publishes ready flags; a layer-2 range waits
-// for the H slices it reads, with its first W2 stages already loaded.
+// parts in part order, so the result does not depend on timing.  A layer-2
+// range loads its first W2 stages, then waits for the H blocks it reads.
+// (Hidden widths past four blocks per CTA run layer 1 the same way as layer
+// 2, with ready words per H slice.)
 //
-// Gated layer 1 (H = act(X W1) * (X W3)): the unit's two tiles are the same
-// 128 columns of W1 and of W3, so the two accumulators hold the gate and the
-// linear product and one thread has both values of its column.
+// Gated layer 1 (H = act(X W1) * (X W3)): the window's two tiles are the
+// same 128 columns of W1 and of W3, so the two accumulators hold the gate and
+// the linear product and one thread has both values of its column.
 //
 // CTA layout (192 threads): warp 0 issues the TMA copies; warp 1 allocates
 // tensor memory and one of its threads issues the MMAs; warps 2-5 drain the
