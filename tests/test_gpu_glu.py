@@ -119,6 +119,7 @@ def test_dense_ffn_with_silu_on_both_paths(cuda_lib):
     (32, 1024, 2048, 512, "silu"),       # two 16-row tiles
     (8, 4096, 8192, 1024, "relu"),       # long split-K ranges
     (64, 1024, 2048, 512, "silu"),       # the 64-row instance
+    (8, 512, 20480, 256, "silu"),        # 320 hidden blocks, more than two per CTA: split layer 1, no window
 ])
 def test_glu_decode_path_full(cuda_lib, M, N, O, P, act):
     X, W1, W3, W2 = _inputs(M, N, O, P, seed=3 * M + O)
