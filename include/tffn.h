@@ -276,6 +276,19 @@ int tffn_timing_end(int* launches, double* total_ms);
 int64_t tffn_debug_engine_task(int64_t m_blocks, int32_t n1, int32_t n2, int32_t group_m,
                                int64_t ticket, int32_t out[3]);
 
+/* Host-side view of a weight stream's work plan, for tests (no GPU needed).
+ * path = 2 (mma.sync stream) or 6 (tcgen05 stream), for M x N x O x P on
+ * `sms` SMs, glu = 1 for the gated form.  out = {grid, window mode (0 split
+ * layer 1; 1 two-block windows; 2 four-block windows), 64-column hidden
+ * blocks, slices of layer 1, slices of layer 2, K chunks per slice of layer 1
+ * (window: chunks of the window's K loop), K chunks per slice of layer 2,
+ * units of layer 1, units of layer 2, most parts of one slice in layer 1 and
+ * in layer 2, bytes of split-K partial sums}.  Returns TFFN_OK,
+ * TFFN_ERR_INVALID_ARG for another path or non-positive sizes, or
+ * TFFN_ERR_UNSUPPORTED past the stream's 256 rows. */
+int tffn_debug_stream_plan(int path, int64_t M, int64_t N, int64_t O, int64_t P, int sms, int glu,
+                           int64_t out[12]);
+
 /* Tile sizes of the engine (rows, columns, k-step) and of the decode stream,
  * for tests and tools: out[0..5] = {BM, BN, BK, stages, decode slice width,
  * decode k chunk}. */

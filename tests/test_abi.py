@@ -142,3 +142,76 @@ def test_ops_fail_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(tffn, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         tffn.load()
+
+
+def _owned_blocks(nblk, grid):
+    return [(c * nblk // grid, (c + 1) * nblk // grid) for c in range(grid)]
+
+
+def _check_stream_k(U, G, kch, maxp):
+    # contiguous ranges of U units over G CTAs: a partition, sizes within one,
+    # every CTA with at least one unit, no slice split over more than maxp CTAs
+    starts = [c * U // G for c in range(G + 1)]
+    assert starts[0] == 0 and starts[-1] == U
+    sizes = [b - a for a, b in zip(starts, starts[1:])]
+    assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
+    owners = {}
+    for c in range(G):
+        for s in range(starts[c] // kch, (starts[c + 1] - 1) // kch + 1):
+            owners.setdefault(s, set()).add(c)
+    assert max(len(v) for v in owners.values()) <= maxp
+
+
+@pytest.mark.parametrize("path,M,N,O,P,glu", [
+    (2, 16, 8192, 28672, 8192, False), (2, 16, 4096, 14336, 4096, True), (2, 32, 4096, 14336, 4096, True),
+    (2, 8, 512, 20480, 256, True), (2, 1, 256, 384, 136, True), (2, 64, 1024, 2048, 512, True),
+    (6, 128, 4096, 14336, 4096, False), (6, 128, 4096, 14336, 4096, True), (6, 256, 4096, 14336, 4096, False),
+    (6, 128, 8192, 28672, 8192, False), (6, 64, 256, 40960, 264, False), (6, 100, 256, 20480, 264, True),
+    (6, 65, 136, 520, 264, False), (6, 1, 256, 264, 72, False),
+])
+@pytest.mark.parametrize("sms", [152, 148, 132])
+def test_stream_plans(lib, path, M, N, O, P, glu, sms):
+    import transformer_ffn_gb300 as tffn
+    pl = tffn.debug_stream_plan(path, M, N, O, P, sms, glu)
+    G, win, nblk = pl["grid"], pl["win"], pl["nblk"]
+    assert 1 <= G <= sms
+    assert nblk == (O + 63) // 64
+    # layer 2 is always Stream-K over its slices
+    cols2 = 128 if path == 2 else 256
+    kc2 = 128 if path == 2 else 64
+    assert pl["slices1"] == (P + cols2 - 1) // cols2 and pl["kch1"] == (O + kc2 - 1) // kc2
+    assert pl["units1"] == pl["slices1"] * pl["kch1"] and G <= pl["units1"]
+    _check_stream_k(pl["units1"], G, pl["kch1"], pl["maxp1"])
+    # the window layer 1: when it is used and how much each CTA owns
+    if path == 2:
+        expect = 1 if (glu and M <= 32 and nblk <= 2 * G) else 0
+    else:
+        expect = 1 if nblk <= 2 * G else (2 if (not glu and nblk <= 4 * G) else 0)
+    assert win == expect
+    if win:
+        owned = _owned_blocks(nblk, G)
+        assert max(b - a for a, b in owned) <= 2 * win
+        assert owned[0][0] == 0 and owned[-1][1] == nblk
+        assert all(owned[i][1] == owned[i + 1][0] for i in range(G - 1))
+        assert pl["maxp0"] <= 1
+    else:
+        assert pl["units0"] == pl["slices0"] * pl["kch0"] and G <= pl["units0"]
+        _check_stream_k(pl["units0"], G, pl["kch0"], pl["maxp0"])
+    # the split-K partial area holds every split slice's parts
+    rows = (32 if M <= 32 else 64) if path == 2 else (32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256)
+    part = rows * (128 if path == 2 else 256) * 4
+    need = 0
+    for l in (0, 1):
+        if l == 0 and win:
+            continue
+        if pl[f"maxp{l}"] > 1:
+            need += pl[f"slices{l}"] * pl[f"maxp{l}"] * part
+    assert pl["partial_bytes"] >= need
+
+
+def test_stream_plan_validation(lib):
+    import transformer_ffn_gb300 as tffn
+    with pytest.raises(tffn.TffnError):
+        tffn.debug_stream_plan(6, 257, 64, 64, 64, 152)
+    with pytest.raises(tffn.TffnError):
+        tffn.debug_stream_plan(3, 16, 64, 64, 64, 152)

@@ -80,6 +80,8 @@ def load():
     L.tffn_debug_engine_task.restype = i64
     L.tffn_debug_tiles.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     L.tffn_debug_tiles.restype = None
+    L.tffn_debug_stream_plan.argtypes = [i32, i64, i64, i64, i64, i32, i32, ctypes.POINTER(ctypes.c_int64)]
+    L.tffn_debug_stream_plan.restype = i32
     _lib = L
     return L
 
@@ -304,6 +306,15 @@ def debug_engine_task(m_blocks, n1, n2, group_m, ticket):
     out = (ctypes.c_int32 * 3)()
     total = load().tffn_debug_engine_task(m_blocks, n1, n2, group_m, ticket, out)
     return int(total), (out[0], out[1], out[2])
+
+
+def debug_stream_plan(path, M, N, O, P, sms, glu=False):
+    """The work plan of the weight stream `path` (2 or 6) as a dict (host only)."""
+    out = (ctypes.c_int64 * 12)()
+    _raise(load().tffn_debug_stream_plan(path, M, N, O, P, sms, 1 if glu else 0, out), "debug_stream_plan")
+    keys = ("grid", "win", "nblk", "slices0", "slices1", "kch0", "kch1", "units0", "units1", "maxp0", "maxp1",
+            "partial_bytes")
+    return dict(zip(keys, list(out)))
 
 
 def debug_tiles():
