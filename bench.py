@@ -1,6 +1,13 @@
 """Benchmark of the fused FFN (and its decode / large / MoE workloads).
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME|all] [--impl reference]
+
+By default (--config all) it measures five workloads one after the other --
+the tiny, prefill, decode, large and MoE FFNs -- and prints ONE line: the
+headline fields are the prefill FFN's, `configs` holds every workload's
+entry (value, roofline, end-to-end figures, clocks, CPU oracle baseline),
+`small_m` summarises the decode workload (weight GB/s) and `large_m` the
+large one (TFLOP/s).  --config NAME measures one workload.
 
 A step is one ffn_forward (or moe_ffn_forward) call over one batch of
 synthetic input resident in HBM.  Timing: W untimed warm-up steps, then K
@@ -68,7 +75,12 @@ CONFIGS = {
                        label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh, "
                              "stress-skewed router (expert 0 in ~98% of tokens)"),
 }
-DEFAULT = "prefill"
+# The default run measures these five workloads (the tiny, prefill, decode,
+# large and MoE FFNs) and prints one line whose headline is the prefill FFN;
+# --config NAME measures one workload.
+SUITE = ("tiny", "prefill", "decode", "large", "moe")
+HEADLINE = "prefill"
+DEFAULT = "all"
 FFN_PATHS = {"auto": 0, "fused": 1, "decode": 2, "two": 3, "reduce": 4, "b2b": 5, "stream": 6}
 FLUSH_BYTES = 256 << 20
 SPEC_BF16_TFLOPS = 2250.0   # GB300 dense bf16 (NVIDIA's 2:4-sparse figures are twice this)
@@ -463,6 +475,42 @@ def time_steps(step, steps, flush_buf, stream):
     return [a.elapsed_time(b) / 1e3 for a, b in evs]
 
 
+def run_e2e_latency(cfg, inp, steps, warmup, stream):
+    """Per-call latency through the public API, one call at a time: upload the
+    step's input from pinned host memory, run the FFN, download its result,
+    synchronise; host wall clock around all four.  Returns the per-step
+    seconds."""
+    import torch
+    import transformer_ffn_gb300 as tffn
+    moe = cfg["kind"] == "moe"
+    X_host = inp.X.cpu().pin_memory()
+    L_host = inp.logits.cpu().pin_memory() if moe else None
+    Y_host = torch.empty((cfg["M"], cfg["P"]), dtype=torch.bfloat16).pin_memory()
+    X_dev = torch.empty_like(inp.X)
+    L_dev = torch.empty_like(inp.logits) if moe else None
+    Y_dev = torch.empty((cfg["M"], cfg["P"]), dtype=torch.bfloat16, device=inp.X.device)
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            X_dev.copy_(X_host, non_blocking=True)
+            if moe:
+                L_dev.copy_(L_host, non_blocking=True)
+            if moe:
+                moe_call(cfg, inp, X_dev, L_dev, out=Y_dev, stream=stream)
+            elif cfg["kind"] == "glu":
+                tffn.ffn_glu_forward(X_dev, inp.W1, inp.W3, inp.W2, cfg["act1"], out=Y_dev, stream=stream)
+            else:
+                tffn.ffn_forward(X_dev, inp.W1, inp.b1, inp.W2, inp.b2, cfg["act1"], cfg["act2"], out=Y_dev,
+                                 stream=stream)
+            Y_host.copy_(Y_dev, non_blocking=True)
+        stream.synchronize()
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    tffn.check()
+    return times
+
+
 def padded_rows(cfg, inp):
     """Rows of the grouped layout, zero padding included (each expert's rows
     rounded up to whole 256-row bands), from the routing the library returns."""
@@ -471,14 +519,14 @@ def padded_rows(cfg, inp):
     return int(sum((c + 255) // 256 * 256 for c in counts))
 
 
-def run_gpu(args, world, rank, local):
+def measure_gpu(name, args, world, rank, local, with_cpu):
+    """One workload: device-timed steps, the dominant kernel's roofline, the
+    end-to-end figures, clocks, and (rank 0, N = 1) the CPU oracle baseline.
+    Returns the workload's entry of the JSON line."""
     import torch
     import transformer_ffn_gb300 as tffn
 
-    tffn.load()
-    tffn.set_option(tffn.OPT_MOE_ORDER, args.moe_order)
-    tffn.set_option(tffn.OPT_PATH, FFN_PATHS[args.ffn_path])
-    cfg = CONFIGS[args.config]
+    cfg = CONFIGS[name]
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     inp = make_inputs(cfg, dev)
@@ -534,46 +582,96 @@ def run_gpu(args, world, rank, local):
     roof["spec_peak"] = SPEC_HBM_GBS if is_hbm_bound(cfg) else SPEC_BF16_TFLOPS
     roof["frac_of_spec"] = roof["achieved"] / roof["spec_peak"]
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json {'hbm_gbs' if is_hbm_bound(cfg) else 'bf16_tflops'})"
-    roof["kernel"] = dominant_kernel(args.config, args.ffn_path)
+    roof["kernel"] = dominant_kernel(name, args.ffn_path)
     roof["kernel_ms"] = dom_s * 1e3
-    roof["traffic"] = recorded_traffic(args.config, roof["kernel"])
+    roof["algorithmic_per_launch"] = weight_bytes(cfg) if is_hbm_bound(cfg) else flops(cfg)
+    roof["traffic"] = recorded_traffic(name, roof["kernel"])
 
-    # ---- end to end through the public API: every step uploads its input from
-    # pinned host memory, runs the FFN and downloads its result.  Steps are
-    # pipelined the way a serving loop runs them: step i+1's upload and step
-    # i-1's download overlap step i's compute (double-buffered device tensors,
-    # one stream per direction, ordered by events).
+    # ---- end to end through the public API.  Pipelined: every step uploads
+    # its input from pinned host memory, runs the FFN and downloads its result,
+    # step i+1's upload and step i-1's download overlapping step i's compute
+    # (double-buffered device tensors, one stream per direction, ordered by
+    # events).  Latency: the same, one call at a time with a synchronisation.
     e2e_mean, h2d, d2h = run_e2e(cfg, inp, args, flush_buf, stream)
     e2e_mean = max_over_ranks(e2e_mean, world)
+    lat = run_e2e_latency(cfg, inp, args.steps, max(2, args.warmup), stream)
+    lat_mean = max_over_ranks(sum(lat) / len(lat), world)
 
-    line = {
-        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": mean_s * 1e3,
-        "ms_per_step_min": min(per_step) * 1e3, "ms_per_step_std": statistics.pstdev(per_step) * 1e3,
-        "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; X~N(0,1), W~N(0,1/fan_in), b~U(-0.1,0.1), bf16)",
-        "config": {"workload": cfg["label"], "parallelism": f"replicas{world}" if world > 1 else "single GPU",
-                   "l2": l2_note,
-                   "global_batch": cfg["M"] * world, "flops_per_step": flops(cfg)},
+    entry = {
+        "workload": cfg["label"], "metric": metric, "value": value, "unit": unit,
+        "ms_per_step": mean_s * 1e3, "ms_per_step_min": min(per_step) * 1e3,
+        "ms_per_step_std": statistics.pstdev(per_step) * 1e3, "steps": args.steps,
+        "l2": l2_note, "global_batch": cfg["M"] * world, "flops_per_step": flops(cfg),
         "roofline": roof,
         "e2e": {"value": rate(cfg, e2e_mean) * world, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean * 1e3,
-                "mode": "pipelined: upload of step i+1 and download of step i-1 overlap step i"},
+                "mode": "pipelined: upload of step i+1 and download of step i-1 overlap step i",
+                "latency": {"value": rate(cfg, lat_mean) * world, "unit": unit, "ms_per_call": lat_mean * 1e3,
+                            "ms_per_call_median": statistics.median(lat) * 1e3,
+                            "mode": "one call at a time: upload, call, download, synchronise (host wall clock)"}},
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed_block": wall,
     }
     if args.ffn_path != "auto":
-        line["config"]["path"] = args.ffn_path
+        entry["path"] = args.ffn_path
     if cfg["kind"] == "moe":
-        line["config"]["routed_rows"] = cfg["M"] * cfg["k"]
-        line["config"]["router"] = cfg.get("router", "balanced")
-        line["config"]["padded_rows"] = padded_rows(cfg, inp)
-        line["config"]["segment_order"] = "largest expert first" if args.moe_order else "expert index"
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        Y_dev = out.clone()
-        line["cpu_baseline"] = cpu_baseline(cfg, inp, Y_dev, budget_s=args.cpu_budget)
+        entry["routed_rows"] = cfg["M"] * cfg["k"]
+        entry["router"] = cfg.get("router", "balanced")
+        entry["padded_rows"] = padded_rows(cfg, inp)
+        entry["segment_order"] = "largest expert first" if args.moe_order else "expert index"
+    if with_cpu and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        entry["cpu_baseline"] = cpu_baseline(name, cfg, inp, out.clone(), budget_s=args.cpu_budget)
+    del inp, out, flush_buf
+    torch.cuda.empty_cache()
+    return entry
+
+
+def _summary(entry):
+    keep = ("workload", "metric", "value", "unit", "ms_per_step")
+    s = {k: entry[k] for k in keep}
+    s["frac"] = entry["roofline"]["frac"]
+    s["kernel_ms"] = entry["roofline"]["kernel_ms"]
+    s["kernel_achieved"] = entry["roofline"]["achieved"]
+    s["e2e_latency_ms"] = entry["e2e"]["latency"]["ms_per_call"]
+    return s
+
+
+def run_gpu(args, world, rank, local):
+    import transformer_ffn_gb300 as tffn
+
+    tffn.load()
+    tffn.set_option(tffn.OPT_MOE_ORDER, args.moe_order)
+    tffn.set_option(tffn.OPT_PATH, FFN_PATHS[args.ffn_path])
+    names = list(SUITE) if args.config == "all" else [args.config]
+    head = HEADLINE if args.config == "all" else args.config
+    entries = {n: measure_gpu(n, args, world, rank, local, with_cpu=True) for n in names}
+    e = entries[head]
+    line = {
+        "metric": e["metric"], "value": e["value"], "unit": e["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": e["ms_per_step"], "ms_per_step_min": e["ms_per_step_min"],
+        "ms_per_step_std": e["ms_per_step_std"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; X~N(0,1), W~N(0,1/fan_in), b~U(-0.1,0.1), bf16)",
+        "config": {"workload": e["workload"], "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                   "l2": e["l2"], "global_batch": e["global_batch"], "flops_per_step": e["flops_per_step"]},
+        "roofline": e["roofline"], "e2e": e["e2e"], "clocks": e["clocks"], "gpu_launches": e["gpu_launches"],
+        "wall_s_timed_block": e["wall_s_timed_block"],
+    }
+    for k in ("path", "routed_rows", "router", "padded_rows", "segment_order"):
+        if k in e:
+            line["config"][k] = e[k]
+    if "cpu_baseline" in e:
+        line["cpu_baseline"] = e["cpu_baseline"]
+    if len(entries) > 1:
+        line["config"]["headline"] = head
+        line["configs"] = entries
+        # the metric's two halves side by side: weight GB/s at small M (the
+        # decode workload), TFLOP/s at the largest M (the large workload)
+        if "decode" in entries:
+            line["small_m"] = _summary(entries["decode"])
+        if "large" in entries:
+            line["large_m"] = _summary(entries["large"])
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -618,30 +716,67 @@ def _sample_work(cfg, nrows):
     return flops(cfg) * nrows / cfg["M"]
 
 
-def cpu_baseline(cfg, inp, Y_dev=None, budget_s=15.0):
-    """The oracle, as it stands, on rows of the same workload: one row at a
-    time until about budget_s seconds of single-threaded work."""
+def host_cpu():
+    """The host CPU's model name and logical core count."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"model": model, "cores": os.cpu_count()}
+
+
+# Workloads the oracle runs in full (a few seconds of fp64 work); the others
+# are sampled (random rows until the time budget) and their full-workload
+# time is extrapolated linearly from the sample.
+CPU_FULL = ("tiny", "decode")
+
+
+def cpu_baseline(name, cfg, inp, Y_dev=None, budget_s=8.0):
+    """The oracle, as it stands, single-threaded on rows of the same workload:
+    every row for the workloads in CPU_FULL, else one random row at a time
+    until about budget_s seconds of work."""
     import numpy as np
     host = _oracle_inputs(cfg, inp)
+    full = name in CPU_FULL
     rng = np.random.default_rng(0)
-    order = rng.permutation(cfg["M"])
+    order = list(range(cfg["M"])) if full else rng.permutation(cfg["M"])
     done, t_total = [], 0.0
     results = []
-    while t_total < budget_s and len(done) < cfg["M"]:
-        r = int(order[len(done)])
+    if full:
         t0 = time.perf_counter()
-        y = _oracle_rows(cfg, host, [r])
-        t_total += time.perf_counter() - t0
-        done.append(r)
-        results.append(y[0])
+        results = list(_oracle_rows(cfg, host, order))
+        t_total = time.perf_counter() - t0
+        done = order
+    else:
+        while t_total < budget_s and len(done) < cfg["M"]:
+            r = int(order[len(done)])
+            t0 = time.perf_counter()
+            y = _oracle_rows(cfg, host, [r])
+            t_total += time.perf_counter() - t0
+            done.append(r)
+            results.append(y[0])
     metric, unit = metric_of(cfg)
+    what = "tokens" if cfg["kind"] == "moe" else "rows"
     out = {"value": (_sample_work(cfg, len(done)) / t_total) / (1e9 if unit == "GB/s" else 1e12),
            "unit": unit, "cores": 1, "kind": "oracle",
-           "sample": f"{len(done)} of {cfg['M']} {'tokens' if cfg['kind'] == 'moe' else 'rows'} "
-                     f"({cfg['label']}), single-threaded C oracle, fp64 accumulation",
-           "seconds": t_total}
+           "sample": (f"all {cfg['M']} {what}" if full else f"{len(done)} random of {cfg['M']} {what}") +
+                     f" ({cfg['label']}), single-threaded C oracle, fp64 accumulation",
+           "seconds": t_total, "host": host_cpu()}
+    if full:
+        out["full_workload_s"] = t_total
+    else:
+        out["extrapolated"] = True
+        out["full_workload_s_extrapolated"] = t_total * cfg["M"] / len(done)
     if Y_dev is not None:
-        got = Y_dev[done].float().cpu().numpy()
+        got = Y_dev[list(done)].float().cpu().numpy()
         want = np.stack(results)
         err = np.abs(got - want)
         out["parity_on_sample"] = bool(np.all(err <= 1e-2 + 1e-2 * np.abs(want)))
@@ -653,7 +788,8 @@ def run_reference(args, world, rank):
     """Reference arm: the CPU oracle timed on host cores, same metric."""
     if rank != 0:
         return
-    cfg = CONFIGS[args.config]
+    name = HEADLINE if args.config == "all" else args.config
+    cfg = CONFIGS[name]
     inp = make_inputs(cfg, "cpu")
     import numpy as np
     host = _oracle_inputs(cfg, inp)
@@ -677,7 +813,8 @@ def run_reference(args, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, same recipe as the GPU arm)",
             "config": {"workload": cfg["label"], "rows_per_step": rows_per_step},
-            "cpu_baseline": {"value": val, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": val, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample,
+                             "host": host_cpu()},
             "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -689,7 +826,9 @@ def main():
                     help="timed steps (default 200 on the GPU, whose steps take 0.05-10 ms, so that the "
                          "clock samples fall inside the timed region; 20 for the CPU reference arm)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default=DEFAULT, choices=sorted(CONFIGS))
+    ap.add_argument("--config", default=DEFAULT, choices=sorted(CONFIGS) + ["all"],
+                    help="workload; 'all' (default) measures " + ", ".join(SUITE) + " with " + HEADLINE +
+                         " as the headline")
     ap.add_argument("--ffn-path", default="auto", choices=sorted(FFN_PATHS),
                     help="dense FFN path: auto, fused (engine), decode, two (two launches), "
                          "reduce (the reduce-add form of the fused-FFN page, section Step 1), "
@@ -697,7 +836,8 @@ def main():
     ap.add_argument("--moe-order", type=int, default=1, choices=(0, 1),
                     help="MoE grouped-layout segment order: 0 expert index, 1 largest expert first")
     ap.add_argument("--impl", default="tffn", choices=["tffn", "reference"])
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=8.0,
+                    help="seconds of oracle work per sampled workload in the CPU baseline")
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

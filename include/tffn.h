@@ -196,13 +196,26 @@ int moe_glu_forward(const void* X, const float* gate_logits, int top_k, const vo
  *     (cudaMemsetAsync) on `stream` before its kernel: calls that overlap on
  *     the GPU (different streams, not ordered) race and corrupt each other.
  *   - It calls no cudaMalloc, cudaFree or allocating routine, and does not use
- *     or need the workspace of the other entry points.  A device wait that ran
- *     out of time leaves Y incomplete; the record stays in the array (not read
- *     by tffn_check) until the next call clears it.
+ *     or need the workspace of the other entry points.
+ *   - Its device waits are bounded by TFFN_OPT_WAIT_LIMIT_MS like every other
+ *     path.  A wait that ran out of time leaves Y incomplete and records the
+ *     error in the array's control block: tffn_check_noalloc() reads it.  The
+ *     next call clears the record, so check before calling again.
  */
 int ffn_forward_decode_noalloc(const void* X, const void* W1, const void* b1, const void* W2,
                                const void* b2, int act1, int act2, int64_t M, int64_t N, int64_t O,
                                int64_t P, void* Y, struct CUstream_st* stream);
+
+/* Error query of ffn_forward_decode_noalloc: synchronise `stream`, then read
+ * and clear the device-side error record in the static scratch array of the
+ * current device.  Like that entry point it has no counterpart in the paper;
+ * it exists because tffn_check() reads the workspace of the other entry
+ * points, which a caller that cannot allocate never has.  Returns TFFN_OK
+ * (also when no call ran on this device), TFFN_ERR_TIMEOUT, TFFN_ERR_DEVICE,
+ * or TFFN_ERR_CUDA if the synchronisation or the 16-byte read failed; it
+ * allocates nothing.  `detail` (nullable, 4 entries) receives {status, wait
+ * site, block, info}. */
+int tffn_check_noalloc(struct CUstream_st* stream, int32_t* detail);
 
 /* Bytes of workspace a call of this shape needs on the current device
  * (E = 0: ffn_forward or ffn_glu_forward, whichever needs more; E >= 1:
@@ -240,10 +253,14 @@ const char* tffn_status_string(int status);
  *                         apply to ffn_forward only; other values are refused
  *                         (-1, option unchanged)
  *   TFFN_OPT_WAIT_LIMIT_MS  device wait limit in ms (default 4000)
- *   TFFN_OPT_SKIP_FLAG    test fault injection: the engine never publishes
- *                         the ready flag of this GEMM1 tile index (-1 = off);
- *                         the waiting GEMM2 tile then times out and the call
- *                         reports TFFN_ERR_TIMEOUT through tffn_check()
+ *   TFFN_OPT_SKIP_FLAG    test fault injection (-1 = off): the engine never
+ *                         publishes the ready flag of this GEMM1 tile index,
+ *                         and the dense decode stream (ffn_forward up to 32
+ *                         rows, and ffn_forward_decode_noalloc) never
+ *                         publishes the flags of this 128-column H slice; the
+ *                         waiting GEMM2 work then times out and the call
+ *                         reports TFFN_ERR_TIMEOUT through tffn_check() (or
+ *                         tffn_check_noalloc())
  *   TFFN_OPT_GROUP_M      row bands per raster group of the engine (default 4)
  *   TFFN_OPT_MOE_ORDER    order of the experts' row segments in the grouped
  *                         layout: 0 expert index, 1 (default) largest row

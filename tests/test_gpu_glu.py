@@ -5,6 +5,7 @@ import pytest
 import torch
 
 import oracle
+import parity
 from transformer_ffn_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -92,9 +93,14 @@ def test_glu_full_size_sampled_rows(cuda_lib):
     X, W1, W3, W2 = _inputs(M, N, O, P, seed=0)
     Y = cuda_lib.ffn_glu_forward(X, W1, W3, W2, "silu")
     cuda_lib.check()
-    rows = [0, 1, 2047, 4095]
-    _assert_close(Y[rows].float().cpu().numpy(), _oracle(X, W1, W3, W2, "silu", rows=rows), "glu full size")
     assert torch.isfinite(Y.float()).all()
+    # every 256-row band (both CTAs of the pair tile, the band edges) and so
+    # every raster group
+    rows = parity.band_rows(M)
+    u = synth.to_u16
+    host = (u(X), u(W1), u(W3), u(W2))
+    want = parity.oracle_rows(lambda r: oracle.glu_ffn(*host, oracle.ACT_SILU, rows=r), rows)
+    parity.assert_close(Y[rows].float().cpu().numpy(), want, "glu full size")
 
 
 def test_dense_ffn_with_silu_on_both_paths(cuda_lib):

@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+import parity
 from transformer_ffn_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -100,7 +101,25 @@ def test_moe_deterministic(cuda_lib):
     assert torch.equal(a, b)
 
 
-def test_moe_full_size_sampled_tokens(cuda_lib):
+def _oracle_tokens(inp, k, act1, act2, tokens):
+    """The oracle on the given tokens, computed over host threads."""
+    u = synth.to_u16
+    host = (u(inp.X), inp.logits.cpu().numpy(), [u(w) for w in inp.W1], [u(b) for b in inp.b1],
+            [u(w) for w in inp.W2], [u(b) for b in inp.b2])
+    return parity.oracle_rows(lambda t: oracle.moe_ffn(*host[:2], k, *host[2:], ACT[act1], ACT[act2], tokens=t),
+                              tokens)
+
+
+def _full_size_tokens(r, T, k, n_random, seed):
+    """Tokens to compare at full size: the first and last, tokens whose grouped
+    row lies in an expert's zero-padded last band, and random ones."""
+    tail = parity.moe_tail_tokens(r["perm"].cpu().numpy(), r["expert_offsets"].cpu().numpy(), k)
+    rng = np.random.default_rng(seed)
+    rand = rng.choice(T, size=n_random, replace=False).tolist()
+    return sorted(set([0, T - 1] + tail + rand)), tail
+
+
+def test_moe_full_size_tokens(cuda_lib):
     # T 8192, N 4096, E 8 experts of O 14336, P 4096, softmax top-2, GELU-tanh
     T, N, O, P, E, k = 8192, 4096, 14336, 4096, 8, 2
     inp = _inputs(T, N, O, P, E, seed=0)
@@ -108,10 +127,11 @@ def test_moe_full_size_sampled_tokens(cuda_lib):
                                     "gelu_tanh", "none", routing=True)
     cuda_lib.check()
     _check_routing(r, inp.logits, k, E)
-    tokens = [0, 1, 4095, 8191, 1234, 7000]
-    _assert_close(Y[tokens].float().cpu().numpy(), _oracle_y(inp, k, "gelu_tanh", "none", tokens=tokens),
-                  "moe full size")
     assert torch.isfinite(Y.float()).all()
+    tokens, tail = _full_size_tokens(r, T, k, 56, seed=1)
+    assert len(tokens) >= 64 and len(tail) >= E
+    parity.assert_close(Y[tokens].float().cpu().numpy(), _oracle_tokens(inp, k, "gelu_tanh", "none", tokens),
+                        "moe full size")
 
 
 @pytest.mark.parametrize("router", ["balanced", "moderate", "stress"])
@@ -147,6 +167,6 @@ def test_moe_full_size_stress_skew_sampled_tokens(cuda_lib):
     _check_routing(r, inp.logits, k, E)
     offs = r["expert_offsets"].cpu().numpy()
     assert offs[1] - offs[0] > 0.95 * T
-    tokens = [0, 3, 4096, 8191]
-    _assert_close(Y[tokens].float().cpu().numpy(), _oracle_y(inp, k, "gelu_tanh", "none", tokens=tokens),
-                  "moe stress full size")
+    tokens, _ = _full_size_tokens(r, T, k, 24, seed=2)
+    parity.assert_close(Y[tokens].float().cpu().numpy(), _oracle_tokens(inp, k, "gelu_tanh", "none", tokens),
+                        "moe stress full size")

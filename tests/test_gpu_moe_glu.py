@@ -6,6 +6,7 @@ import pytest
 import torch
 
 import oracle
+import parity
 from transformer_ffn_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -57,8 +58,17 @@ def test_moe_glu_full_size_sampled_tokens(cuda_lib):
     # Mixtral-class expert layer: T 8192, N 4096, 8 experts of O 14336, P 4096, top-2, SwiGLU
     T, N, O, P, E, k = 8192, 4096, 14336, 4096, 8, 2
     inp = synth.moe_glu_inputs(T, N, O, P, E, seed=0, device="cuda")
-    Y = cuda_lib.moe_glu_forward(inp.X, inp.logits, k, inp.W1, inp.W3, inp.W2, "silu")
+    Y, r = cuda_lib.moe_glu_forward(inp.X, inp.logits, k, inp.W1, inp.W3, inp.W2, "silu", routing=True)
     cuda_lib.check()
-    tokens = [0, 2048, 8191]
-    _assert_close(Y[tokens].float().cpu().numpy(), _oracle(inp, k, "silu", tokens=tokens), "moe glu full size")
     assert torch.isfinite(Y.float()).all()
+    # tokens in every expert's zero-padded last band, plus random ones
+    tail = parity.moe_tail_tokens(r["perm"].cpu().numpy(), r["expert_offsets"].cpu().numpy(), k)
+    rng = np.random.default_rng(3)
+    tokens = sorted(set([0, T - 1] + tail + rng.choice(T, size=48, replace=False).tolist()))
+    assert len(tokens) >= 64
+    u = synth.to_u16
+    host = (u(inp.X), inp.logits.cpu().numpy(), [u(w) for w in inp.W1], [u(w) for w in inp.W3],
+            [u(w) for w in inp.W2])
+    want = parity.oracle_rows(lambda t: oracle.moe_glu_ffn(*host[:2], k, *host[2:], oracle.ACT_SILU, tokens=t),
+                              tokens)
+    parity.assert_close(Y[tokens].float().cpu().numpy(), want, "moe glu full size")

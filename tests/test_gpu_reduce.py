@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+import parity
 from transformer_ffn_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -71,15 +72,18 @@ def test_reduce_form_agrees_with_engine(reduce_path):
     assert torch.all(d <= 2e-2 + 2e-2 * e.float().abs())
 
 
-def test_reduce_form_full_size_sampled_rows(reduce_path):
+def test_reduce_form_full_size_band_rows(reduce_path):
     # the prefill workload: M 4096, N 4096, O 16384, P 4096, GELU-tanh
     M, N, O, P = 4096, 4096, 16384, 4096
     inp = synth.ffn_inputs(M, N, O, P, seed=0, device="cuda")
     Y = reduce_path.ffn_forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh", "none")
     reduce_path.check()
-    rows = [0, 255, 2048, 4095]
-    _assert_close(Y[rows].float().cpu().numpy(), _oracle(inp, ("gelu_tanh", "none"), rows=rows), "full size")
     assert torch.isfinite(Y.float()).all()
+    rows = parity.band_rows(M)
+    u = synth.to_u16
+    host = (u(inp.X), u(inp.W1), u(inp.b1), u(inp.W2), u(inp.b2))
+    want = parity.oracle_rows(lambda r: oracle.ffn(*host, oracle.ACT_GELU_TANH, oracle.ACT_NONE, rows=r), rows)
+    parity.assert_close(Y[rows].float().cpu().numpy(), want, "full size")
 
 
 # ------------------------------------------------- back-to-back form (path 5)
@@ -121,12 +125,15 @@ def test_b2b_form_deterministic_and_close_to_engine(b2b_path):
     assert torch.all(d <= 2e-2 + 2e-2 * e.float().abs())
 
 
-def test_b2b_form_full_size_sampled_rows(b2b_path):
+def test_b2b_form_full_size_band_rows(b2b_path):
     # the prefill workload through the back-to-back form (H recomputed for each
     # of the 16 Y tiles of a band): slow, but exact
     M, N, O, P = 4096, 4096, 16384, 4096
     inp = synth.ffn_inputs(M, N, O, P, seed=0, device="cuda")
     Y = b2b_path.ffn_forward(inp.X, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh", "none")
     b2b_path.check()
-    rows = [1, 1000, 4095]
-    _assert_close(Y[rows].float().cpu().numpy(), _oracle(inp, ("gelu_tanh", "none"), rows=rows), "b2b full size")
+    rows = parity.band_rows(M)
+    u = synth.to_u16
+    host = (u(inp.X), u(inp.W1), u(inp.b1), u(inp.W2), u(inp.b2))
+    want = parity.oracle_rows(lambda r: oracle.ffn(*host, oracle.ACT_GELU_TANH, oracle.ACT_NONE, rows=r), rows)
+    parity.assert_close(Y[rows].float().cpu().numpy(), want, "b2b full size")

@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+import parity
 from transformer_ffn_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -152,21 +153,24 @@ def test_stream_rows_past_its_limit_run_the_engine(cuda_lib):
 
 
 @pytest.mark.parametrize("M", [128, 256])
-def test_stream_llama3_8b_sampled_rows(cuda_lib, M):
+def test_stream_llama3_8b_all_rows(cuda_lib, M):
     # batched decode of the Llama 3 8B FFN shape (dense form, GELU)
     N, O, P = 4096, 14336, 4096
     inp = synth.ffn_inputs(M, N, O, P, seed=0, device="cuda")
     Y = _dense(cuda_lib, inp, "gelu_tanh", "none")
-    rows = sorted({0, M - 1, M // 3, (2 * M) // 3, 17})
-    _assert_close(Y[rows].float().cpu().numpy(), _dense_oracle(inp, "gelu_tanh", "none", rows=rows), f"8B M={M}")
-    assert torch.isfinite(Y.float()).all()
+    u = synth.to_u16
+    host = (u(inp.X), u(inp.W1), u(inp.b1), u(inp.W2), u(inp.b2))
+    want = parity.oracle_rows(
+        lambda r: oracle.ffn(*host, oracle.ACT_GELU_TANH, oracle.ACT_NONE, rows=r), range(M))
+    parity.assert_close(Y.float().cpu().numpy(), want, f"8B M={M}")
 
 
 @pytest.mark.parametrize("M", [128, 256])
-def test_stream_swiglu_llama3_8b_sampled_rows(cuda_lib, M):
+def test_stream_swiglu_llama3_8b_all_rows(cuda_lib, M):
     N, O, P = 4096, 14336, 4096
     g = synth.glu_inputs(M, N, O, P, seed=0, device="cuda")
     Y = _glu(cuda_lib, g, "silu")
-    rows = sorted({0, 5, 63, M // 2 + 7, M - 1})
-    _assert_close(Y[rows].float().cpu().numpy(), _glu_oracle(g, "silu", rows=rows), f"SwiGLU 8B M={M}")
-    assert torch.isfinite(Y.float()).all()
+    u = synth.to_u16
+    host = (u(g.X), u(g.W1), u(g.W3), u(g.W2))
+    want = parity.oracle_rows(lambda r: oracle.glu_ffn(*host, oracle.ACT_SILU, rows=r), range(M))
+    parity.assert_close(Y.float().cpu().numpy(), want, f"SwiGLU 8B M={M}")

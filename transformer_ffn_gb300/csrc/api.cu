@@ -382,6 +382,11 @@ void fill_layer(engine::LayerArgs& la, int64_t K, int64_t ncols, int act, int ou
 
 }  // namespace
 
+namespace tffn {
+uint64_t option_wait_limit_ns() { return wait_limit_ns(); }
+int32_t option_skip_flag() { return static_cast<int32_t>(g_opt_skip.load()); }
+}  // namespace tffn
+
 // The weight-streaming decode launch (dense, or gated when W3 is given).
 static int run_decode(DeviceState& d, uint8_t* base, const DenseLayout& L, const void* X, const void* W1,
                       const void* W3, const void* b1, const void* W2, const void* b2, int act1, int act2, int64_t M,
@@ -410,6 +415,7 @@ static int run_decode(DeviceState& d, uint8_t* base, const DenseLayout& L, const
     p.act1 = act1;
     p.act2 = act2;
     p.glu = glu ? 1 : 0;
+    p.skip_slice = glu ? -1 : static_cast<int32_t>(g_opt_skip.load());
     p.wait_limit_ns = wait_limit_ns();
     p.plan = decode::make_plan(M, N, O, P, d.sms, glu);
     if (static_cast<size_t>(p.plan.slices[0]) * 4 > FLAG_WORDS ||

@@ -364,7 +364,7 @@ __device__ bool flush(const Params& p, const WaitCtx& w, int layer, int64_t slic
         // the call's epoch (release, gpu scope).
         ptx::fence_proxy_async_global();
         __syncwarp();   // the warp's stores, then one release by lane 0
-        if (lane == 0)
+        if (lane == 0 && slice != p.skip_slice)
             ptx::st_release_gpu(p.flags + slice * CONSUMER_WARPS + cw, epoch);
     }
     return true;

@@ -174,6 +174,8 @@ struct Params {
     int32_t M, N, O, P;
     int32_t act1, act2;
     int32_t glu;               // 1: layer 1 is gated (no biases)
+    int32_t skip_slice;        // test fault injection: this dense layer-1 slice's H flags are
+                               // never published (-1 = off); its readers then time out
     uint64_t wait_limit_ns;
     Plan plan;
 };

@@ -23,6 +23,12 @@ struct Params;
 
 constexpr int MOE_MAX_E = 64;
 
+// Process-wide options shared by every entry point (tffn_set_option):
+// the device wait limit in nanoseconds and the test fault-injection index
+// (-1 = off).
+uint64_t option_wait_limit_ns();
+int32_t option_skip_flag();
+
 // The engine launches clusters of two CTAs; max_pairs caps the number of CTA
 // pairs (further capped by how many pairs can be resident at once).
 int launch_engine_dense(const engine::Params<1>& p, int max_pairs, cudaStream_t s);

@@ -147,7 +147,8 @@ extern "C" int ffn_forward_decode_noalloc(const void* X, const void* W1, const v
     p.P = static_cast<int32_t>(P);
     p.act1 = act1;
     p.act2 = act2;   // flags and epoch were just cleared: the kernel uses epoch 1
-    p.wait_limit_ns = 4000ull * 1000000ull;
+    p.skip_slice = option_skip_flag();
+    p.wait_limit_ns = option_wait_limit_ns();
     const uint32_t arows = M <= 16 ? 16u : 32u;
     if (map2d(&p.map_w[0], W1, O, N, 64, decode::KC) || map2d(&p.map_w[1], W2, P, O, 64, decode::KC) ||
         map2d(&p.map_a[0], X, N, M, 64, arows) || map2d(&p.map_a[1], p.H, O, M, 64, arows))
@@ -155,4 +156,31 @@ extern "C" int ffn_forward_decode_noalloc(const void* X, const void* W1, const v
     if (launch_decode(p, p.plan.grid, s) != 0)
         return TFFN_ERR_CUDA;
     return TFFN_OK;
+}
+
+extern "C" int tffn_check_noalloc(struct CUstream_st* stream, int32_t* detail)
+{
+    if (detail)
+        detail[0] = detail[1] = detail[2] = detail[3] = 0;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TFFN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return TFFN_ERR_CUDA;
+    const NoallocDevice& d = g_noalloc_dev[dev];
+    if (!d.ready)
+        return TFFN_OK;   // no call has run on this device
+    // The first four words of the control block: {status, wait site, block, info}.
+    uint32_t rec[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(rec, d.scratch, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TFFN_ERR_CUDA;
+    if (detail)
+        for (int i = 0; i < 4; ++i)
+            detail[i] = static_cast<int32_t>(rec[i]);
+    if (rec[0] == 0)
+        return TFFN_OK;
+    if (cudaMemset(d.scratch, 0, sizeof(rec)) != cudaSuccess)
+        return TFFN_ERR_CUDA;
+    return static_cast<int32_t>(rec[0]) == TFFN_ERR_TIMEOUT ? TFFN_ERR_TIMEOUT : TFFN_ERR_DEVICE;
 }
