@@ -76,3 +76,15 @@ def moe_tail_tokens(perm, offsets, k, band=256, per_expert=2):
         for j in picks:
             toks.append(int(perm[offsets[e] + j]) // k)
     return sorted(set(toks))
+
+
+def with_random(chosen, total, n, seed):
+    """The chosen indices plus distinct random ones from [0, total) until
+    there are n (or all of them), sorted."""
+    out = set(int(x) for x in chosen)
+    rng = np.random.default_rng(seed)
+    for x in rng.permutation(total):
+        if len(out) >= min(n, total):
+            break
+        out.add(int(x))
+    return sorted(out)

@@ -110,13 +110,12 @@ def _oracle_tokens(inp, k, act1, act2, tokens):
                               tokens)
 
 
-def _full_size_tokens(r, T, k, n_random, seed):
-    """Tokens to compare at full size: the first and last, tokens whose grouped
-    row lies in an expert's zero-padded last band, and random ones."""
+def _full_size_tokens(r, T, k, n, seed):
+    """n or more tokens to compare at full size: the first and last, tokens
+    whose grouped row lies in an expert's zero-padded last band, and random
+    ones."""
     tail = parity.moe_tail_tokens(r["perm"].cpu().numpy(), r["expert_offsets"].cpu().numpy(), k)
-    rng = np.random.default_rng(seed)
-    rand = rng.choice(T, size=n_random, replace=False).tolist()
-    return sorted(set([0, T - 1] + tail + rand)), tail
+    return parity.with_random(set([0, T - 1] + tail), T, n, seed=seed), tail
 
 
 def test_moe_full_size_tokens(cuda_lib):
@@ -128,7 +127,7 @@ def test_moe_full_size_tokens(cuda_lib):
     cuda_lib.check()
     _check_routing(r, inp.logits, k, E)
     assert torch.isfinite(Y.float()).all()
-    tokens, tail = _full_size_tokens(r, T, k, 56, seed=1)
+    tokens, tail = _full_size_tokens(r, T, k, 64, seed=1)
     assert len(tokens) >= 64 and len(tail) >= E
     parity.assert_close(Y[tokens].float().cpu().numpy(), _oracle_tokens(inp, k, "gelu_tanh", "none", tokens),
                         "moe full size")
@@ -167,6 +166,6 @@ def test_moe_full_size_stress_skew_sampled_tokens(cuda_lib):
     _check_routing(r, inp.logits, k, E)
     offs = r["expert_offsets"].cpu().numpy()
     assert offs[1] - offs[0] > 0.95 * T
-    tokens, _ = _full_size_tokens(r, T, k, 24, seed=2)
+    tokens, _ = _full_size_tokens(r, T, k, 32, seed=2)
     parity.assert_close(Y[tokens].float().cpu().numpy(), _oracle_tokens(inp, k, "gelu_tanh", "none", tokens),
                         "moe stress full size")

@@ -63,9 +63,7 @@ def test_moe_glu_full_size_sampled_tokens(cuda_lib):
     assert torch.isfinite(Y.float()).all()
     # tokens in every expert's zero-padded last band, plus random ones
     tail = parity.moe_tail_tokens(r["perm"].cpu().numpy(), r["expert_offsets"].cpu().numpy(), k)
-    rng = np.random.default_rng(3)
-    tokens = sorted(set([0, T - 1] + tail + rng.choice(T, size=48, replace=False).tolist()))
-    assert len(tokens) >= 64
+    tokens = parity.with_random(set([0, T - 1] + tail), T, 64, seed=3)
     u = synth.to_u16
     host = (u(inp.X), inp.logits.cpu().numpy(), [u(w) for w in inp.W1], [u(w) for w in inp.W3],
             [u(w) for w in inp.W2])

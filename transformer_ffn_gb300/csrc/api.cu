@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -46,6 +47,51 @@ constexpr int64_t STREAM_MAX_M = 128;  // then the tensor-core weight stream, th
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// ------------------------------------------------------ launch-parameter cache
+// A forward call's kernel parameters -- the encoded tensor maps (a driver call
+// each, a few microseconds together) and the work plan -- depend only on the
+// call's pointers, shapes, activations, resolved path and workspace base.  The
+// last few distinct calls per kind and device are kept; a repeated call (the
+// same layer in a serving loop) launches from the cached copy after
+// refreshing the fields that follow the process-wide options.  Tensor maps
+// hold addresses and shapes only, so a cached entry stays valid whatever the
+// tensors contain.
+struct CallKey {
+    int32_t kind = 0, path = 0, act1 = 0, act2 = 0;
+    int64_t dims[6] = {0, 0, 0, 0, 0, 0};
+    std::vector<const void*> ptrs;
+    bool operator==(const CallKey& o) const
+    {
+        return kind == o.kind && path == o.path && act1 == o.act1 && act2 == o.act2 &&
+               std::memcmp(dims, o.dims, sizeof(dims)) == 0 && ptrs == o.ptrs;
+    }
+};
+
+template <class P>
+struct ParamCache {
+    static constexpr int SLOTS = 4;
+    CallKey key[SLOTS];
+    std::unique_ptr<P> params[SLOTS];
+    int next = 0;
+    P* find(const CallKey& k)
+    {
+        for (int i = 0; i < SLOTS; ++i)
+            if (params[i] && key[i] == k)
+                return params[i].get();
+        return nullptr;
+    }
+    P* store(const CallKey& k, const P& p)
+    {
+        const int i = next;
+        next = (next + 1) % SLOTS;
+        key[i] = k;
+        if (!params[i])
+            params[i].reset(new P);
+        std::memcpy(static_cast<void*>(params[i].get()), &p, sizeof(P));
+        return params[i].get();
+    }
+};
+
 struct DeviceState {
     bool init = false;
     int sms = 0;
@@ -56,6 +102,10 @@ struct DeviceState {
     bool user_set = false;
     bool needs_reset = true;
     uint32_t launches = 0;   // flag-using launches since the flag region was cleared
+    ParamCache<decode::Params> decode_cache;
+    ParamCache<wstream::Params> wstream_cache;
+    ParamCache<engine::Params<1>> engine_cache;
+    ParamCache<engine::Params<MOE_MAX_E>> moe_cache;
 };
 
 std::mutex g_mu;
@@ -387,6 +437,25 @@ uint64_t option_wait_limit_ns() { return wait_limit_ns(); }
 int32_t option_skip_flag() { return static_cast<int32_t>(g_opt_skip.load()); }
 }  // namespace tffn
 
+// Key of a dense-FFN call: everything its kernel parameters depend on.
+static CallKey dense_key(int kind, int path, const void* X, const void* W1, const void* W3, const void* b1,
+                         const void* W2, const void* b2, void* Y, const uint8_t* base, int act1, int act2,
+                         int64_t M, int64_t N, int64_t O, int64_t P, int sms)
+{
+    CallKey k;
+    k.kind = kind;
+    k.path = path;
+    k.act1 = act1;
+    k.act2 = act2;
+    k.dims[0] = M;
+    k.dims[1] = N;
+    k.dims[2] = O;
+    k.dims[3] = P;
+    k.dims[4] = sms;
+    k.ptrs = {X, W1, W3, b1, W2, b2, Y, base};
+    return k;
+}
+
 // The weight-streaming decode launch (dense, or gated when W3 is given).
 static int run_decode(DeviceState& d, uint8_t* base, const DenseLayout& L, const void* X, const void* W1,
                       const void* W3, const void* b1, const void* W2, const void* b2, int act1, int act2, int64_t M,
@@ -396,48 +465,54 @@ static int run_decode(DeviceState& d, uint8_t* base, const DenseLayout& L, const
     if (rc != TFFN_OK)
         return rc;
     const bool glu = W3 != nullptr;
-    decode::Params p{};
-    p.X = static_cast<const __nv_bfloat16*>(X);
-    p.W1 = static_cast<const __nv_bfloat16*>(W1);
-    p.b1 = static_cast<const __nv_bfloat16*>(b1);
-    p.W2 = static_cast<const __nv_bfloat16*>(W2);
-    p.b2 = static_cast<const __nv_bfloat16*>(b2);
-    p.Y = static_cast<__nv_bfloat16*>(Y);
-    p.H = reinterpret_cast<__nv_bfloat16*>(base + L.off_h);
-    p.partial = reinterpret_cast<float*>(base + L.off_part);
-    p.counters = reinterpret_cast<uint32_t*>(base + OFF_DCOUNT);
-    p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
-    p.ctrl = reinterpret_cast<DevCtrl*>(base);
-    p.M = static_cast<int32_t>(M);
-    p.N = static_cast<int32_t>(N);
-    p.O = static_cast<int32_t>(O);
-    p.P = static_cast<int32_t>(P);
-    p.act1 = act1;
-    p.act2 = act2;
-    p.glu = glu ? 1 : 0;
-    p.skip_slice = glu ? -1 : static_cast<int32_t>(g_opt_skip.load());
-    p.wait_limit_ns = wait_limit_ns();
-    p.plan = decode::make_plan(M, N, O, P, d.sms, glu);
-    if (static_cast<size_t>(p.plan.slices[0]) * 4 > FLAG_WORDS ||
-        (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * 4 > DCOUNT_WORDS)
-        return TFFN_ERR_UNSUPPORTED;
-    const uint32_t arows = M <= 16 ? 16u : static_cast<uint32_t>(decode::decode_rows(M));
-    // Gated layer 1 loads 64-column boxes of W1 and W3 (128 B per row) whose
-    // neighbours belong to other units: no promotion past 128 B, or every
-    // weight row would be fetched twice.
-    const CUtensorMapL2promotion w1_promo =
-        glu ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
-    // the gated window reads 128 adjacent columns of W1 and of W3 per row
-    // (two boxes each): 256-byte promotion, boxes of KC1 rows
-    const uint32_t w1_rows = p.plan.win ? static_cast<uint32_t>(decode::KC1) : static_cast<uint32_t>(decode::KC);
-    const CUtensorMapL2promotion w1p = p.plan.win ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : w1_promo;
-    if (make_map(&p.map_w[0], W1, O, N, 64, w1_rows, w1p) ||
-        make_map(&p.map_w[1], W2, P, O, 64, decode::KC) || make_map(&p.map_a[0], X, N, M, 64, arows) ||
-        make_map(&p.map_a[1], p.H, O, M, 64, arows) ||
-        (glu && make_map(&p.map_w3, W3, O, N, 64, w1_rows, w1p)))
-        return TFFN_ERR_INVALID_ARG;
+    const CallKey key = dense_key(2, L.path, X, W1, W3, b1, W2, b2, Y, base, act1, act2, M, N, O, P, d.sms);
+    decode::Params* cp = d.decode_cache.find(key);
+    if (cp == nullptr) {
+        decode::Params p{};
+        p.X = static_cast<const __nv_bfloat16*>(X);
+        p.W1 = static_cast<const __nv_bfloat16*>(W1);
+        p.b1 = static_cast<const __nv_bfloat16*>(b1);
+        p.W2 = static_cast<const __nv_bfloat16*>(W2);
+        p.b2 = static_cast<const __nv_bfloat16*>(b2);
+        p.Y = static_cast<__nv_bfloat16*>(Y);
+        p.H = reinterpret_cast<__nv_bfloat16*>(base + L.off_h);
+        p.partial = reinterpret_cast<float*>(base + L.off_part);
+        p.counters = reinterpret_cast<uint32_t*>(base + OFF_DCOUNT);
+        p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+        p.ctrl = reinterpret_cast<DevCtrl*>(base);
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.O = static_cast<int32_t>(O);
+        p.P = static_cast<int32_t>(P);
+        p.act1 = act1;
+        p.act2 = act2;
+        p.glu = glu ? 1 : 0;
+        p.plan = decode::make_plan(M, N, O, P, d.sms, glu);
+        if (static_cast<size_t>(p.plan.slices[0]) * 4 > FLAG_WORDS ||
+            (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * 4 > DCOUNT_WORDS)
+            return TFFN_ERR_UNSUPPORTED;
+        const uint32_t arows = M <= 16 ? 16u : static_cast<uint32_t>(decode::decode_rows(M));
+        // Gated layer 1 loads 64-column boxes of W1 and W3 (128 B per row) whose
+        // neighbours belong to other units: no promotion past 128 B, or every
+        // weight row would be fetched twice.
+        const CUtensorMapL2promotion w1_promo =
+            glu ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+        // the gated window reads 128 adjacent columns of W1 and of W3 per row
+        // (two boxes each): 256-byte promotion, boxes of KC1 rows
+        const uint32_t w1_rows =
+            p.plan.win ? static_cast<uint32_t>(decode::KC1) : static_cast<uint32_t>(decode::KC);
+        const CUtensorMapL2promotion w1p = p.plan.win ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : w1_promo;
+        if (make_map(&p.map_w[0], W1, O, N, 64, w1_rows, w1p) ||
+            make_map(&p.map_w[1], W2, P, O, 64, decode::KC) || make_map(&p.map_a[0], X, N, M, 64, arows) ||
+            make_map(&p.map_a[1], p.H, O, M, 64, arows) ||
+            (glu && make_map(&p.map_w3, W3, O, N, 64, w1_rows, w1p)))
+            return TFFN_ERR_INVALID_ARG;
+        cp = d.decode_cache.store(key, p);
+    }
+    cp->skip_slice = glu ? -1 : static_cast<int32_t>(g_opt_skip.load());
+    cp->wait_limit_ns = wait_limit_ns();
     timing_start(s);
-    if (launch_decode(p, p.plan.grid, s) != 0)
+    if (launch_decode(*cp, cp->plan.grid, s) != 0)
         return TFFN_ERR_CUDA;
     timing_stop(s);
     g_last_launches = 1;
@@ -453,36 +528,41 @@ static int run_wstream(DeviceState& d, uint8_t* base, const DenseLayout& L, cons
     if (rc != TFFN_OK)
         return rc;
     const bool glu = W3 != nullptr;
-    wstream::Params p{};
-    p.b1 = static_cast<const __nv_bfloat16*>(b1);
-    p.b2 = static_cast<const __nv_bfloat16*>(b2);
-    p.Y = static_cast<__nv_bfloat16*>(Y);
-    p.H = reinterpret_cast<__nv_bfloat16*>(base + L.off_h);
-    p.partial = reinterpret_cast<float*>(base + L.off_part);
-    p.counters = reinterpret_cast<uint32_t*>(base + OFF_DCOUNT);
-    p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
-    p.ctrl = reinterpret_cast<DevCtrl*>(base);
-    p.M = static_cast<int32_t>(M);
-    p.N = static_cast<int32_t>(N);
-    p.O = static_cast<int32_t>(O);
-    p.P = static_cast<int32_t>(P);
-    p.act1 = act1;
-    p.act2 = act2;
-    p.glu = glu ? 1 : 0;
-    p.wait_limit_ns = wait_limit_ns();
-    p.plan = wstream::make_plan(M, N, O, P, d.sms, glu);
-    const size_t flag_words = p.plan.win ? static_cast<size_t>(p.plan.nblk) * 2
-                                         : static_cast<size_t>(p.plan.slices[0]) * wstream::EPI_WARPS;
-    if (flag_words > FLAG_WORDS ||
-        2 * (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * wstream::EPI_WARPS > DCOUNT_WORDS)
-        return TFFN_ERR_UNSUPPORTED;
-    const uint32_t rows = static_cast<uint32_t>(p.plan.rows);
-    if (make_map(&p.map_w[0], W1, O, N, 64, wstream::KC) || make_map(&p.map_w[1], W2, P, O, 64, wstream::KC) ||
-        make_map(&p.map_x[0], X, N, M, 64, rows) || make_map(&p.map_x[1], p.H, O, M, 64, rows) ||
-        (glu && make_map(&p.map_w3, W3, O, N, 64, wstream::KC)))
-        return TFFN_ERR_INVALID_ARG;
+    const CallKey key = dense_key(6, L.path, X, W1, W3, b1, W2, b2, Y, base, act1, act2, M, N, O, P, d.sms);
+    wstream::Params* cp = d.wstream_cache.find(key);
+    if (cp == nullptr) {
+        wstream::Params p{};
+        p.b1 = static_cast<const __nv_bfloat16*>(b1);
+        p.b2 = static_cast<const __nv_bfloat16*>(b2);
+        p.Y = static_cast<__nv_bfloat16*>(Y);
+        p.H = reinterpret_cast<__nv_bfloat16*>(base + L.off_h);
+        p.partial = reinterpret_cast<float*>(base + L.off_part);
+        p.counters = reinterpret_cast<uint32_t*>(base + OFF_DCOUNT);
+        p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+        p.ctrl = reinterpret_cast<DevCtrl*>(base);
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.O = static_cast<int32_t>(O);
+        p.P = static_cast<int32_t>(P);
+        p.act1 = act1;
+        p.act2 = act2;
+        p.glu = glu ? 1 : 0;
+        p.plan = wstream::make_plan(M, N, O, P, d.sms, glu);
+        const size_t flag_words = p.plan.win ? static_cast<size_t>(p.plan.nblk) * 2
+                                             : static_cast<size_t>(p.plan.slices[0]) * wstream::EPI_WARPS;
+        if (flag_words > FLAG_WORDS ||
+            2 * (static_cast<size_t>(p.plan.slices[0]) + p.plan.slices[1]) * wstream::EPI_WARPS > DCOUNT_WORDS)
+            return TFFN_ERR_UNSUPPORTED;
+        const uint32_t rows = static_cast<uint32_t>(p.plan.rows);
+        if (make_map(&p.map_w[0], W1, O, N, 64, wstream::KC) || make_map(&p.map_w[1], W2, P, O, 64, wstream::KC) ||
+            make_map(&p.map_x[0], X, N, M, 64, rows) || make_map(&p.map_x[1], p.H, O, M, 64, rows) ||
+            (glu && make_map(&p.map_w3, W3, O, N, 64, wstream::KC)))
+            return TFFN_ERR_INVALID_ARG;
+        cp = d.wstream_cache.store(key, p);
+    }
+    cp->wait_limit_ns = wait_limit_ns();
     timing_start(s);
-    if (launch_wstream(p, s) != 0)
+    if (launch_wstream(*cp, s) != 0)
         return TFFN_ERR_CUDA;
     timing_stop(s);
     g_last_launches = 1;
@@ -621,21 +701,26 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
         return TFFN_OK;
     }
 
-    engine::Params<1> p;
-    std::memset(&p, 0, sizeof(p));
-    void* H = base + L.off_h;
-    const int64_t rows_h = L.m_blocks * engine::BM;
-    const bool b3d = (O % 64 == 0) && (P % 64 == 0);
-    if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) || make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) ||
-        make_map_b(&p.map_b[0][0], W1, O, N, b3d) || make_map_b(&p.map_b[1][0], W2, P, O, b3d))
-        return TFFN_ERR_INVALID_ARG;
-    p.b3d = b3d ? 1 : 0;
-    p.bias[0][0] = static_cast<const __nv_bfloat16*>(b1);
-    p.bias[1][0] = static_cast<const __nv_bfloat16*>(b2);
-    fill_layer<1>(p.layer[0], N, O, act1, 0, rows_h, H);
-    fill_layer<1>(p.layer[1], O, P, act2, 0, M, Y);
-
-    return run_dense_engine(*d, base, L, p, s);
+    const CallKey key = dense_key(1, L.path, X, W1, nullptr, b1, W2, b2, Y, base, act1, act2, M, N, O, P, d->sms);
+    engine::Params<1>* cp = d->engine_cache.find(key);
+    if (cp == nullptr) {
+        engine::Params<1> p;
+        std::memset(&p, 0, sizeof(p));
+        void* H = base + L.off_h;
+        const int64_t rows_h = L.m_blocks * engine::BM;
+        const bool b3d = (O % 64 == 0) && (P % 64 == 0);
+        if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) ||
+            make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) || make_map_b(&p.map_b[0][0], W1, O, N, b3d) ||
+            make_map_b(&p.map_b[1][0], W2, P, O, b3d))
+            return TFFN_ERR_INVALID_ARG;
+        p.b3d = b3d ? 1 : 0;
+        p.bias[0][0] = static_cast<const __nv_bfloat16*>(b1);
+        p.bias[1][0] = static_cast<const __nv_bfloat16*>(b2);
+        fill_layer<1>(p.layer[0], N, O, act1, 0, rows_h, H);
+        fill_layer<1>(p.layer[1], O, P, act2, 0, M, Y);
+        cp = d->engine_cache.store(key, p);
+    }
+    return run_dense_engine(*d, base, L, *cp, s);
 }
 
 int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W2, int act, int64_t M, int64_t N,
@@ -667,20 +752,26 @@ int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W
     if (L.path == 6)
         return run_wstream(*d, base, L, X, W1, W3, nullptr, W2, nullptr, act, TFFN_ACT_NONE, M, N, O, P, Y, s);
 
-    engine::Params<1> p;
-    std::memset(&p, 0, sizeof(p));
-    void* H = base + L.off_h;
-    const int64_t rows_h = L.m_blocks * engine::BM;
-    const bool b3d = (O % 64 == 0) && (P % 64 == 0);
-    if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) || make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) ||
-        make_map_b(&p.map_b[0][0], W1, O, N, b3d) || make_map_b(&p.map_b_lin[0], W3, O, N, b3d) ||
-        make_map_b(&p.map_b[1][0], W2, P, O, b3d))
-        return TFFN_ERR_INVALID_ARG;
-    p.b3d = b3d ? 1 : 0;
-    p.glu = 1;
-    fill_layer<1>(p.layer[0], N, O, act, 0, rows_h, H);
-    fill_layer<1>(p.layer[1], O, P, TFFN_ACT_NONE, 0, M, Y);
-    return run_dense_engine(*d, base, L, p, s);
+    const CallKey key =
+        dense_key(11, L.path, X, W1, W3, nullptr, W2, nullptr, Y, base, act, TFFN_ACT_NONE, M, N, O, P, d->sms);
+    engine::Params<1>* cp = d->engine_cache.find(key);
+    if (cp == nullptr) {
+        engine::Params<1> p;
+        std::memset(&p, 0, sizeof(p));
+        void* H = base + L.off_h;
+        const int64_t rows_h = L.m_blocks * engine::BM;
+        const bool b3d = (O % 64 == 0) && (P % 64 == 0);
+        if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) ||
+            make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) || make_map_b(&p.map_b[0][0], W1, O, N, b3d) ||
+            make_map_b(&p.map_b_lin[0], W3, O, N, b3d) || make_map_b(&p.map_b[1][0], W2, P, O, b3d))
+            return TFFN_ERR_INVALID_ARG;
+        p.b3d = b3d ? 1 : 0;
+        p.glu = 1;
+        fill_layer<1>(p.layer[0], N, O, act, 0, rows_h, H);
+        fill_layer<1>(p.layer[1], O, P, TFFN_ACT_NONE, 0, M, Y);
+        cp = d->engine_cache.store(key, p);
+    }
+    return run_dense_engine(*d, base, L, *cp, s);
 }
 
 // The MoE forward; W3 (an array of E pointers) non-null: gated experts.
@@ -743,36 +834,59 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
     void* H = base + L.off_h;
     float* Yp = reinterpret_cast<float*>(base + L.off_yp);
 
-    engine::Params<MOE_MAX_E>* pp = new engine::Params<MOE_MAX_E>;
-    std::memset(pp, 0, sizeof(*pp));
-    engine::Params<MOE_MAX_E>& p = *pp;
-    int bad = make_map(&p.map_a[0], Xp, N, L.Rmax, 64, engine::BM_CTA) |
-              make_map(&p.map_a[1], H, O, L.Rmax, 64, engine::BM_CTA);
-    const bool b3d = (O % 64 == 0) && (P % 64 == 0);
-    p.b3d = b3d ? 1 : 0;
-    for (int e = 0; e < E && !bad; ++e) {
-        bad |= make_map_b(&p.map_b[0][e], W1[e], O, N, b3d);
-        bad |= make_map_b(&p.map_b[1][e], W2[e], P, O, b3d);
-        if (glu)
-            bad |= make_map_b(&p.map_b_lin[e], W3[e], O, N, b3d);
-        p.bias[0][e] = b1 ? static_cast<const __nv_bfloat16*>(b1[e]) : nullptr;
-        p.bias[1][e] = b2 ? static_cast<const __nv_bfloat16*>(b2[e]) : nullptr;
+    CallKey key;
+    key.kind = glu ? 65 : 64;
+    key.act1 = act1;
+    key.act2 = act2;
+    key.dims[0] = T;
+    key.dims[1] = N;
+    key.dims[2] = O;
+    key.dims[3] = P;
+    key.dims[4] = E;
+    key.dims[5] = top_k;
+    key.ptrs.reserve(2 + 5 * static_cast<size_t>(E));
+    key.ptrs.push_back(base);
+    key.ptrs.push_back(Y);
+    for (int e = 0; e < E; ++e) {
+        key.ptrs.push_back(W1[e]);
+        key.ptrs.push_back(W2[e]);
+        key.ptrs.push_back(glu ? W3[e] : nullptr);
+        key.ptrs.push_back(b1 ? b1[e] : nullptr);
+        key.ptrs.push_back(b2 ? b2[e] : nullptr);
     }
-    if (bad) {
-        delete pp;
-        return TFFN_ERR_INVALID_ARG;
+    engine::Params<MOE_MAX_E>* cp = d->moe_cache.find(key);
+    if (cp == nullptr) {
+        std::unique_ptr<engine::Params<MOE_MAX_E>> pp(new engine::Params<MOE_MAX_E>);
+        std::memset(static_cast<void*>(pp.get()), 0, sizeof(*pp));
+        engine::Params<MOE_MAX_E>& p = *pp;
+        int bad = make_map(&p.map_a[0], Xp, N, L.Rmax, 64, engine::BM_CTA) |
+                  make_map(&p.map_a[1], H, O, L.Rmax, 64, engine::BM_CTA);
+        const bool b3d = (O % 64 == 0) && (P % 64 == 0);
+        p.b3d = b3d ? 1 : 0;
+        for (int e = 0; e < E && !bad; ++e) {
+            bad |= make_map_b(&p.map_b[0][e], W1[e], O, N, b3d);
+            bad |= make_map_b(&p.map_b[1][e], W2[e], P, O, b3d);
+            if (glu)
+                bad |= make_map_b(&p.map_b_lin[e], W3[e], O, N, b3d);
+            p.bias[0][e] = b1 ? static_cast<const __nv_bfloat16*>(b1[e]) : nullptr;
+            p.bias[1][e] = b2 ? static_cast<const __nv_bfloat16*>(b2[e]) : nullptr;
+        }
+        if (bad)
+            return TFFN_ERR_INVALID_ARG;
+        fill_layer<MOE_MAX_E>(p.layer[0], N, O, act1, 0, L.Rmax, H);
+        fill_layer<MOE_MAX_E>(p.layer[1], O, P, act2, 1, L.Rmax, Yp);
+        p.layer[0].n_tiles = L.n1;
+        p.glu = glu ? 1 : 0;
+        p.m_blocks = -1;
+        p.m_blocks_dev = nb;
+        p.band_expert = band;
+        p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+        p.ctrl = reinterpret_cast<DevCtrl*>(base);
+        p.mode = MODE_FUSED;
+        cp = d->moe_cache.store(key, p);
     }
-    fill_layer<MOE_MAX_E>(p.layer[0], N, O, act1, 0, L.Rmax, H);
-    fill_layer<MOE_MAX_E>(p.layer[1], O, P, act2, 1, L.Rmax, Yp);
-    p.layer[0].n_tiles = L.n1;
-    p.glu = glu ? 1 : 0;
-    p.m_blocks = -1;
-    p.m_blocks_dev = nb;
-    p.band_expert = band;
-    p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
-    p.ctrl = reinterpret_cast<DevCtrl*>(base);
+    engine::Params<MOE_MAX_E>& p = *cp;
     p.wait_limit_ns = wait_limit_ns();
-    p.mode = MODE_FUSED;
     p.group_m = static_cast<int32_t>(g_opt_group.load() < 1 ? 1 : g_opt_group.load());
     p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
 
@@ -788,7 +902,6 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
         timing_stop(s);
     }
     fail |= launch_moe_combine(Yp, pos, w, T, top_k, P, Y, d->sms * 4, s);
-    delete pp;
     if (fail)
         return TFFN_ERR_CUDA;
     g_last_launches = 6;
