@@ -461,13 +461,24 @@ def l2_policy(cfg, dev):
 
 
 def time_steps(step, steps, flush_buf, stream):
-    """Per-step device time (s) of `steps` steps (flush_buf, if given, is
-    written between them to flush L2)."""
+    """Device time (s) of `steps` steps.  With an L2 flush between steps
+    (flush_buf written outside the step events), each step is bracketed by
+    its own pair of events and the per-step times are returned.  Without one,
+    the steps run back to back between one pair of events (an event record
+    between two kernels serialises them, which would add its own gap to every
+    step) and the list holds the block's mean once per step."""
     import torch
+    if flush_buf is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) / 1e3 / steps] * steps
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in evs:
-        if flush_buf is not None:
-            flush_buf.zero_()
+        flush_buf.zero_()
         a.record(stream)
         step()
         b.record(stream)
@@ -586,6 +597,9 @@ def measure_gpu(name, args, world, rank, local, with_cpu):
     roof["kernel_ms"] = dom_s * 1e3
     roof["algorithmic_per_launch"] = weight_bytes(cfg) if is_hbm_bound(cfg) else flops(cfg)
     roof["traffic"] = recorded_traffic(name, roof["kernel"])
+    if weight_bytes(cfg) < 64e6 and is_hbm_bound(cfg):
+        roof["note"] = ("launch/latency-bound: a step moves only "
+                        f"{weight_bytes(cfg) / 1e6:.1f} MB, so its fraction of HBM is context, not a target")
 
     # ---- end to end through the public API.  Pipelined: every step uploads
     # its input from pinned host memory, runs the FFN and downloads its result,
@@ -599,8 +613,12 @@ def measure_gpu(name, args, world, rank, local, with_cpu):
 
     entry = {
         "workload": cfg["label"], "metric": metric, "value": value, "unit": unit,
-        "ms_per_step": mean_s * 1e3, "ms_per_step_min": min(per_step) * 1e3,
-        "ms_per_step_std": statistics.pstdev(per_step) * 1e3, "steps": args.steps,
+        "ms_per_step": mean_s * 1e3,
+        "ms_per_step_min": min(per_step) * 1e3 if flush_buf is not None else None,
+        "ms_per_step_std": statistics.pstdev(per_step) * 1e3 if flush_buf is not None else None,
+        "timing": ("per-step event pairs, L2 flushed between steps" if flush_buf is not None
+                   else "one event pair around the back-to-back steps"),
+        "steps": args.steps,
         "l2": l2_note, "global_batch": cfg["M"] * world, "flops_per_step": flops(cfg),
         "roofline": roof,
         "e2e": {"value": rate(cfg, e2e_mean) * world, "unit": unit, "h2d_bytes_per_step": h2d,
@@ -654,7 +672,8 @@ def run_gpu(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; X~N(0,1), W~N(0,1/fan_in), b~U(-0.1,0.1), bf16)",
         "config": {"workload": e["workload"], "parallelism": f"replicas{world}" if world > 1 else "single GPU",
-                   "l2": e["l2"], "global_batch": e["global_batch"], "flops_per_step": e["flops_per_step"]},
+                   "l2": e["l2"], "timing": e["timing"], "global_batch": e["global_batch"],
+                   "flops_per_step": e["flops_per_step"]},
         "roofline": e["roofline"], "e2e": e["e2e"], "clocks": e["clocks"], "gpu_launches": e["gpu_launches"],
         "wall_s_timed_block": e["wall_s_timed_block"],
     }
