@@ -265,13 +265,20 @@ const char* tffn_status_string(int status);
  *   TFFN_OPT_MOE_ORDER    order of the experts' row segments in the grouped
  *                         layout: 0 expert index, 1 (default) largest row
  *                         count first.  Results are identical either way.
+ *   TFFN_OPT_MOE_COMBINE  1 (default): the gate-weighted sum of a token's
+ *                         expert outputs is formed in the expert FFN's layer-2
+ *                         epilogue by the last of the token's rows to finish
+ *                         (when T x ceil(P/256) counters fit the workspace's
+ *                         sync region, else as 0); 0: a separate combine
+ *                         kernel.  Results are identical either way.
  * Returns the previous value. */
 enum {
     TFFN_OPT_PATH = 1,
     TFFN_OPT_WAIT_LIMIT_MS = 2,
     TFFN_OPT_SKIP_FLAG = 3,
     TFFN_OPT_GROUP_M = 4,
-    TFFN_OPT_MOE_ORDER = 5
+    TFFN_OPT_MOE_ORDER = 5,
+    TFFN_OPT_MOE_COMBINE = 6
 };
 int64_t tffn_set_option(int option, int64_t value);
 

@@ -169,3 +169,30 @@ def test_moe_full_size_stress_skew_sampled_tokens(cuda_lib):
     tokens, _ = _full_size_tokens(r, T, k, 32, seed=2)
     parity.assert_close(Y[tokens].float().cpu().numpy(), _oracle_tokens(inp, k, "gelu_tanh", "none", tokens),
                         "moe stress full size")
+
+
+@pytest.mark.parametrize("T,N,O,P,E,k,router", [
+    (300, 64, 256, 128, 8, 2, "balanced"),
+    (700, 128, 384, 264, 8, 2, "stress"),     # one expert in most tokens; ragged last Y tile
+    (129, 64, 512, 520, 16, 4, "moderate"),   # top-4, three Y tiles
+    (50, 64, 128, 64, 4, 4, "balanced"),      # top_k = E
+    (40, 64, 128, 64, 1, 1, "balanced"),      # a single expert
+])
+def test_moe_fused_combine_equals_combine_kernel(cuda_lib, T, N, O, P, E, k, router):
+    # The gate-weighted sum formed in the expert FFN's layer-2 epilogue (by the
+    # last of a token's rows to finish) and by the separate combine kernel are
+    # the same fp32 arithmetic in slot order: bit-equal, and equal to the oracle.
+    inp = synth.moe_inputs(T, N, O, P, E, seed=T + k, device="cuda", router=router)
+    prev = cuda_lib.set_option(cuda_lib.OPT_MOE_COMBINE, 1)
+    try:
+        fused = [cuda_lib.moe_ffn_forward(inp.X, inp.logits, k, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh", "relu")
+                 for _ in range(2)]
+        assert cuda_lib.last_launch_count() == 5
+        cuda_lib.set_option(cuda_lib.OPT_MOE_COMBINE, 0)
+        sep = cuda_lib.moe_ffn_forward(inp.X, inp.logits, k, inp.W1, inp.b1, inp.W2, inp.b2, "gelu_tanh", "relu")
+        assert cuda_lib.last_launch_count() == 6
+    finally:
+        cuda_lib.set_option(cuda_lib.OPT_MOE_COMBINE, prev)
+    cuda_lib.check()
+    assert torch.equal(fused[0], sep) and torch.equal(fused[1], sep)
+    _assert_close(sep.float().cpu().numpy(), _oracle_y(inp, k, "gelu_tanh", "relu"), "combine")

@@ -14,7 +14,7 @@ import torch
 __all__ = ["ffn_forward", "moe_ffn_forward", "load", "check", "set_option", "workspace_bytes",
            "set_workspace", "last_launch_count", "timing_begin", "timing_end", "TffnError",
            "ACT_NONE", "ACT_RELU", "ACT_GELU_TANH", "ACT_SILU", "ffn_glu_forward", "moe_glu_forward", "OPT_PATH", "OPT_WAIT_LIMIT_MS",
-           "OPT_SKIP_FLAG", "OPT_GROUP_M", "OPT_MOE_ORDER", "LIB_PATH"]
+           "OPT_SKIP_FLAG", "OPT_GROUP_M", "OPT_MOE_ORDER", "OPT_MOE_COMBINE", "LIB_PATH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtffn.so")
@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libtffn.so")
 ACT_NONE, ACT_RELU, ACT_GELU_TANH, ACT_SILU = 0, 1, 2, 3
 _ACTS = {"none": ACT_NONE, None: ACT_NONE, "relu": ACT_RELU, "gelu_tanh": ACT_GELU_TANH,
          "gelu": ACT_GELU_TANH, "silu": ACT_SILU, "swish": ACT_SILU}
-OPT_PATH, OPT_WAIT_LIMIT_MS, OPT_SKIP_FLAG, OPT_GROUP_M, OPT_MOE_ORDER = 1, 2, 3, 4, 5
+OPT_PATH, OPT_WAIT_LIMIT_MS, OPT_SKIP_FLAG, OPT_GROUP_M, OPT_MOE_ORDER, OPT_MOE_COMBINE = 1, 2, 3, 4, 5, 6
 
 _lib = None
 

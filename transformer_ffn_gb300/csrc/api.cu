@@ -38,6 +38,10 @@ constexpr size_t FLAG_WORDS = size_t(1) << 20;
 constexpr size_t OFF_DCOUNT = OFF_FLAGS + FLAG_WORDS * 4;
 constexpr size_t DCOUNT_WORDS = size_t(1) << 16;
 constexpr size_t SYNC_BYTES = size_t(5) << 20;
+// MoE combine arrival counters (one per token and Y column tile), reset by
+// the last arriver, in the rest of the sync region.
+constexpr size_t OFF_MCOUNT = OFF_DCOUNT + DCOUNT_WORDS * 4;
+constexpr size_t MCOUNT_WORDS = (SYNC_BYTES - OFF_MCOUNT) / 4;
 static_assert(OFF_DCOUNT + DCOUNT_WORDS * 4 <= SYNC_BYTES, "sync region layout");
 constexpr uint32_t EPOCH_LIMIT = 0x7FFFFFF0u;      // launches before the flag region is cleared
 
@@ -116,6 +120,7 @@ std::atomic<int64_t> g_opt_wait_ms{4000};
 std::atomic<int64_t> g_opt_skip{-1};
 std::atomic<int64_t> g_opt_group{4};
 std::atomic<int64_t> g_opt_moe_order{1};
+std::atomic<int64_t> g_opt_moe_combine{1};
 
 thread_local int g_last_launches = 0;
 thread_local bool g_timing = false;
@@ -378,8 +383,8 @@ DenseLayout dense_layout(int64_t M, int64_t N, int64_t O, int64_t P, int sms, bo
 struct MoeLayout {
     int64_t R = 0, Rmax = 0, mbmax = 0;
     int32_t n1 = 0, n2 = 0;
-    size_t off_idx, off_w, off_pos, off_hist, off_bpad, off_boff, off_pad, off_band, off_nb, off_xp, off_h, off_yp,
-        total;
+    size_t off_idx, off_w, off_pos, off_hist, off_bpad, off_boff, off_pad, off_band, off_nb, off_rowent, off_xp,
+        off_h, off_yp, total;
 };
 
 // glu: gated experts, whose layer-1 tiles cover 128 hidden columns
@@ -409,6 +414,7 @@ MoeLayout moe_layout(int64_t T, int64_t N, int64_t O, int64_t P, int E, int k, b
     L.off_pad = take(static_cast<size_t>(2 * E) * 4);
     L.off_band = take(static_cast<size_t>(L.mbmax) * 4);
     L.off_nb = take(4);
+    L.off_rowent = take(static_cast<size_t>(L.Rmax) * 4);
     L.off_xp = take(static_cast<size_t>(L.Rmax) * N * 2);
     L.off_h = take(static_cast<size_t>(L.Rmax) * O * 2);
     L.off_yp = take(static_cast<size_t>(L.Rmax) * P * 4);
@@ -830,9 +836,15 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
     int32_t* padt = reinterpret_cast<int32_t*>(base + L.off_pad);
     int32_t* band = reinterpret_cast<int32_t*>(base + L.off_band);
     int32_t* nb = reinterpret_cast<int32_t*>(base + L.off_nb);
+    int32_t* rowent = reinterpret_cast<int32_t*>(base + L.off_rowent);
     void* Xp = base + L.off_xp;
     void* H = base + L.off_h;
     float* Yp = reinterpret_cast<float*>(base + L.off_yp);
+    // The weighted sum of the experts' outputs runs in the engine's layer-2
+    // epilogue when the per-token counters fit the sync region (else, or with
+    // TFFN_OPT_MOE_COMBINE = 0, as a separate kernel; identical results).
+    const bool fused_combine = g_opt_moe_combine.load() != 0 &&
+                               static_cast<size_t>(T) * static_cast<size_t>(L.n2) <= MCOUNT_WORDS;
 
     CallKey key;
     key.kind = glu ? 65 : 64;
@@ -886,6 +898,12 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
         cp = d->moe_cache.store(key, p);
     }
     engine::Params<MOE_MAX_E>& p = *cp;
+    p.row_entry = fused_combine ? rowent : nullptr;
+    p.comb_pos = pos;
+    p.comb_w = w;
+    p.comb_cnt = fused_combine ? reinterpret_cast<uint32_t*>(base + OFF_MCOUNT) : nullptr;
+    p.comb_y = static_cast<__nv_bfloat16*>(Y);
+    p.comb_k = top_k;
     p.wait_limit_ns = wait_limit_ns();
     p.group_m = static_cast<int32_t>(g_opt_group.load() < 1 ? 1 : g_opt_group.load());
     p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
@@ -894,17 +912,19 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
     fail |= launch_moe_route(gate_logits, T, E, top_k, idx, w, hist, s);
     fail |= launch_moe_plan(hist, T, E, engine::BM, g_opt_moe_order.load() != 0 ? 1 : 0, bpad, boff, band, nb, padt,
                             routing ? routing->expert_offsets : nullptr, s);
-    fail |= launch_moe_scatter(idx, T, E, top_k, bpad, boff, pos, routing ? routing->perm : nullptr, s);
-    fail |= launch_moe_gather(X, pos, T, top_k, padt, E, N, Xp, d->sms * 4, s);
+    fail |= launch_moe_scatter(idx, T, E, top_k, bpad, boff, pos, routing ? routing->perm : nullptr,
+                               fused_combine ? rowent : nullptr, s);
+    fail |= launch_moe_gather(X, pos, T, top_k, padt, E, N, Xp, fused_combine ? rowent : nullptr, d->sms * 4, s);
     if (!fail) {
         timing_start(s);
         fail |= launch_engine_grouped(p, d->sms / 2, s);
         timing_stop(s);
     }
-    fail |= launch_moe_combine(Yp, pos, w, T, top_k, P, Y, d->sms * 4, s);
+    if (!fused_combine)
+        fail |= launch_moe_combine(Yp, pos, w, T, top_k, P, Y, d->sms * 4, s);
     if (fail)
         return TFFN_ERR_CUDA;
-    g_last_launches = 6;
+    g_last_launches = fused_combine ? 5 : 6;
     if (routing && routing->topk_idx &&
         cudaMemcpyAsync(routing->topk_idx, idx, static_cast<size_t>(L.R) * 4, cudaMemcpyDeviceToDevice, s) !=
             cudaSuccess)
@@ -1027,6 +1047,7 @@ int64_t tffn_set_option(int option, int64_t value)
     case TFFN_OPT_SKIP_FLAG: return g_opt_skip.exchange(value);
     case TFFN_OPT_GROUP_M: return g_opt_group.exchange(value);
     case TFFN_OPT_MOE_ORDER: return g_opt_moe_order.exchange(value);
+    case TFFN_OPT_MOE_COMBINE: return g_opt_moe_combine.exchange(value);
     default: return -1;
     }
 }

@@ -116,6 +116,17 @@ struct Params {
     int32_t b3d;                               // 1: map_b are 3-D {64 cols, K, cols/64} maps
     int32_t glu;                               // 1: layer 1 is gated, H = act(X W1) * (X W3)
     CUtensorMap map_b_lin[MAX_E];              // glu: W3[e], laid out like map_b[0][e]
+    // MoE combine fused into the layer-2 epilogue (comb_cnt NULL: off; the
+    // separate combine kernel runs instead).  row_entry[r] is the routing
+    // entry t*k+s of grouped row r (-1 for a padding row, which is then not
+    // stored); the last of a token's k rows to finish a Y column tile sums
+    // the k expert outputs in slot order: Y[t] = sum_s w[t,s] Yp[pos[t,s]].
+    const int32_t* row_entry;                  // [rows of the grouped layout]
+    const int32_t* comb_pos;                   // [T * k] grouped row of each entry
+    const float* comb_w;                       // [T * k] gate weights
+    uint32_t* comb_cnt;                        // [T * n2] arrivals, reset by the last arriver
+    __nv_bfloat16* comb_y;                     // Y [T x ncols of layer 2]
+    int32_t comb_k;
 };
 
 // Hidden columns one layer-1 tile produces: a gated tile spends its 256
@@ -556,6 +567,65 @@ __device__ __forceinline__ void drain_any(int act, bool gated, uint32_t taddr, i
 #undef TFFN_DRAIN
 }
 
+// Fused MoE combine after a layer-2 tile: each lane's row (routing entry
+// t*k+s, or -1 for a padding row) has stored its fp32 outputs of Y column tile
+// `tile`; its arrival is counted for (t, tile), and the rows that are the last
+// of their token's k rows are then finished by the whole warp, one after
+// another: lane l forms columns [8l, 8l+8) of Y[t] = bf16(sum_s w[t,s]
+// Yp[pos[t,s]]) in slot order (fp32 fma from 0, the same arithmetic as the
+// separate combine kernel, so the result does not depend on which row
+// finished last), with coalesced reads of the k expert rows.
+template <int MAX_E>
+__device__ __noinline__ void combine_rows(const Params<MAX_E>& p, int32_t entry, int32_t tile, int32_t col0,
+                                          int32_t ncols, int lane)
+{
+    const int k = p.comb_k;
+    bool last = false;
+    if (entry >= 0) {
+        uint32_t* cnt = p.comb_cnt + static_cast<int64_t>(entry / k) * p.layer[1].n_tiles + tile;
+        __threadfence();   // this row's stores before its arrival
+        last = atomicAdd(cnt, 1u) == static_cast<uint32_t>(k - 1);
+        if (last)
+            *cnt = 0u;     // all k rows have arrived: ready for the next call
+    }
+    uint32_t m = __ballot_sync(0xffffffffu, last);
+    if (m == 0u)
+        return;
+    __threadfence();       // every other row of those tokens is stored and visible
+    const float* yp = static_cast<const float*>(p.layer[1].out);
+    const int64_t ld = p.layer[1].ld_out;
+    const int32_t col = col0 + lane * 8;
+    const bool in = col < ncols;   // ncols is a multiple of 8
+    while (m != 0u) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1u;
+        const int64_t t = __shfl_sync(0xffffffffu, entry, src) / k;
+        if (!in)
+            continue;
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            a[i] = 0.0f;
+        for (int sl = 0; sl < k; ++sl) {
+            const float g = __ldg(p.comb_w + t * k + sl);
+            const float4* v4 =
+                reinterpret_cast<const float4*>(yp + static_cast<int64_t>(__ldg(p.comb_pos + t * k + sl)) * ld + col);
+            const float4 u = __ldcg(v4), v = __ldcg(v4 + 1);
+            a[0] = fmaf(g, u.x, a[0]);
+            a[1] = fmaf(g, u.y, a[1]);
+            a[2] = fmaf(g, u.z, a[2]);
+            a[3] = fmaf(g, u.w, a[3]);
+            a[4] = fmaf(g, v.x, a[4]);
+            a[5] = fmaf(g, v.y, a[5]);
+            a[6] = fmaf(g, v.z, a[6]);
+            a[7] = fmaf(g, v.w, a[7]);
+        }
+        *reinterpret_cast<uint4*>(p.comb_y + t * static_cast<int64_t>(ncols) + col) =
+            make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                       pack_bf16x2(a[6], a[7]));
+    }
+}
+
 template <int MAX_E>
 __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w, uint32_t tmem_base,
                              uint32_t rank, int warp, int lane, float* bias_slice)
@@ -582,6 +652,11 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
             break;
         fetch_bias_part(gated ? nullptr : p.bias[L][expert_of(p, task.y)], task.z * BN, la.ncols, bias_slice, quad,
                         lane);
+        // Fused MoE combine: this thread's row's routing entry (-1: a padding
+        // row, not stored), read before the accumulator wait.
+        const bool fuse = MAX_E > 1 && L == 1 && p.comb_cnt != nullptr;
+        const int64_t row = static_cast<int64_t>(task.y) * BM + rank * BM_CTA + quad * 32 + lane;
+        const int32_t entry = (fuse && row < la.rows) ? __ldg(p.row_entry + row) : -1;
         __syncwarp();
         if (lane == 0)
             ptx::mbar_arrive(ptx::smem_u32(&aux.bias_ready));
@@ -597,8 +672,7 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         const bool out_f32 = la.out_f32 != 0;
         const int64_t ld_out = la.ld_out;
         void* const out = la.out;
-        const int64_t row = static_cast<int64_t>(task.y) * BM + rank * BM_CTA + quad * 32 + lane;
-        const bool row_ok = row < la.rows;
+        const bool row_ok = fuse ? entry >= 0 : row < la.rows;
         const int32_t tile_cols = gated ? BN_CTA : BN;
         const int32_t col_base = task.z * tile_cols;
         const int nchunks = ncols - col_base >= tile_cols ? tile_cols / 32 : (ncols - col_base + 31) / 32;
@@ -614,6 +688,8 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         if (lane == 0)
             arrive_on_leader(ptx::smem_u32(&aux.tmem_empty[acc]), rank);
         ++iter;
+        if (fuse)
+            combine_rows(p, entry, task.z, col_base, ncols, lane);
 
         // Layer-1 tile: publish this warp's 32 rows of the H tile by stamping
         // the warp's flag word with the call's epoch (release, gpu scope).

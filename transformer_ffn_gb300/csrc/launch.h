@@ -45,10 +45,12 @@ int launch_moe_route(const float* logits, int64_t T, int E, int k, int32_t* idx,
 int launch_moe_plan(const int32_t* blk_hist, int64_t T, int E, int bm, int size_desc, int32_t* blk_pad,
                     int32_t* blk_off, int32_t* band_expert, int32_t* nbands, int32_t* pad, int32_t* offs_out,
                     cudaStream_t s);
+// row_entry (nullable): the routing entry of each grouped row, -1 for padding rows
+// (the scatter writes the real rows, the gather the padding rows).
 int launch_moe_scatter(const int32_t* idx, int64_t T, int E, int k, const int32_t* blk_pad, const int32_t* blk_off,
-                       int32_t* pos, int32_t* perm_out, cudaStream_t s);
+                       int32_t* pos, int32_t* perm_out, int32_t* row_entry, cudaStream_t s);
 int launch_moe_gather(const void* X, const int32_t* pos, int64_t T, int k, const int32_t* pad, int E, int64_t N,
-                      void* Xp, int grid, cudaStream_t s);
+                      void* Xp, int32_t* row_entry, int grid, cudaStream_t s);
 int launch_moe_combine(const float* Yp, const int32_t* pos, const float* w, int64_t T, int k, int64_t P,
                        void* Y, int grid, cudaStream_t s);
 

@@ -156,7 +156,7 @@ __global__ void plan_kernel(const int32_t* __restrict__ blk_hist, int nblk, int 
 __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int E, int k,
                                                      const int32_t* __restrict__ blk_pad,
                                                      const int32_t* __restrict__ blk_off, int32_t* __restrict__ pos,
-                                                     int32_t* __restrict__ perm_out)
+                                                     int32_t* __restrict__ perm_out, int32_t* __restrict__ row_entry)
 {
     __shared__ int32_t cnt[64];
     const int lane = threadIdx.x;
@@ -175,7 +175,10 @@ __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__
         const int rank = __popc(same & ((1u << lane) - 1u));
         const int32_t base = valid ? cnt[e] : 0;
         if (valid) {
-            pos[i0 + j] = blk_pad[b * E + e] + base + rank;
+            const int32_t r = blk_pad[b * E + e] + base + rank;
+            pos[i0 + j] = r;
+            if (row_entry)
+                row_entry[r] = static_cast<int32_t>(i0 + j);
             if (perm_out)
                 perm_out[blk_off[b * E + e] + base + rank] = static_cast<int32_t>(i0 + j);
         }
@@ -189,9 +192,10 @@ __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__
 // ------------------------------------------------------------------- gather
 // One warp per entry: X_perm[pos[i]] = X[i / k]; then the experts' padding
 // rows (pad[2e] first row, pad[2e+1] count), numbered across experts, are
-// zeroed, one per warp.
+// zeroed, one per warp, and marked -1 in row_entry (when given).
 __global__ void gather_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restrict__ pos, int64_t R, int k,
-                              const int32_t* __restrict__ pad, int E, int64_t N, __nv_bfloat16* __restrict__ Xp)
+                              const int32_t* __restrict__ pad, int E, int64_t N, __nv_bfloat16* __restrict__ Xp,
+                              int32_t* __restrict__ row_entry)
 {
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -216,6 +220,8 @@ __global__ void gather_kernel(const __nv_bfloat16* __restrict__ X, const int32_t
         uint4* dst = reinterpret_cast<uint4*>(Xp + (pad[2 * e] + rest) * N);
         for (int64_t c = lane; c < nvec; c += 32)
             dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        if (row_entry && lane == 0)
+            row_entry[pad[2 * e] + rest] = -1;
     }
 }
 
@@ -270,17 +276,17 @@ int launch_moe_plan(const int32_t* blk_hist, int64_t T, int E, int bm, int size_
 }
 
 int launch_moe_scatter(const int32_t* idx, int64_t T, int E, int k, const int32_t* blk_pad, const int32_t* blk_off,
-                       int32_t* pos, int32_t* perm_out, cudaStream_t s)
+                       int32_t* pos, int32_t* perm_out, int32_t* row_entry, cudaStream_t s)
 {
-    moe::scatter_kernel<<<moe_route_blocks(T), 32, 0, s>>>(idx, T, E, k, blk_pad, blk_off, pos, perm_out);
+    moe::scatter_kernel<<<moe_route_blocks(T), 32, 0, s>>>(idx, T, E, k, blk_pad, blk_off, pos, perm_out, row_entry);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_moe_gather(const void* X, const int32_t* pos, int64_t T, int k, const int32_t* pad, int E, int64_t N,
-                      void* Xp, int grid, cudaStream_t s)
+                      void* Xp, int32_t* row_entry, int grid, cudaStream_t s)
 {
     moe::gather_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), pos, T * k, k, pad, E, N,
-                                            static_cast<__nv_bfloat16*>(Xp));
+                                            static_cast<__nv_bfloat16*>(Xp), row_entry);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
