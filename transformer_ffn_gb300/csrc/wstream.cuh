@@ -180,6 +180,11 @@ inline Plan make_plan(int64_t M, int64_t N, int64_t O, int64_t P, int grid, bool
         g = pl.units[0];
     pl.grid = static_cast<int32_t>(g);
     int64_t off = 0;
+    if (pl.win) {
+        // the window layer 1 is never split: one part per hidden block
+        pl.maxp[0] = 1;
+        pl.part_off[0] = 0;
+    }
     for (int l = pl.win ? 1 : 0; l < 2; ++l) {
         int32_t maxp = 1;
         for (int64_t s = 0; s < pl.slices[l]; ++s) {
