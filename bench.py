@@ -51,6 +51,10 @@ CONFIGS = {
                    label="decode FFN M=16 N=8192 O=28672 P=8192, ReLU"),
     "large": dict(kind="ffn", M=16384, N=8192, O=28672, P=8192, act1="gelu_tanh", act2="relu",
                   label="large prefill FFN M=16384 N=8192 O=28672 P=8192, GELU-tanh + ReLU"),
+    "large_m2048": dict(kind="ffn", M=2048, N=8192, O=28672, P=8192, act1="gelu_tanh", act2="relu",
+                        label="large-FFN dimensions at 2048 rows (M=2048 N=8192 O=28672 P=8192, GELU-tanh + ReLU): "
+                              "the engine on the large FFN's weights with a footprint small enough for a full ncu "
+                              "capture"),
     "moe": dict(kind="moe", M=8192, N=4096, O=14336, P=4096, E=8, k=2, act1="gelu_tanh", act2="none",
                 label="MoE FFN T=8192 N=4096 E=8 O=14336 P=4096, softmax top-2, GELU-tanh"),
     "swiglu": dict(kind="glu", M=4096, N=4096, O=14336, P=4096, act1="silu", act2="none",
