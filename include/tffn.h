@@ -261,7 +261,9 @@ const char* tffn_status_string(int status);
  *                         waiting GEMM2 work then times out and the call
  *                         reports TFFN_ERR_TIMEOUT through tffn_check() (or
  *                         tffn_check_noalloc())
- *   TFFN_OPT_GROUP_M      row bands per raster group of the engine (default 4)
+ *   TFFN_OPT_GROUP_M      row bands per raster group of the engine; 0
+ *                         (default): 8 when N >= 8192, else 4 (the measured
+ *                         optima on GB300)
  *   TFFN_OPT_MOE_ORDER    order of the experts' row segments in the grouped
  *                         layout: 0 expert index, 1 (default) largest row
  *                         count first.  Results are identical either way.

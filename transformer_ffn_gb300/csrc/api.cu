@@ -118,7 +118,7 @@ DeviceState g_dev[64];
 std::atomic<int64_t> g_opt_path{0};
 std::atomic<int64_t> g_opt_wait_ms{4000};
 std::atomic<int64_t> g_opt_skip{-1};
-std::atomic<int64_t> g_opt_group{4};
+std::atomic<int64_t> g_opt_group{0};
 std::atomic<int64_t> g_opt_moe_order{1};
 std::atomic<int64_t> g_opt_moe_combine{1};
 
@@ -291,6 +291,20 @@ void timing_stop(cudaStream_t s)
         return;
     cudaEventRecord(g_events[g_events_used].second, s);
     ++g_events_used;
+}
+
+// Row bands per raster group of the engine.  Inside a group the tiles go
+// column by column, so the CTA pairs in flight read (pairs / group) weight
+// panels of N x 256 at a time; on GB300 both measured optima hold ~38 MB of
+// panels in flight: 4 bands at N 4096 (prefill: 0.731 ms against 0.749-0.762
+// at 2, 8 or 16), 8 bands at N 8192 (large: 9.61 ms against 9.71-9.77 at 4
+// and 9.81-9.87 at 16).  TFFN_OPT_GROUP_M > 0 overrides.
+int32_t raster_group(int64_t N)
+{
+    const int64_t g = g_opt_group.load();
+    if (g > 0)
+        return static_cast<int32_t>(g);
+    return N >= 8192 ? 8 : 4;
 }
 
 uint64_t wait_limit_ns()
@@ -587,7 +601,7 @@ static int run_dense_engine(DeviceState& d, uint8_t* base, const DenseLayout& L,
     p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
     p.ctrl = reinterpret_cast<DevCtrl*>(base);
     p.wait_limit_ns = wait_limit_ns();
-    p.group_m = static_cast<int32_t>(g_opt_group.load() < 1 ? 1 : g_opt_group.load());
+    p.group_m = raster_group(p.layer[0].K);
     p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
     if (L.path == 1) {
         int rc = count_launch(d, base, s);
@@ -905,7 +919,7 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
     p.comb_y = static_cast<__nv_bfloat16*>(Y);
     p.comb_k = top_k;
     p.wait_limit_ns = wait_limit_ns();
-    p.group_m = static_cast<int32_t>(g_opt_group.load() < 1 ? 1 : g_opt_group.load());
+    p.group_m = raster_group(N);
     p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
 
     int fail = 0;
