@@ -526,6 +526,39 @@ def run_e2e_latency(cfg, inp, steps, warmup, stream):
     return times
 
 
+def run_unfused(cfg, inp, steps, warmup, stream):
+    """Context comparator (bench only, never the library's path): the same
+    dense or gated FFN as separate kernels -- cuBLAS GEMMs through
+    torch.matmul and torch's elementwise bias / activation kernels, H kept in
+    bf16 between the layers as the fused path keeps it.  Returns the mean
+    seconds per step (one event pair around back-to-back steps)."""
+    import torch
+    import torch.nn.functional as F
+    acts = {"none": lambda x: x, "relu": F.relu, "gelu_tanh": lambda x: F.gelu(x, approximate="tanh"),
+            "silu": F.silu}
+    a1, a2 = acts[cfg["act1"]], acts[cfg["act2"]]
+    X = inp.X
+    if cfg["kind"] == "glu":
+        def step():
+            H = a1(X @ inp.W1) * (X @ inp.W3)
+            return H @ inp.W2
+    else:
+        def step():
+            H = a1(torch.addmm(inp.b1, X, inp.W1))
+            return a2(torch.addmm(inp.b2, H, inp.W2))
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / steps
+
+
 def padded_rows(cfg, inp):
     """Rows of the grouped layout, zero padding included (each expert's rows
     rounded up to whole 256-row bands), from the routing the library returns."""
@@ -635,6 +668,13 @@ def measure_gpu(name, args, world, rank, local, with_cpu):
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed_block": wall,
     }
+    if cfg["kind"] in ("ffn", "glu") and not args.no_unfused:
+        u_s = max_over_ranks(run_unfused(cfg, inp, args.steps, max(2, args.warmup), stream), world)
+        entry["unfused_comparator"] = {
+            "impl": "the same FFN as separate kernels: cuBLAS GEMMs (torch.matmul / addmm) and torch "
+                    "elementwise bias and activation kernels, H in bf16 between the layers",
+            "value": rate(cfg, u_s) * world, "unit": unit, "ms_per_step": u_s * 1e3,
+            "fused_speedup": u_s / mean_s}
     if args.ffn_path != "auto":
         entry["path"] = args.ffn_path
     if cfg["kind"] == "moe":
@@ -656,6 +696,8 @@ def _summary(entry):
     s["kernel_ms"] = entry["roofline"]["kernel_ms"]
     s["kernel_achieved"] = entry["roofline"]["achieved"]
     s["e2e_latency_ms"] = entry["e2e"]["latency"]["ms_per_call"]
+    if "unfused_comparator" in entry:
+        s["fused_speedup_vs_unfused"] = entry["unfused_comparator"]["fused_speedup"]
     return s
 
 
@@ -798,6 +840,19 @@ def cpu_baseline(name, cfg, inp, Y_dev=None, budget_s=8.0):
     else:
         out["extrapolated"] = True
         out["full_workload_s_extrapolated"] = t_total * cfg["M"] / len(done)
+    # the same rows, row-parallel over every host core (ctypes releases the
+    # interpreter lock during each C call): a second figure, labelled as such
+    from concurrent.futures import ThreadPoolExecutor
+    nthr = max(1, min(os.cpu_count() or 1, len(done)))
+    rows = [int(r) for r in done]
+    chunks = [rows[i * len(rows) // nthr:(i + 1) * len(rows) // nthr] for i in range(nthr)]
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=nthr) as ex:
+        list(ex.map(lambda c: _oracle_rows(cfg, host, c), [c for c in chunks if c]))
+    t_all = time.perf_counter() - t0
+    out["all_cores"] = {"value": (_sample_work(cfg, len(done)) / t_all) / (1e9 if unit == "GB/s" else 1e12),
+                        "unit": unit, "cores": nthr, "seconds": t_all,
+                        "kind": "oracle, the same rows split over host threads (row-parallel)"}
     if Y_dev is not None:
         got = Y_dev[list(done)].float().cpu().numpy()
         want = np.stack(results)
@@ -863,6 +918,8 @@ def main():
                     help="seconds of oracle work per sampled workload in the CPU baseline")
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true",
+                    help="skip the unfused comparator (cuBLAS GEMMs + torch elementwise kernels)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 20 if args.impl == "reference" else 200

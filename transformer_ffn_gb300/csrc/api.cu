@@ -731,7 +731,9 @@ int ffn_forward(const void* X, const void* W1, const void* b1, const void* W2, c
         const bool b3d = (O % 64 == 0) && (P % 64 == 0);
         if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) ||
             make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) || make_map_b(&p.map_b[0][0], W1, O, N, b3d) ||
-            make_map_b(&p.map_b[1][0], W2, P, O, b3d))
+            make_map_b(&p.map_b[1][0], W2, P, O, b3d) ||
+            make_map(&p.map_out[0], H, O, rows_h, engine::OUT_COLS, 32) ||
+            make_map(&p.map_out[1], Y, P, M, engine::OUT_COLS, 32))
             return TFFN_ERR_INVALID_ARG;
         p.b3d = b3d ? 1 : 0;
         p.bias[0][0] = static_cast<const __nv_bfloat16*>(b1);
@@ -783,7 +785,9 @@ int ffn_glu_forward(const void* X, const void* W1, const void* W3, const void* W
         const bool b3d = (O % 64 == 0) && (P % 64 == 0);
         if (make_map(&p.map_a[0], X, N, M, 64, engine::BM_CTA) ||
             make_map(&p.map_a[1], H, O, rows_h, 64, engine::BM_CTA) || make_map_b(&p.map_b[0][0], W1, O, N, b3d) ||
-            make_map_b(&p.map_b_lin[0], W3, O, N, b3d) || make_map_b(&p.map_b[1][0], W2, P, O, b3d))
+            make_map_b(&p.map_b_lin[0], W3, O, N, b3d) || make_map_b(&p.map_b[1][0], W2, P, O, b3d) ||
+            make_map(&p.map_out[0], H, O, rows_h, engine::OUT_COLS, 32) ||
+            make_map(&p.map_out[1], Y, P, M, engine::OUT_COLS, 32))
             return TFFN_ERR_INVALID_ARG;
         p.b3d = b3d ? 1 : 0;
         p.glu = 1;
@@ -885,8 +889,12 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
         std::unique_ptr<engine::Params<MOE_MAX_E>> pp(new engine::Params<MOE_MAX_E>);
         std::memset(static_cast<void*>(pp.get()), 0, sizeof(*pp));
         engine::Params<MOE_MAX_E>& p = *pp;
+        // outputs: H_perm (bf16, boxes of 32 rows x 64 columns) and the fp32
+        // Y_perm (boxes of 32 rows x 32 columns, 128 bytes per row either way)
         int bad = make_map(&p.map_a[0], Xp, N, L.Rmax, 64, engine::BM_CTA) |
-                  make_map(&p.map_a[1], H, O, L.Rmax, 64, engine::BM_CTA);
+                  make_map(&p.map_a[1], H, O, L.Rmax, 64, engine::BM_CTA) |
+                  make_map(&p.map_out[0], H, O, L.Rmax, engine::OUT_COLS, 32) |
+                  make_map_f32(&p.map_out[1], Yp, P, L.Rmax);
         const bool b3d = (O % 64 == 0) && (P % 64 == 0);
         p.b3d = b3d ? 1 : 0;
         for (int e = 0; e < E && !bad; ++e) {

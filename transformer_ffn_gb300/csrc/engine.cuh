@@ -16,8 +16,8 @@
 // the pair (128 each) and B's columns split between the pair (128 each), and
 // writes each CTA's tensor memory with its 128 rows x 256 columns.  Each CTA
 // therefore streams only half of the B tile: 32 KiB per 64-deep k-stage per
-// SM, seven stages deep (all of a CTA's shared memory but the barrier block
-// and one 1 KiB bias slice).
+// SM, six stages deep, beside 32 KiB of output staging buffers, the barrier
+// block and one 1 KiB bias slice (all of a CTA's shared memory).
 //
 // CTA layout (224 threads, one CTA per SM, two CTAs per cluster):
 //   warp 0      A loader.  The leader (cluster rank 0) takes tickets and
@@ -36,8 +36,10 @@
 //               lanes x 256 fp32 columns).
 //   warps 2..5  epilogue: tcgen05.ld the CTA's accumulator (one TMEM lane
 //               quadrant per warp, one row per thread), bias, activation,
-//               round, store; the accumulator is double-buffered so the
-//               epilogue of one tile overlaps the main loop of the next.
+//               round, write the rows into the warp's swizzled staging
+//               buffer, TMA-store each 32-row box; the accumulator is
+//               double-buffered so the epilogue of one tile overlaps the
+//               main loop of the next.
 //               The four warps share the tile's bias slice in shared memory
 //               (each fetches a quarter before the accumulator wait).
 //   warp 1 of the peer CTA has no role after the allocation.
@@ -63,9 +65,9 @@ constexpr int BN = 256;                                   // columns of a tile
 constexpr int BN_CTA = 128;                               // B columns loaded per CTA
 constexpr int BK = 64;
 #ifndef TFFN_ENGINE_STAGES
-#define TFFN_ENGINE_STAGES 7
+#define TFFN_ENGINE_STAGES 6
 #endif
-constexpr int STAGES = TFFN_ENGINE_STAGES;              // 7 x 32 KiB: all the shared memory a CTA gets
+constexpr int STAGES = TFFN_ENGINE_STAGES;              // 6 x 32 KiB, beside the output staging buffers
 constexpr int A_STAGE_BYTES = BM_CTA * BK * 2;            // 16 KiB
 constexpr int B_BOX_BYTES = 64 * BK * 2;                  // 8 KiB: 64 cols x 64 k
 constexpr int B_STAGE_BYTES = BK * BN_CTA * 2;            // 16 KiB
@@ -78,7 +80,14 @@ constexpr int FLAG_WORDS_PER_TILE = 2 * EPI_WARPS;        // one per epilogue wa
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int AUX_BYTES = 1024;
 constexpr int BIAS_BYTES = BN * 4;                        // the tile's fp32 bias, shared by the epilogue warps
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + BIAS_BYTES + 1024;   // + alignment slack
+// bf16 outputs leave through shared memory and TMA stores: each epilogue warp
+// owns two 4 KiB buffers, each a 32-row x 64-column box in the 128-byte
+// swizzled layout (per-thread row stores from the epilogue slowed the
+// concurrent main loop's operand feed by 9-12 %).
+constexpr int OUT_COLS = 64;
+constexpr int OUT_BUF_BYTES = 32 * OUT_COLS * 2;          // 4 KiB
+constexpr int OUT_BYTES = EPI_WARPS * 2 * OUT_BUF_BYTES;  // 32 KiB
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + AUX_BYTES + BIAS_BYTES + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 // Arrivals that free a task slot (counted on the leader): leader MMA thread,
 // leader B loader, leader epilogue warps, peer A loader, peer B loader, peer
@@ -101,6 +110,8 @@ struct LayerArgs {
 template <int MAX_E>
 struct Params {
     CUtensorMap map_a[2];                      // layer-1 A (X), layer-2 A (H); box {64, 128}
+    CUtensorMap map_out[2];                    // outputs H [rows x O], Y [rows x P] stored by TMA from the
+                                               // epilogue: bf16 box {64, 32}; fp32 (MoE Y_perm) box {32, 32}
     CUtensorMap map_b[2][MAX_E];               // W1[e], W2[e]; b3d: {64, 64, 2} else {64, 64}
     const __nv_bfloat16* bias[2][MAX_E];       // b1[e], b2[e] (nullable)
     LayerArgs layer[2];
@@ -456,115 +467,190 @@ __device__ __forceinline__ void fetch_bias_part(const __nv_bfloat16* bias, int32
     *reinterpret_cast<float2*>(slice + i) = v;
 }
 
-// Rounding and the row's store of 32 finished values at column col.
-__device__ __forceinline__ void store_row_chunk(const float (&v)[32], void* out, bool out_f32, int64_t row,
-                                                int64_t ld_out, int32_t col, int32_t ncols)
+// ---- bf16 outputs through shared memory and TMA stores.
+// A staging buffer holds a 32-row x 64-column bf16 box in the 128-byte
+// swizzled layout a TMA store reads: 16-byte chunk j (0..7) of row r sits at
+// r * 128 + (j ^ (r % 8)) * 16.  Each thread writes its own row, one 32-column
+// half (chunks 4h .. 4h+3) at a time.
+__device__ __forceinline__ void stage_half(uint32_t buf, int lane, int h, const uint32_t (&pk)[16])
 {
-    const int nvalid = ncols - col < 32 ? ncols - col : 32;   // multiple of 8
-    if (out_f32) {
-        float* dst = static_cast<float*>(out) + row * ld_out + col;
+    const uint32_t rowaddr = buf + static_cast<uint32_t>(lane) * 128u;
+    const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            if (q * 4 < nvalid)
-                reinterpret_cast<float4*>(dst)[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
-    } else {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + row * ld_out + col;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (q * 8 < nvalid)
-                reinterpret_cast<uint4*>(dst)[q] =
-                    make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                               pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-    }
+    for (int j = 0; j < 4; ++j)
+        ptx::st_shared_v4(rowaddr + (((static_cast<uint32_t>(4 * h + j)) ^ sw) << 4), pk[4 * j], pk[4 * j + 1],
+                          pk[4 * j + 2], pk[4 * j + 3]);
 }
 
-// Bias, activation, rounding and the row's store for one 32-column chunk.
-// The activation is a template argument, chosen once per tile.
+// Bias, activation and bf16 rounding of 32 accumulator columns into 16 packed
+// words (the same arithmetic as store_chunk).
 template <int ACT>
-__device__ __forceinline__ void store_chunk(const uint32_t (&acc)[32], uint32_t bias_smem, bool row_ok, void* out,
-                                            bool out_f32, int64_t row, int64_t ld_out, int32_t col, int32_t ncols)
+__device__ __forceinline__ void convert32(const uint32_t (&acc)[32], uint32_t bias_smem, uint32_t (&pk)[16])
 {
-    float v[32];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         float4 b;   // the same address in every lane: a broadcast
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                      : "=f"(b.x), "=f"(b.y), "=f"(b.z), "=f"(b.w)
                      : "r"(bias_smem + q * 16));
-        v[q * 4 + 0] = act_apply(ACT, __uint_as_float(acc[q * 4 + 0]) + b.x);
-        v[q * 4 + 1] = act_apply(ACT, __uint_as_float(acc[q * 4 + 1]) + b.y);
-        v[q * 4 + 2] = act_apply(ACT, __uint_as_float(acc[q * 4 + 2]) + b.z);
-        v[q * 4 + 3] = act_apply(ACT, __uint_as_float(acc[q * 4 + 3]) + b.w);
+        pk[2 * q] = pack_bf16x2(act_apply(ACT, __uint_as_float(acc[q * 4 + 0]) + b.x),
+                                act_apply(ACT, __uint_as_float(acc[q * 4 + 1]) + b.y));
+        pk[2 * q + 1] = pack_bf16x2(act_apply(ACT, __uint_as_float(acc[q * 4 + 2]) + b.z),
+                                    act_apply(ACT, __uint_as_float(acc[q * 4 + 3]) + b.w));
     }
-    if (row_ok)
-        store_row_chunk(v, out, out_f32, row, ld_out, col, ncols);
 }
 
-// Drain one 128 x BN accumulator quadrant-row by quadrant-row: chunk c+1's
-// TMEM load is in flight while chunk c is computed and stored.
+// Before a staging buffer is rewritten: the store issued from it two boxes
+// ago has finished reading it (lane 0 issued every store of the warp).
+__device__ __forceinline__ void out_buffer_free(int lane)
+{
+    if (lane == 0)
+        ptx::bulk_wait_group_read<1>();
+    __syncwarp();
+}
+
+// The staged box to global memory: every lane's shared-memory writes are made
+// visible to the async proxy, then lane 0 issues the store as one bulk group.
+// Rows and columns outside the map (past the output's extent) are not written.
+__device__ __forceinline__ void out_store_box(const CUtensorMap* map, uint32_t buf, int lane, int32_t x, int32_t y)
+{
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        ptx::tma_store_2d(map, buf, x, y);
+        ptx::bulk_commit_group();
+    }
+}
+
+// Drain one accumulator tile through the staging buffers, 64 columns per box;
+// the TMEM load of the next 32 columns is in flight while the current ones are
+// converted.  Returns the warp's next staging buffer.
 template <int ACT>
-__device__ __forceinline__ void drain_tile(uint32_t taddr, int nchunks, uint32_t bias_smem, bool row_ok, void* out,
-                                           bool out_f32, int64_t row, int64_t ld_out, int32_t col_base, int32_t ncols)
+__device__ __forceinline__ uint32_t drain_tile_tma(uint32_t taddr, int nchunks, uint32_t bias_smem,
+                                                   const CUtensorMap* map, uint32_t stage, uint32_t sb, int lane,
+                                                   int32_t row0, int32_t col_base)
 {
     uint32_t ra[32], rb[32];
     __syncwarp();
     ptx::tmem_ld_32x32b_x32(taddr, ra);
     for (int c = 0; c < nchunks; c += 2) {
+        const uint32_t buf = stage + sb * OUT_BUF_BYTES;
+        out_buffer_free(lane);
+        uint32_t pk[16];
         ptx::tmem_ld_wait();
         if (c + 1 < nchunks)
             ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, rb);
-        store_chunk<ACT>(ra, bias_smem + c * 128, row_ok, out, out_f32, row, ld_out, col_base + c * 32, ncols);
+        convert32<ACT>(ra, bias_smem + c * 128, pk);
+        stage_half(buf, lane, 0, pk);
         if (c + 1 < nchunks) {
             ptx::tmem_ld_wait();
             if (c + 2 < nchunks)
                 ptx::tmem_ld_32x32b_x32(taddr + (c + 2) * 32, ra);
-            store_chunk<ACT>(rb, bias_smem + (c + 1) * 128, row_ok, out, out_f32, row, ld_out,
-                             col_base + (c + 1) * 32, ncols);
-        }
-    }
-}
-
-// Drain a gated layer-1 tile: accumulator columns [0, 128) hold X W1 and
-// [128, 256) hold X W3 for the same 128 hidden columns; H = act(gate) * lin.
-template <int ACT>
-__device__ __forceinline__ void drain_glu(uint32_t taddr, int nchunks, bool row_ok, void* out, int64_t row,
-                                          int64_t ld_out, int32_t col_base, int32_t ncols)
-{
-    for (int c = 0; c < nchunks; ++c) {
-        uint32_t g[32], u[32];
-        __syncwarp();
-        ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
-        ptx::tmem_ld_32x32b_x32(taddr + BN_CTA + c * 32, u);
-        ptx::tmem_ld_wait();
-        float v[32];
+            convert32<ACT>(rb, bias_smem + (c + 1) * 128, pk);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            v[i] = act_apply(ACT, __uint_as_float(g[i])) * __uint_as_float(u[i]);
-        if (row_ok)
-            store_row_chunk(v, out, false, row, ld_out, col_base + c * 32, ncols);
+            for (int i = 0; i < 16; ++i)
+                pk[i] = 0u;   // columns past the output: clipped by the store
+        }
+        stage_half(buf, lane, 1, pk);
+        out_store_box(map, buf, lane, col_base + c * 32, row0);
+        sb ^= 1u;
     }
+    return sb;
 }
 
-// One finished accumulator tile, with the activation resolved to a template
-// argument once.
-__device__ __forceinline__ void drain_any(int act, bool gated, uint32_t taddr, int nchunks, uint32_t bias_smem,
-                                          bool row_ok, void* out, bool out_f32, int64_t row, int64_t ld_out,
-                                          int32_t col_base, int32_t ncols)
+// Gated layer-1 tile through the staging buffers: gate columns [0, 128) and
+// linear columns [128, 256) of the accumulator give 128 H columns.
+template <int ACT>
+__device__ __forceinline__ uint32_t drain_glu_tma(uint32_t taddr, int nchunks, const CUtensorMap* map,
+                                                  uint32_t stage, uint32_t sb, int lane, int32_t row0,
+                                                  int32_t col_base)
 {
-#define TFFN_DRAIN(A)                                                                                        \
-    do {                                                                                                     \
-        if (gated)                                                                                           \
-            drain_glu<A>(taddr, nchunks, row_ok, out, row, ld_out, col_base, ncols);                         \
-        else                                                                                                 \
-            drain_tile<A>(taddr, nchunks, bias_smem, row_ok, out, out_f32, row, ld_out, col_base, ncols);    \
+    for (int c = 0; c < nchunks; c += 2) {
+        const uint32_t buf = stage + sb * OUT_BUF_BYTES;
+        out_buffer_free(lane);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t pk[16];
+            if (c + h < nchunks) {
+                uint32_t g[32], u[32];
+                __syncwarp();
+                ptx::tmem_ld_32x32b_x32(taddr + (c + h) * 32, g);
+                ptx::tmem_ld_32x32b_x32(taddr + BN_CTA + (c + h) * 32, u);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(act_apply(ACT, __uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
+                                        act_apply(ACT, __uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = 0u;
+            }
+            stage_half(buf, lane, h, pk);
+        }
+        out_store_box(map, buf, lane, col_base + c * 32, row0);
+        sb ^= 1u;
+    }
+    return sb;
+}
+
+// fp32 output (the MoE experts' Y rows before the weighted sum): a 32-column
+// chunk is a full 128-byte row of a 32 x 32 fp32 box, converted in place.
+template <int ACT>
+__device__ __forceinline__ uint32_t drain_tile_tma_f32(uint32_t taddr, int nchunks, uint32_t bias_smem,
+                                                       const CUtensorMap* map, uint32_t stage, uint32_t sb, int lane,
+                                                       int32_t row0, int32_t col_base)
+{
+    const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
+    for (int c = 0; c < nchunks; ++c) {
+        uint32_t ra[32];
+        const uint32_t buf = stage + sb * OUT_BUF_BYTES;
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(taddr + c * 32, ra);
+        out_buffer_free(lane);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float4 b;   // the same address in every lane: a broadcast
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(b.x), "=f"(b.y), "=f"(b.z), "=f"(b.w)
+                         : "r"(bias_smem + c * 128 + q * 16));
+            ptx::st_shared_v4(buf + static_cast<uint32_t>(lane) * 128u + ((static_cast<uint32_t>(q) ^ sw) << 4),
+                              __float_as_uint(act_apply(ACT, __uint_as_float(ra[q * 4 + 0]) + b.x)),
+                              __float_as_uint(act_apply(ACT, __uint_as_float(ra[q * 4 + 1]) + b.y)),
+                              __float_as_uint(act_apply(ACT, __uint_as_float(ra[q * 4 + 2]) + b.z)),
+                              __float_as_uint(act_apply(ACT, __uint_as_float(ra[q * 4 + 3]) + b.w)));
+        }
+        out_store_box(map, buf, lane, col_base + c * 32, row0);
+        sb ^= 1u;
+    }
+    return sb;
+}
+
+// A finished accumulator tile through the staging buffers and TMA stores, the
+// activation resolved to a template argument once; returns the warp's next
+// staging buffer.
+__device__ __forceinline__ uint32_t drain_any_tma(int act, bool gated, bool out_f32, uint32_t taddr, int nchunks,
+                                                  uint32_t bias_smem, const CUtensorMap* map, uint32_t stage,
+                                                  uint32_t sb, int lane, int32_t row0, int32_t col_base)
+{
+#define TFFN_DRAIN_TMA(A)                                                                              \
+    do {                                                                                               \
+        if (gated)                                                                                     \
+            return drain_glu_tma<A>(taddr, nchunks, map, stage, sb, lane, row0, col_base);       \
+        if (out_f32)                                                                                   \
+            return drain_tile_tma_f32<A>(taddr, nchunks, bias_smem, map, stage, sb, lane, row0, col_base); \
+        return drain_tile_tma<A>(taddr, nchunks, bias_smem, map, stage, sb, lane, row0, col_base); \
     } while (0)
     switch (act) {
-    case TFFN_ACT_GELU_TANH: TFFN_DRAIN(TFFN_ACT_GELU_TANH); break;
-    case TFFN_ACT_SILU: TFFN_DRAIN(TFFN_ACT_SILU); break;
-    case TFFN_ACT_RELU: TFFN_DRAIN(TFFN_ACT_RELU); break;
-    default: TFFN_DRAIN(TFFN_ACT_NONE); break;
+    case TFFN_ACT_GELU_TANH: TFFN_DRAIN_TMA(TFFN_ACT_GELU_TANH); break;
+    case TFFN_ACT_SILU: TFFN_DRAIN_TMA(TFFN_ACT_SILU); break;
+    case TFFN_ACT_RELU: TFFN_DRAIN_TMA(TFFN_ACT_RELU); break;
+    default: TFFN_DRAIN_TMA(TFFN_ACT_NONE); break;
     }
-#undef TFFN_DRAIN
+#undef TFFN_DRAIN_TMA
+    return sb;
 }
 
 // Fused MoE combine after a layer-2 tile: each lane's row (routing entry
@@ -628,11 +714,12 @@ __device__ __noinline__ void combine_rows(const Params<MAX_E>& p, int32_t entry,
 
 template <int MAX_E>
 __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w, uint32_t tmem_base,
-                             uint32_t rank, int warp, int lane, float* bias_slice)
+                             uint32_t rank, int warp, int lane, float* bias_slice, uint32_t out_stage)
 {
     const uint32_t quad = static_cast<uint32_t>(warp & 3);   // TMEM lanes [32*quad, 32*quad+32)
     const int32_t n1 = p.layer[0].n_tiles;
     uint32_t iter = 0;
+    uint32_t sb = 0;   // the warp's next staging buffer
     Ring ring;
     for (;;) {
         int4 task;
@@ -670,15 +757,13 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         const int32_t ncols = la.ncols;
         const int act = la.act;
         const bool out_f32 = la.out_f32 != 0;
-        const int64_t ld_out = la.ld_out;
-        void* const out = la.out;
-        const bool row_ok = fuse ? entry >= 0 : row < la.rows;
         const int32_t tile_cols = gated ? BN_CTA : BN;
         const int32_t col_base = task.z * tile_cols;
         const int nchunks = ncols - col_base >= tile_cols ? tile_cols / 32 : (ncols - col_base + 31) / 32;
         const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * BN;
-        drain_any(act, gated, taddr, nchunks, ptx::smem_u32(bias_slice), row_ok, out, out_f32, row, ld_out, col_base,
-                  ncols);
+        const int32_t row0 = task.y * BM + static_cast<int32_t>(rank) * BM_CTA + static_cast<int32_t>(quad) * 32;
+        sb = drain_any_tma(act, gated, out_f32, taddr, nchunks, ptx::smem_u32(bias_slice), &p.map_out[L], out_stage,
+                           sb, lane, row0, col_base);
         __syncwarp();
         if (lane == 0)
             ptx::mbar_arrive(ptx::smem_u32(&aux.bias_free));
@@ -688,12 +773,23 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
         if (lane == 0)
             arrive_on_leader(ptx::smem_u32(&aux.tmem_empty[acc]), rank);
         ++iter;
-        if (fuse)
+        if (fuse) {
+            // the warp's rows are in memory (its stores completed, the async
+            // proxy's writes ordered before the arrivals) before they are counted
+            if (lane == 0) {
+                ptx::bulk_wait_group<0>();
+                ptx::fence_proxy_async_global();
+            }
+            __syncwarp();
             combine_rows(p, entry, task.z, col_base, ncols, lane);
+        }
 
         // Layer-1 tile: publish this warp's 32 rows of the H tile by stamping
         // the warp's flag word with the call's epoch (release, gpu scope).
+        // The tile's TMA stores (issued by lane 0) complete first.
         if (L == 0 && p.mode == MODE_FUSED) {
+            if (lane == 0)
+                ptx::bulk_wait_group<0>();
             ptx::fence_proxy_async_global();
             __syncwarp();
             if (lane == 0) {
@@ -705,6 +801,10 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
             }
         }
     }
+    // Every store of this warp has completed before the CTA can leave.
+    if (lane == 0)
+        ptx::bulk_wait_group<0>();
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------- kernel
@@ -714,7 +814,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Aux& aux = *reinterpret_cast<Aux*>(stages + STAGES * STAGE_BYTES);
+    Aux& aux = *reinterpret_cast<Aux*>(stages + STAGES * STAGE_BYTES + OUT_BYTES);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const uint32_t rank = ptx::cluster_ctarank();
@@ -777,8 +877,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
         if (lane == 0 && rank == 0)
             run_mma(p, aux, stages, w, tmem_base);
     } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
-        float* bias_slice = reinterpret_cast<float*>(stages + STAGES * STAGE_BYTES + AUX_BYTES);
-        run_epilogue(p, aux, w, tmem_base, rank, warp, lane, bias_slice);
+        float* bias_slice = reinterpret_cast<float*>(stages + STAGES * STAGE_BYTES + OUT_BYTES + AUX_BYTES);
+        const uint32_t out_stage = ptx::smem_u32(stages + STAGES * STAGE_BYTES) +
+                                   static_cast<uint32_t>((warp - 2) * 2 * OUT_BUF_BYTES);
+        run_epilogue(p, aux, w, tmem_base, rank, warp, lane, bias_slice, out_stage);
     }
     __syncwarp();
     ptx::tc_fence_before();

@@ -122,6 +122,23 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 2-D tiled store of one shared-memory box into global memory through a
+// tensor map, as a member of this thread's current bulk async-group (elements
+// outside the tensor are not written).  x must keep the 16-byte rule of
+// tma_load_2d, and neither coordinate may be negative.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // Asynchronous tile reduction: adds a shared-memory box element-wise into
 // global memory through a tensor map (an fp32 map: fp32 add), as a member of
 // this thread's current bulk async-group.  Elements outside the tensor are
