@@ -68,12 +68,16 @@ __device__ __forceinline__ void raise_error(const WaitCtx& w, uint32_t code, uin
     }
 }
 
-// Wait for the phase of `bar` with this parity; false on abort or timeout.
-static __device__ __noinline__ bool wait_mbar(const WaitCtx& w, uint32_t bar, uint32_t parity,
-                                       uint32_t where)
+// Polls made inline before a wait falls back to its timed loop.  The hot
+// loops (a stage ring's full / empty barriers) wait on every k-block; an
+// out-of-line call there cost the engine 4-8 % (GEMM of 4096 x 4096 x 16384:
+// 357 -> 328 us with the inline polls).
+constexpr int FAST_POLLS = 4096;
+
+// The timed part of wait_mbar (out of line: rarely reached).
+static __device__ __noinline__ bool wait_mbar_timed(const WaitCtx& w, uint32_t bar, uint32_t parity,
+                                                    uint32_t where)
 {
-    if (ptx::mbar_try_wait(bar, parity))
-        return true;
     const uint64_t t0 = ptx::globaltimer();
     for (;;) {
         if (ptx::mbar_try_wait(bar, parity))
@@ -87,13 +91,21 @@ static __device__ __noinline__ bool wait_mbar(const WaitCtx& w, uint32_t bar, ui
     }
 }
 
-// Same, acquiring at cluster scope: for barriers that receive arrivals from the
-// peer CTA of a cluster (or from its tensor-core commits).
-static __device__ __noinline__ bool wait_mbar_cl(const WaitCtx& w, uint32_t bar, uint32_t parity,
-                                                 uint32_t where)
+// Wait for the phase of `bar` with this parity: at most FAST_POLLS inline
+// probes, then the timed loop; false on abort or timeout.
+__device__ __forceinline__ bool wait_mbar(const WaitCtx& w, uint32_t bar, uint32_t parity, uint32_t where)
 {
-    if (ptx::mbar_try_wait_cluster(bar, parity))
-        return true;
+#pragma unroll 1
+    for (int i = 0; i < FAST_POLLS; ++i)
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+    return wait_mbar_timed(w, bar, parity, where);
+}
+
+// The timed part of wait_mbar_cl.
+static __device__ __noinline__ bool wait_mbar_cl_timed(const WaitCtx& w, uint32_t bar, uint32_t parity,
+                                                       uint32_t where)
+{
     const uint64_t t0 = ptx::globaltimer();
     for (;;) {
         if (ptx::mbar_try_wait_cluster(bar, parity))
@@ -105,6 +117,17 @@ static __device__ __noinline__ bool wait_mbar_cl(const WaitCtx& w, uint32_t bar,
             return false;
         }
     }
+}
+
+// Same, acquiring at cluster scope: for barriers that receive arrivals from the
+// peer CTA of a cluster (or from its tensor-core commits).
+__device__ __forceinline__ bool wait_mbar_cl(const WaitCtx& w, uint32_t bar, uint32_t parity, uint32_t where)
+{
+#pragma unroll 1
+    for (int i = 0; i < FAST_POLLS; ++i)
+        if (ptx::mbar_try_wait_cluster(bar, parity))
+            return true;
+    return wait_mbar_cl_timed(w, bar, parity, where);
 }
 
 // Wait (acquire, gpu scope) until *flag == epoch; false on abort or timeout.
