@@ -595,7 +595,11 @@ def measure_gpu(name, args, world, rank, local, with_cpu):
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
-    tffn.timing_begin()
+    # one dominant-kernel launch in four gets its own event pair when the
+    # steps run back to back (an event recorded between two kernels
+    # serialises them and would slow every step it sits in)
+    timing_every = 4 if flush_buf is None and args.steps >= 8 else 1
+    tffn.timing_begin(timing_every)
     sampler.mark("start")
     t0 = time.perf_counter()
     per_step = time_steps(step, args.steps, flush_buf, stream)
@@ -632,6 +636,9 @@ def measure_gpu(name, args, world, rank, local, with_cpu):
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json {'hbm_gbs' if is_hbm_bound(cfg) else 'bf16_tflops'})"
     roof["kernel"] = dominant_kernel(name, args.ffn_path)
     roof["kernel_ms"] = dom_s * 1e3
+    roof["kernel_launches_timed"] = n_dom
+    roof["kernel_timing"] = (f"CUDA event pair around one launch of every {timing_every} in the timed region"
+                             if timing_every > 1 else "CUDA event pair around every launch in the timed region")
     roof["algorithmic_per_launch"] = weight_bytes(cfg) if is_hbm_bound(cfg) else flops(cfg)
     roof["traffic"] = recorded_traffic(name, roof["kernel"])
     if weight_bytes(cfg) < 64e6 and is_hbm_bound(cfg):

@@ -293,6 +293,11 @@ int tffn_last_launch_count(void);
  * returns the number of timed launches and their summed milliseconds. */
 int tffn_timing_begin(void);
 int tffn_timing_end(int* launches, double* total_ms);
+/* Time only one dominant launch of every `every` (>= 1; default 1) from the
+ * next tffn_timing_begin on: an event pair recorded between two kernels
+ * serialises them, so sampling keeps most launches back to back.  Returns
+ * TFFN_ERR_INVALID_ARG for every < 1. */
+int tffn_timing_sample(int every);
 
 /* Host-side view of the engine's task order, for tests (no GPU needed):
  * the task of `ticket` for a fused launch with m_blocks row bands, n1 GEMM1

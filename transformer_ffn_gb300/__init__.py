@@ -75,6 +75,8 @@ def load():
     L.tffn_timing_begin.restype = i32
     L.tffn_timing_end.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_double)]
     L.tffn_timing_end.restype = i32
+    L.tffn_timing_sample.argtypes = [i32]
+    L.tffn_timing_sample.restype = i32
     L.tffn_debug_engine_task.argtypes = [i64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, i64,
                                          ctypes.POINTER(ctypes.c_int32)]
     L.tffn_debug_engine_task.restype = i64
@@ -290,8 +292,12 @@ def last_launch_count():
     return int(load().tffn_last_launch_count())
 
 
-def timing_begin():
-    _raise(load().tffn_timing_begin(), "timing_begin")
+def timing_begin(every=1):
+    """Time the dominant kernel of the next forward calls: one launch of every
+    `every` gets a CUDA event pair (the others run back to back)."""
+    L = load()
+    _raise(L.tffn_timing_sample(int(every)), "timing_sample")
+    _raise(L.tffn_timing_begin(), "timing_begin")
 
 
 def timing_end():

@@ -124,6 +124,9 @@ std::atomic<int64_t> g_opt_moe_combine{1};
 
 thread_local int g_last_launches = 0;
 thread_local bool g_timing = false;
+thread_local int g_timing_every = 1;        // time one dominant launch of every g_timing_every
+thread_local uint64_t g_timing_seen = 0;
+thread_local bool g_timing_this = false;
 thread_local std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_events;
 thread_local size_t g_events_used = 0;
 
@@ -274,7 +277,8 @@ int count_launch(DeviceState& d, uint8_t* base, cudaStream_t s)
 
 void timing_start(cudaStream_t s)
 {
-    if (!g_timing)
+    g_timing_this = g_timing && (g_timing_seen++ % static_cast<uint64_t>(g_timing_every)) == 0;
+    if (!g_timing_this)
         return;
     if (g_events_used == g_events.size()) {
         cudaEvent_t a, b;
@@ -287,8 +291,9 @@ void timing_start(cudaStream_t s)
 
 void timing_stop(cudaStream_t s)
 {
-    if (!g_timing)
+    if (!g_timing_this)
         return;
+    g_timing_this = false;
     cudaEventRecord(g_events[g_events_used].second, s);
     ++g_events_used;
 }
@@ -1080,6 +1085,15 @@ int tffn_timing_begin(void)
 {
     g_timing = true;
     g_events_used = 0;
+    g_timing_seen = 0;
+    return TFFN_OK;
+}
+
+int tffn_timing_sample(int every)
+{
+    if (every < 1)
+        return TFFN_ERR_INVALID_ARG;
+    g_timing_every = every;
     return TFFN_OK;
 }
 
