@@ -215,3 +215,43 @@ def test_stream_plan_validation(lib):
         tffn.debug_stream_plan(6, 257, 64, 64, 64, 152)
     with pytest.raises(tffn.TffnError):
         tffn.debug_stream_plan(3, 16, 64, 64, 64, 152)
+
+
+def test_timing_sample_and_options_without_gpu(lib):
+    # the sampling interval of the dominant-kernel timing is validated on the
+    # host; the MoE combine option round-trips like the others
+    lib.tffn_timing_sample.argtypes = [ctypes.c_int]
+    lib.tffn_timing_sample.restype = ctypes.c_int
+    assert lib.tffn_timing_sample(0) == -1
+    assert lib.tffn_timing_sample(-3) == -1
+    assert lib.tffn_timing_sample(4) == 0
+    assert lib.tffn_timing_sample(1) == 0
+    lib.tffn_set_option.argtypes = [ctypes.c_int, ctypes.c_int64]
+    lib.tffn_set_option.restype = ctypes.c_int64
+    prev = lib.tffn_set_option(6, 0)          # TFFN_OPT_MOE_COMBINE
+    assert prev == 1                          # fused by default
+    assert lib.tffn_set_option(6, prev) == 0
+    prev = lib.tffn_set_option(4, 0)          # TFFN_OPT_GROUP_M: 0 = chosen by shape
+    assert lib.tffn_set_option(4, prev) == 0
+
+
+def test_noalloc_validation_without_gpu(lib):
+    # argument errors come back before any CUDA call; the error query fails
+    # cleanly (TFFN_ERR_CUDA) when there is no device to synchronise
+    fn = lib.ffn_forward_decode_noalloc
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i64, i64, i64, vp, vp]
+    fn.restype = i32
+    p = ctypes.c_void_p(1 << 20)
+    assert fn(p, p, None, p, None, 1, 0, 33, 64, 64, 64, p, None) == -1     # more than 32 rows
+    assert fn(p, p, None, p, None, 1, 0, 16, 60, 64, 64, p, None) == -1     # N not a multiple of 8
+    assert fn(p, p, None, p, None, 9, 0, 16, 64, 64, 64, p, None) == -1     # unknown activation
+    assert fn(None, None, None, None, None, 1, 0, 0, 64, 64, 64, None, None) == 0   # empty call
+    chk = lib.tffn_check_noalloc
+    chk.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    chk.restype = i32
+    import torch
+    if not torch.cuda.is_available():
+        detail = (ctypes.c_int32 * 4)(7, 7, 7, 7)
+        assert chk(None, detail) == -3
+        assert list(detail) == [0, 0, 0, 0]
