@@ -599,6 +599,8 @@ static int run_wstream(DeviceState& d, uint8_t* base, const DenseLayout& L, cons
 static int run_dense_engine(DeviceState& d, uint8_t* base, const DenseLayout& L, engine::Params<1>& p,
                             cudaStream_t s)
 {
+    if (engine_total_tickets(L.m_blocks, L.n1, L.n2, MODE_FUSED) > ENGINE_MAX_TICKETS)
+        return TFFN_ERR_INVALID_ARG;
     p.layer[0].n_tiles = L.n1;
     p.m_blocks = L.m_blocks;
     p.m_blocks_dev = nullptr;
@@ -935,6 +937,8 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
     p.group_m = raster_group(N);
     p.skip_flag = static_cast<int32_t>(g_opt_skip.load());
 
+    if (engine_total_tickets(L.mbmax, L.n1, L.n2, MODE_FUSED) > ENGINE_MAX_TICKETS)
+        return TFFN_ERR_INVALID_ARG;
     int fail = 0;
     fail |= launch_moe_route(gate_logits, T, E, top_k, idx, w, hist, s);
     fail |= launch_moe_plan(hist, T, E, engine::BM, g_opt_moe_order.load() != 0 ? 1 : 0, bpad, boff, band, nb, padt,

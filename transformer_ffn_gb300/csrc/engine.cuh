@@ -226,6 +226,21 @@ __device__ __forceinline__ bool read_task(AuxT& aux, const WaitCtx& w, Ring& r, 
     return true;
 }
 
+// Leader's producer: hand a task to this CTA's consumers (a plain store and a
+// local arrival) and to the peer CTA's.  The peer's copy travels as one
+// asynchronous 16-byte store that completes the peer's slot barrier itself,
+// so the producer goes on to its copies without waiting for the remote write.
+template <class AuxT>
+__device__ __forceinline__ void publish_task(AuxT& aux, Ring& r, int4 task)
+{
+    aux.task[r.slot] = task;
+    ptx::mbar_arrive(ptx::smem_u32(&aux.task_full[r.slot]));
+    const uint32_t peer_full = ptx::mapa(ptx::smem_u32(&aux.task_full[r.slot]), 1);
+    ptx::mbar_arrive_expect_tx_cluster_relaxed(peer_full, static_cast<uint32_t>(sizeof(int4)));
+    ptx::st_async_v4(ptx::mapa(ptx::smem_u32(&aux.task[r.slot]), 1), task, peer_full);
+    r.advance();
+}
+
 // Layer-2 producer: make sure H chunk j of the band is published, polling a
 // window of up to H_WINDOW chunks at once (relaxed loads of this CTA's four
 // words per chunk, independent so they overlap), then one acquire fence and
@@ -288,17 +303,14 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
         int4 task;
         if (rank == 0) {
             const uint32_t t = atomicAdd(&p.ctrl->ticket, 1u);
-            EngineTask et = engine_task(static_cast<int64_t>(t), m_blocks, n1, n2, p.group_m, p.mode);
+            EngineTask et = engine_task_t<int32_t>(static_cast<int32_t>(t), static_cast<int32_t>(m_blocks), n1, n2,
+                                                   p.group_m, p.mode);
             if (static_cast<int64_t>(t) >= total)
                 et.layer = -1;
             task = make_int4(et.layer, et.band, et.tile, 0);
             if (!wait_mbar_cl(w, ptx::smem_u32(&aux.task_empty[ring.slot]), ring.phase ^ 1u, SITE_TASK_EMPTY))
                 break;
-            aux.task[ring.slot] = task;
-            ptx::st_cluster_v4(ptx::mapa(ptx::smem_u32(&aux.task[ring.slot]), 1), task);
-            ptx::mbar_arrive(ptx::smem_u32(&aux.task_full[ring.slot]));
-            ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&aux.task_full[ring.slot]), 1));
-            ring.advance();
+            publish_task(aux, ring, task);
         } else if (!read_task(aux, w, ring, rank, false, 0, task)) {
             break;
         }

@@ -396,10 +396,26 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, int4 v)
+// Store 16 bytes into the shared memory of a CTA of the cluster and count
+// them on an mbarrier of that CTA (complete_tx).  The issuing thread does not
+// wait for the remote store; a waiter that sees the barrier's phase complete
+// also sees the stored bytes.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, int4 v, uint32_t cluster_bar)
 {
-    asm volatile("st.shared::cluster.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.s32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_bar)
+                 : "memory");
+}
+
+// Arrive on an mbarrier of a CTA of the cluster and announce `bytes` of
+// complete_tx still to come in this phase.  Relaxed: it orders none of this
+// thread's earlier memory accesses (the data it announces travels with the
+// complete_tx of st_async_v4).
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster_relaxed(uint32_t cluster_bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
+                 "r"(bytes)
                  : "memory");
 }
 

@@ -70,11 +70,7 @@ __device__ void run_producer(const Params& p, Aux& aux, uint8_t* smem, const Wai
                        : make_int4(-1, 0, 0, 0);
             if (!wait_mbar_cl(w, ptx::smem_u32(&aux.task_empty[ring.slot]), ring.phase ^ 1u, SITE_TASK_EMPTY))
                 break;
-            aux.task[ring.slot] = task;
-            ptx::st_cluster_v4(ptx::mapa(ptx::smem_u32(&aux.task[ring.slot]), 1), task);
-            ptx::mbar_arrive(ptx::smem_u32(&aux.task_full[ring.slot]));
-            ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&aux.task_full[ring.slot]), 1));
-            ring.advance();
+            engine::publish_task(aux, ring, task);
         } else if (!engine::read_task(aux, w, ring, rank, false, 0, task)) {
             break;
         }
@@ -563,11 +559,7 @@ __device__ void b2b_producer(const Params& p, B2BAux& aux, uint8_t* smem, const 
                        : make_int4(-1, 0, 0, 0);
             if (!wait_mbar_cl(w, ptx::smem_u32(&aux.task_empty[ring.slot]), ring.phase ^ 1u, SITE_TASK_EMPTY))
                 break;
-            aux.task[ring.slot] = task;
-            ptx::st_cluster_v4(ptx::mapa(ptx::smem_u32(&aux.task[ring.slot]), 1), task);
-            ptx::mbar_arrive(ptx::smem_u32(&aux.task_full[ring.slot]));
-            ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&aux.task_full[ring.slot]), 1));
-            ring.advance();
+            engine::publish_task(aux, ring, task);
         } else if (!engine::read_task(aux, w, ring, rank, false, 0, task)) {
             break;
         }

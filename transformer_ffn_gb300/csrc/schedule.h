@@ -48,11 +48,15 @@ TFFN_HD int64_t engine_total_tickets(int64_t m_blocks, int32_t n1, int32_t n2, i
     return m_blocks * (static_cast<int64_t>(n1) + n2);
 }
 
-TFFN_HD EngineTask engine_in_group(int32_t layer, int64_t group, int64_t idx, int64_t m_blocks,
-                                   int32_t group_m)
+// The mapping is written once for any signed index type I: the host and the
+// schedule tests use int64_t; the kernel uses int32_t (32-bit division is
+// several times cheaper than 64-bit division on the GPU, and the host refuses
+// launches whose ticket count does not fit in 31 bits).
+template <typename I>
+TFFN_HD EngineTask engine_in_group_t(int32_t layer, I group, I idx, I m_blocks, I group_m)
 {
-    int64_t first = group * group_m;
-    int64_t gsize = m_blocks - first < group_m ? m_blocks - first : group_m;
+    const I first = group * group_m;
+    const I gsize = m_blocks - first < group_m ? m_blocks - first : group_m;
     EngineTask r;
     r.layer = layer;
     r.band = static_cast<int32_t>(first + idx % gsize);
@@ -60,8 +64,8 @@ TFFN_HD EngineTask engine_in_group(int32_t layer, int64_t group, int64_t idx, in
     return r;
 }
 
-TFFN_HD EngineTask engine_task(int64_t t, int64_t m_blocks, int32_t n1, int32_t n2,
-                               int32_t group_m, int32_t mode)
+template <typename I>
+TFFN_HD EngineTask engine_task_t(I t, I m_blocks, I n1, I n2, I group_m, int32_t mode)
 {
     EngineTask end;
     end.layer = -1;
@@ -69,52 +73,61 @@ TFFN_HD EngineTask engine_task(int64_t t, int64_t m_blocks, int32_t n1, int32_t 
     end.tile = 0;
     if (t < 0 || m_blocks <= 0)
         return end;
-    const int64_t ng = (m_blocks + group_m - 1) / group_m;
-    const int64_t full = static_cast<int64_t>(group_m);
+    const I ng = (m_blocks + group_m - 1) / group_m;
 
     if (mode == MODE_LAYER1 || mode == MODE_LAYER2) {
-        const int32_t n = mode == MODE_LAYER1 ? n1 : n2;
+        const I n = mode == MODE_LAYER1 ? n1 : n2;
         if (t >= m_blocks * n)
             return end;
-        const int64_t g = t / (full * n);
-        return engine_in_group(mode == MODE_LAYER1 ? 0 : 1, g, t - g * full * n, m_blocks, group_m);
+        const I g = t / (group_m * n);
+        return engine_in_group_t<I>(mode == MODE_LAYER1 ? 0 : 1, g, t - g * group_m * n, m_blocks, group_m);
     }
 
-    auto gsize = [&](int64_t g) -> int64_t {
-        int64_t rest = m_blocks - g * group_m;
-        return rest < group_m ? rest : full;
+    auto gsize = [&](I g) -> I {
+        const I rest = m_blocks - g * group_m;
+        return rest < group_m ? rest : group_m;
     };
     // L1(g0)
-    int64_t len = gsize(0) * n1;
+    I len = gsize(0) * n1;
     if (t < len)
-        return engine_in_group(0, 0, t, m_blocks, group_m);
+        return engine_in_group_t<I>(0, 0, t, m_blocks, group_m);
     t -= len;
     // pairs [L1(g), L2(g-1)] for g = 1 .. ng-1; pairs 1 .. ng-2 are full-sized
     // (only the last group can be short), so whole pairs are skipped at once
-    int64_t g0 = 1;
+    I g0 = 1;
     if (ng >= 3) {
-        const int64_t pair = full * (n1 + n2);
-        int64_t skip = t / pair;
+        const I pair = group_m * (n1 + n2);
+        I skip = t / pair;
         if (skip > ng - 2)
             skip = ng - 2;
         t -= skip * pair;
         g0 += skip;
     }
-    for (int64_t g = g0; g < ng; ++g) {
+    for (I g = g0; g < ng; ++g) {
         len = gsize(g) * n1;
         if (t < len)
-            return engine_in_group(0, g, t, m_blocks, group_m);
+            return engine_in_group_t<I>(0, g, t, m_blocks, group_m);
         t -= len;
         len = gsize(g - 1) * n2;
         if (t < len)
-            return engine_in_group(1, g - 1, t, m_blocks, group_m);
+            return engine_in_group_t<I>(1, g - 1, t, m_blocks, group_m);
         t -= len;
     }
     // L2(g_last)
     len = gsize(ng - 1) * n2;
     if (t < len)
-        return engine_in_group(1, ng - 1, t, m_blocks, group_m);
+        return engine_in_group_t<I>(1, ng - 1, t, m_blocks, group_m);
     return end;
 }
+
+TFFN_HD EngineTask engine_task(int64_t t, int64_t m_blocks, int32_t n1, int32_t n2, int32_t group_m,
+                               int32_t mode)
+{
+    return engine_task_t<int64_t>(t, m_blocks, n1, n2, group_m, mode);
+}
+
+// Largest ticket count a launch may have: the kernel's ticket counter and its
+// task arithmetic are 32-bit, and every pair takes one ticket past the end.
+constexpr int64_t ENGINE_MAX_TICKETS = (int64_t(1) << 31) - (int64_t(1) << 16);
 
 }  // namespace tffn
