@@ -28,6 +28,8 @@ using namespace tffn;
 // [0, 256)                 DevCtrl
 // [256, 256 + 4 MiB)       ready flags / counters (engine: one per layer-1 tile)
 // [.., + 256 KiB)          decode split-K arrival counters
+// [.., + 64 KiB)           engine band counts
+// [.., SYNC_BYTES)         MoE combine arrival counters
 // [SYNC_BYTES, ...)        data: H, grouped rows, partial sums
 // The sync region is zeroed when a workspace is (re)initialised; after that,
 // flags are compared against the epoch kept in the control block (advanced by
@@ -38,12 +40,25 @@ constexpr size_t FLAG_WORDS = size_t(1) << 20;
 constexpr size_t OFF_DCOUNT = OFF_FLAGS + FLAG_WORDS * 4;
 constexpr size_t DCOUNT_WORDS = size_t(1) << 16;
 constexpr size_t SYNC_BYTES = size_t(5) << 20;
+// Engine band counts (two per 256-row band), zeroed by the last CTA out of
+// every fused engine launch; used by nothing else.
+constexpr size_t OFF_BCOUNT = OFF_DCOUNT + DCOUNT_WORDS * 4;
+constexpr size_t BCOUNT_WORDS = size_t(1) << 14;
 // MoE combine arrival counters (one per token and Y column tile), reset by
 // the last arriver, in the rest of the sync region.
-constexpr size_t OFF_MCOUNT = OFF_DCOUNT + DCOUNT_WORDS * 4;
+constexpr size_t OFF_MCOUNT = OFF_BCOUNT + BCOUNT_WORDS * 4;
 constexpr size_t MCOUNT_WORDS = (SYNC_BYTES - OFF_MCOUNT) / 4;
-static_assert(OFF_DCOUNT + DCOUNT_WORDS * 4 <= SYNC_BYTES, "sync region layout");
+static_assert(OFF_MCOUNT < SYNC_BYTES, "sync region layout");
 constexpr uint32_t EPOCH_LIMIT = 0x7FFFFFF0u;      // launches before the flag region is cleared
+
+// The band counts of a fused engine launch over `bands` bands (NULL when
+// there are more bands than the region holds: the producers then poll the
+// per-tile flags only).
+static uint32_t* band_counts(uint8_t* base, int64_t bands)
+{
+    return static_cast<size_t>(bands) * 2 <= BCOUNT_WORDS ? reinterpret_cast<uint32_t*>(base + OFF_BCOUNT) : nullptr;
+}
+
 
 constexpr int64_t DECODE_MAX_M = 32;   // the mma.sync weight stream wins up to here (measured)
 constexpr int64_t STREAM_MAX_M = 128;  // then the tensor-core weight stream, then the engine (measured);
@@ -606,6 +621,7 @@ static int run_dense_engine(DeviceState& d, uint8_t* base, const DenseLayout& L,
     p.m_blocks_dev = nullptr;
     p.band_expert = nullptr;
     p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+    p.band_count = band_counts(base, L.m_blocks);
     p.ctrl = reinterpret_cast<DevCtrl*>(base);
     p.wait_limit_ns = wait_limit_ns();
     p.group_m = raster_group(p.layer[0].K);
@@ -922,6 +938,7 @@ static int moe_forward(const void* X, const float* gate_logits, int top_k, const
         p.m_blocks_dev = nb;
         p.band_expert = band;
         p.flags = reinterpret_cast<uint32_t*>(base + OFF_FLAGS);
+        p.band_count = band_counts(base, L.mbmax);
         p.ctrl = reinterpret_cast<DevCtrl*>(base);
         p.mode = MODE_FUSED;
         cp = d->moe_cache.store(key, p);

@@ -119,6 +119,11 @@ struct Params {
     const int32_t* m_blocks_dev;
     const int32_t* band_expert;                // expert of each band (NULL: expert 0)
     uint32_t* flags;                           // [m_blocks * n1 * 8] ready words
+    // Per band and CTA rank: how many layer-1 epilogue warps of this launch
+    // have published their rows of the band (n1 * EPI_WARPS: the CTA's whole
+    // band of H is ready).  Zero when a launch starts; the last CTA out
+    // zeroes it again.  NULL: layer-2 producers poll the per-tile flags only.
+    uint32_t* band_count;                      // [m_blocks * 2]
     DevCtrl* ctrl;
     uint64_t wait_limit_ns;
     int32_t mode;                              // EngineMode
@@ -286,6 +291,15 @@ static __device__ __noinline__ bool wait_h_chunks(const WaitCtx& w, const uint32
     }
 }
 
+// Whole band of H published for this CTA's rows: one acquire load of the
+// band's count instead of a poll over its per-tile flags.
+template <int MAX_E>
+__device__ __forceinline__ bool band_complete(const Params<MAX_E>& p, int32_t band, uint32_t rank, int32_t n1)
+{
+    return p.band_count != nullptr &&
+           ptx::ld_acquire_gpu(&p.band_count[band * 2 + rank]) == static_cast<uint32_t>(n1 * EPI_WARPS);
+}
+
 // ----------------------------------------------------------------- producer
 template <int MAX_E>
 __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, const WaitCtx& w,
@@ -325,6 +339,10 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
         const bool wait_h = (L == 1 && p.mode == MODE_FUSED);
         // H chunks [0, ready_upto) of this band are known to be published
         int ready_upto = wait_h ? 0 : n1;
+        if (wait_h && band_complete(p, task.y, rank, n1)) {
+            ptx::fence_proxy_async_global();
+            ready_upto = n1;
+        }
         const uint32_t* band_flags =
             p.flags + static_cast<uint32_t>(task.y * n1) * FLAG_WORDS_PER_TILE + rank * EPI_WARPS;
         bool ok = true;
@@ -809,13 +827,21 @@ __device__ void run_epilogue(const Params<MAX_E>& p, Aux& aux, const WaitCtx& w,
                 if (fi != p.skip_flag) {
                     __threadfence();
                     ptx::st_release_gpu(&p.flags[fi * FLAG_WORDS_PER_TILE + rank * EPI_WARPS + quad], aux.epoch);
+                    // counted after the fence above, which orders the rows
+                    // before the count as it does before the flag
+                    if (p.band_count != nullptr)
+                        ptx::red_relaxed_add_gpu(&p.band_count[task.y * 2 + rank], 1u);
                 }
             }
         }
     }
-    // Every store of this warp has completed before the CTA can leave.
-    if (lane == 0)
+    // Every store of this warp has completed before the CTA can leave, and
+    // its band counts are ordered before the CTA's exit count (the last CTA
+    // out zeroes them).
+    if (lane == 0) {
         ptx::bulk_wait_group<0>();
+        __threadfence();
+    }
     __syncwarp();
 }
 
@@ -911,6 +937,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) engine_kernel(const __grid_con
             p.ctrl->ticket = 0u;
             p.ctrl->done = 0u;
             p.ctrl->epoch = aux.epoch;
+            if (p.band_count != nullptr && p.mode == MODE_FUSED) {
+                const int64_t mb = p.m_blocks >= 0 ? p.m_blocks : static_cast<int64_t>(*p.m_blocks_dev);
+                for (int64_t i = 0; i < 2 * mb; ++i)
+                    p.band_count[i] = 0u;
+            }
             __threadfence();
         }
     }

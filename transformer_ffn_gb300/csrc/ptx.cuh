@@ -223,6 +223,13 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v)
 
 // Release-add without a result: one thread publishes what its warp (after a
 // __syncwarp) or CTA (after a barrier) wrote before it.
+// Relaxed add without a result: the thread does not wait for it.  Ordered
+// after this thread's earlier writes only by a release fence before it.
+__device__ __forceinline__ void red_relaxed_add_gpu(uint32_t* p, uint32_t v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v)
 {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
