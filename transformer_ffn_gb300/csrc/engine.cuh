@@ -313,18 +313,32 @@ __device__ void run_producer(const Params<MAX_E>& p, Aux& aux, uint8_t* stages, 
     for (int s = 0; s < STAGES; ++s)
         last_phase[s] = -1;
 
-    for (;;) {
+    // The leader claims tickets one task ahead: when it starts a task, the
+    // next one is already claimed and in both CTAs' rings, so the B loader,
+    // the MMA thread and the peer move on to it without waiting for the
+    // claim.  Holding one ticket ahead keeps the schedule deadlock-free: a
+    // pair only holds a ticket larger than the one it runs, and every task
+    // waits only on tasks with smaller tickets.
+    auto claim_publish = [&](int4& out) -> bool {
+        const uint32_t t = atomicAdd(&p.ctrl->ticket, 1u);
+        EngineTask et = engine_task_t<int32_t>(static_cast<int32_t>(t), static_cast<int32_t>(m_blocks), n1, n2,
+                                               p.group_m, p.mode);
+        if (static_cast<int64_t>(t) >= total)
+            et.layer = -1;
+        out = make_int4(et.layer, et.band, et.tile, 0);
+        if (!wait_mbar_cl(w, ptx::smem_u32(&aux.task_empty[ring.slot]), ring.phase ^ 1u, SITE_TASK_EMPTY))
+            return false;
+        publish_task(aux, ring, out);
+        return true;
+    };
+    int4 ahead = make_int4(-1, 0, 0, 0);
+    const bool started = rank != 0 || claim_publish(ahead);
+    while (started) {
         int4 task;
         if (rank == 0) {
-            const uint32_t t = atomicAdd(&p.ctrl->ticket, 1u);
-            EngineTask et = engine_task_t<int32_t>(static_cast<int32_t>(t), static_cast<int32_t>(m_blocks), n1, n2,
-                                                   p.group_m, p.mode);
-            if (static_cast<int64_t>(t) >= total)
-                et.layer = -1;
-            task = make_int4(et.layer, et.band, et.tile, 0);
-            if (!wait_mbar_cl(w, ptx::smem_u32(&aux.task_empty[ring.slot]), ring.phase ^ 1u, SITE_TASK_EMPTY))
+            task = ahead;
+            if (task.x >= 0 && !claim_publish(ahead))
                 break;
-            publish_task(aux, ring, task);
         } else if (!read_task(aux, w, ring, rank, false, 0, task)) {
             break;
         }
