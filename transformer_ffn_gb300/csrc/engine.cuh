@@ -6,10 +6,12 @@
 //   layer 1 tile (band i, tile j):  H[i, j] = bf16(act1(X[i, :] W1[:, j] + b1[j]))
 //   layer 2 tile (band i, tile k):  Y[i, k] = act2(H[i, :] W2[:, k] + b2[k])
 // with fp32 accumulation in tensor memory.  A layer-1 tile publishes ready
-// flags once its H tile is in global memory; a layer-2 tile of the same band
-// waits on those flags chunk by chunk before its TMA loads read H, so H is
-// consumed while the rest of H is still being produced (the page's per-tile
-// flag, used here between the SMs of one GPU).
+// flags once its H tile is in global memory and counts itself in its band's
+// tally; a layer-2 tile of the same band starts at once when the tally says
+// the whole band is written, and otherwise waits on the flags chunk by chunk
+// before its TMA loads read H, so H is consumed while the rest of H is still
+// being produced (the page's per-tile flag, used here between the SMs of one
+// GPU).
 //
 // Tiles are 256 x 256 and belong to a cluster of two CTAs on two SMs (a CTA
 // pair): tcgen05.mma.cta_group::2 with M = 256 reads A's rows split between
@@ -20,10 +22,10 @@
 // block and one 1 KiB bias slice (all of a CTA's shared memory).
 //
 // CTA layout (224 threads, one CTA per SM, two CTAs per cluster):
-//   warp 0      A loader.  The leader (cluster rank 0) takes tickets and
-//               publishes each task to both CTAs' task rings; each A loader
-//               streams its CTA's A rows (and, for layer 2, waits on the H
-//               flags first).
+//   warp 0      A loader.  The leader (cluster rank 0) takes tickets one
+//               task ahead and publishes each task to both CTAs' task rings;
+//               each A loader streams its CTA's A rows (and, for layer 2,
+//               checks that H is ready first).
 //   warp 6      B loader: streams the CTA's B columns, one TMA copy per stage
 //               (a 3-D map covers both 64-column halves).  A and B copies are
 //               issued by different warps because one warp issues bulk copies
