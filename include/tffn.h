@@ -303,7 +303,8 @@ int tffn_timing_sample(int every);
  * the task of `ticket` for a fused launch with m_blocks row bands, n1 GEMM1
  * and n2 GEMM2 column tiles and raster groups of group_m bands.  out[0] =
  * layer (0 or 1, -1 past the end), out[1] = row band, out[2] = column tile.
- * Returns the total number of tickets. */
+ * Returns the total number of tickets, or -1 if the 32-bit form of the
+ * mapping that the kernel runs disagrees with this 64-bit one. */
 int64_t tffn_debug_engine_task(int64_t m_blocks, int32_t n1, int32_t n2, int32_t group_m,
                                int64_t ticket, int32_t out[3]);
 

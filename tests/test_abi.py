@@ -112,7 +112,8 @@ def test_engine_task_order_is_dependency_safe(lib):
         seen = set()
         done_l1 = {}
         for t in range(total):
-            _, (layer, band, tile) = tffn.debug_engine_task(mb, n1, n2, gm, t)
+            tot_t, (layer, band, tile) = tffn.debug_engine_task(mb, n1, n2, gm, t)
+            assert tot_t == total     # -1: the kernel's 32-bit mapping disagrees
             assert layer in (0, 1)
             assert 0 <= band < mb
             assert (layer, band, tile) not in seen
@@ -125,8 +126,28 @@ def test_engine_task_order_is_dependency_safe(lib):
                 # every layer-1 tile of this band has a smaller ticket
                 assert done_l1.get(band, 0) == n1
         assert len(seen) == total
-        _, (layer, _, _) = tffn.debug_engine_task(mb, n1, n2, gm, total)
-        assert layer == -1
+        tot_t, (layer, _, _) = tffn.debug_engine_task(mb, n1, n2, gm, total)
+        assert tot_t == total and layer == -1
+
+
+def test_engine_task_32bit_form_at_scale(lib):
+    """The kernel's 32-bit ticket arithmetic against the 64-bit form on
+    launches with hundreds of thousands of tickets (sampled tickets, every
+    segment boundary of the first and last groups)."""
+    import random
+    import transformer_ffn_gb300 as tffn
+    rnd = random.Random(3)
+    for (mb, n1, n2, gm) in [(4096, 112, 32, 8), (8191, 64, 16, 4), (2000, 7, 300, 3), (65536, 4, 1, 16)]:
+        total, _ = tffn.debug_engine_task(mb, n1, n2, gm, 0)
+        assert total == mb * (n1 + n2)
+        first = min(gm, mb)
+        picks = set(rnd.randrange(total) for _ in range(2000))
+        picks |= {0, first * n1 - 1, first * n1, total - 1, total - first * n2, max(total - first * n2 - 1, 0)}
+        for t in sorted(picks):
+            tot_t, (layer, band, tile) = tffn.debug_engine_task(mb, n1, n2, gm, t)
+            assert tot_t == total, (mb, n1, n2, gm, t)
+            assert layer in (0, 1) and 0 <= band < mb
+            assert 0 <= tile < (n1 if layer == 0 else n2)
 
 
 def test_debug_tiles(lib):

@@ -1147,6 +1147,16 @@ int64_t tffn_debug_engine_task(int64_t m_blocks, int32_t n1, int32_t n2, int32_t
     EngineTask t = engine_task(ticket, m_blocks, n1, n2, group_m, MODE_FUSED);
     if (ticket >= total)
         t.layer = -1;
+    // The kernel maps tickets in 32-bit arithmetic: check it against this
+    // 64-bit form wherever a launch may use it.
+    if (total <= ENGINE_MAX_TICKETS && ticket >= 0 && ticket < ENGINE_MAX_TICKETS) {
+        EngineTask t32 = engine_task_t<int32_t>(static_cast<int32_t>(ticket), static_cast<int32_t>(m_blocks), n1,
+                                                n2, group_m, MODE_FUSED);
+        if (ticket >= total)
+            t32.layer = -1;
+        if (t32.layer != t.layer || (t.layer >= 0 && (t32.band != t.band || t32.tile != t.tile)))
+            return -1;
+    }
     if (out) {
         out[0] = t.layer;
         out[1] = t.band;
