@@ -152,18 +152,31 @@ static __device__ __noinline__ bool wait_flag(const WaitCtx& w, const uint32_t* 
 
 // Activations (fp32).  GELU uses the tanh form written through the identity
 // 0.5 x (1 + tanh(u)) = x / (1 + exp(-2u)), which keeps full relative accuracy
-// for negative x where 1 + tanh(u) would cancel.  SiLU is x sigma(x) =
-// x / (1 + exp(-x)); the exponent is capped at 80 so the denominator stays
-// finite (below x = -80 the result is below 1e-33 in magnitude either way).
+// for negative x where 1 + tanh(u) would cancel.  With u = sqrt(2/pi) (x +
+// 0.044715 x^3), exp(-2u) = 2^(x (c0 + c1 x^2)) for c0 = -2 sqrt(2/pi) log2(e)
+// and c1 = 0.044715 c0: three multiply-adds before the base-2 exponential
+// (the epilogue's activation arithmetic shows in the whole launch's time).
+// A very negative x gives 2^y = inf and a result of -0, GELU's limit; below
+// 2^-126 (x beyond ~10) the exponential flushes to 0 and the result is x.
+// SiLU is x sigma(x) = x / (1 + exp(-x)); the exponent is capped at 80 so the
+// denominator stays finite (below x = -80 the result is below 1e-33 in
+// magnitude either way).
+__device__ __forceinline__ float ex2_approx(float y)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+
 __device__ __forceinline__ float act_apply(int act, float x)
 {
     if (act == TFFN_ACT_RELU)
         return fmaxf(x, 0.0f);
     if (act == TFFN_ACT_GELU_TANH) {
-        const float k0 = 0.7978845608028654f;   // sqrt(2/pi)
-        const float k1 = 0.044715f;
-        const float u = k0 * fmaf(k1 * x, x * x, x);
-        return __fdividef(x, 1.0f + __expf(-2.0f * u));
+        const float c0 = -2.3022082f;    // -2 sqrt(2/pi) / ln 2
+        const float c1 = -0.10294324f;   // 0.044715 c0
+        const float e = ex2_approx(x * fmaf(c1, x * x, c0));
+        return __fdividef(x, 1.0f + e);
     }
     if (act == TFFN_ACT_SILU)
         return __fdividef(x, 1.0f + __expf(fminf(-x, 80.0f)));
