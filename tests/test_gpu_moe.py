@@ -53,6 +53,7 @@ def _check_routing(r, logits, k, E):
     (40, 64, 128, 64, 1, 1, ("relu", "none")),
     (50, 64, 128, 64, 4, 4, ("gelu_tanh", "none")),      # top_k = E
     (200, 1024, 256, 128, 4, 2, ("gelu_tanh", "none")),  # N > O
+    (5000, 64, 128, 64, 40, 2, ("relu", "none")),        # 40 token blocks, more experts than warps in the plan
 ])
 def test_moe_small_full(cuda_lib, T, N, O, P, E, k, acts):
     inp = _inputs(T, N, O, P, E, seed=T + E)

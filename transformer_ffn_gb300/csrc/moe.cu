@@ -71,7 +71,8 @@ __global__ void __launch_bounds__(ROUTE_BLOCK) route_kernel(const float* __restr
 }
 
 // --------------------------------------------------------------------- plan
-// One small CTA.  From the per-block counts: each expert's padded segment
+// One CTA, one warp per expert (up to 32; a warp takes experts w, w + 32).
+// From the per-block counts: each expert's padded segment
 // (laid out in expert index order, or, with size_desc, largest row count
 // first -- ties to the lower index -- the schedule order of "Fine-Grained
 // Compute-Communication Overlap for MoE", section 4.4, rule (ii)), the band
@@ -86,12 +87,22 @@ __global__ void plan_kernel(const int32_t* __restrict__ blk_hist, int nblk, int 
 {
     __shared__ int32_t tot[64], s_pad[64], s_end[64], s_off[65];
     __shared__ int32_t s_nbands;
-    const int e = threadIdx.x;
-    if (e < E) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    // Each warp sums the token blocks' counts of its experts, 32 blocks at a time.
+    for (int e = warp; e < E; e += nwarps) {
         int32_t c = 0;
-        for (int b = 0; b < nblk; ++b)
-            c += blk_hist[static_cast<int64_t>(b) * E + e];
-        tot[e] = c;
+        for (int b0 = 0; b0 < nblk; b0 += 32) {
+            const int b = b0 + lane;
+            int32_t v = b < nblk ? blk_hist[static_cast<int64_t>(b) * E + e] : 0;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1)
+                v += __shfl_xor_sync(0xffffffffu, v, d);
+            c += v;
+        }
+        if (lane == 0)
+            tot[e] = c;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -124,18 +135,33 @@ __global__ void plan_kernel(const int32_t* __restrict__ blk_hist, int nblk, int 
         *nbands = p / bm;
     }
     __syncthreads();
-    if (e < E) {
+    // Each block's first row in the padded and in the unpadded layout, per
+    // expert: an exclusive prefix sum over the blocks in token order.
+    for (int e = warp; e < E; e += nwarps) {
         int32_t rp = s_pad[e], ro = s_off[e];
-        for (int b = 0; b < nblk; ++b) {
+        for (int b0 = 0; b0 < nblk; b0 += 32) {
+            const int b = b0 + lane;
             const int64_t at = static_cast<int64_t>(b) * E + e;
-            blk_pad[at] = rp;
-            blk_off[at] = ro;
-            const int32_t c = blk_hist[at];
-            rp += c;
-            ro += c;
+            const int32_t v = b < nblk ? blk_hist[at] : 0;
+            int32_t incl = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t u = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d)
+                    incl += u;
+            }
+            if (b < nblk) {
+                blk_pad[at] = rp + incl - v;
+                blk_off[at] = ro + incl - v;
+            }
+            const int32_t chunk = __shfl_sync(0xffffffffu, incl, 31);
+            rp += chunk;
+            ro += chunk;
         }
-        pad[2 * e] = s_pad[e] + tot[e];
-        pad[2 * e + 1] = s_end[e] - (s_pad[e] + tot[e]);
+        if (lane == 0) {
+            pad[2 * e] = s_pad[e] + tot[e];
+            pad[2 * e + 1] = s_end[e] - (s_pad[e] + tot[e]);
+        }
     }
     for (int b = threadIdx.x; b < s_nbands; b += blockDim.x) {
         int x = 0;
@@ -270,8 +296,9 @@ int launch_moe_plan(const int32_t* blk_hist, int64_t T, int E, int bm, int size_
                     int32_t* blk_off, int32_t* band_expert, int32_t* nbands, int32_t* pad, int32_t* offs_out,
                     cudaStream_t s)
 {
-    moe::plan_kernel<<<1, 64, 0, s>>>(blk_hist, moe_route_blocks(T), E, bm, size_desc, blk_pad, blk_off,
-                                      band_expert, nbands, pad, offs_out);
+    const int warps = E < 32 ? E : 32;   // one warp per expert, up to 32
+    moe::plan_kernel<<<1, 32 * warps, 0, s>>>(blk_hist, moe_route_blocks(T), E, bm, size_desc, blk_pad, blk_off,
+                                              band_expert, nbands, pad, offs_out);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
