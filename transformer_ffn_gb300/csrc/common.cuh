@@ -158,9 +158,9 @@ static __device__ __noinline__ bool wait_flag(const WaitCtx& w, const uint32_t* 
 // (the epilogue's activation arithmetic shows in the whole launch's time).
 // A very negative x gives 2^y = inf and a result of -0, GELU's limit; below
 // 2^-126 (x beyond ~10) the exponential flushes to 0 and the result is x.
-// SiLU is x sigma(x) = x / (1 + exp(-x)); the exponent is capped at 80 so the
-// denominator stays finite (below x = -80 the result is below 1e-33 in
-// magnitude either way).
+// SiLU is x sigma(x) = x / (1 + exp(-x)), exp(-x) taken the same way; the
+// exponent is capped at 80 so the denominator stays finite (below x = -80
+// the result is below 1e-33 in magnitude either way).
 __device__ __forceinline__ float ex2_approx(float y)
 {
     float r;
@@ -179,7 +179,7 @@ __device__ __forceinline__ float act_apply(int act, float x)
         return __fdividef(x, 1.0f + e);
     }
     if (act == TFFN_ACT_SILU)
-        return __fdividef(x, 1.0f + __expf(fminf(-x, 80.0f)));
+        return __fdividef(x, 1.0f + ex2_approx(fmaxf(x, -80.0f) * -1.44269504f));   // exp(-x) = 2^(-x / ln 2)
     return x;
 }
 
