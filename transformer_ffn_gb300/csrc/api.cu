@@ -59,7 +59,6 @@ static uint32_t* band_counts(uint8_t* base, int64_t bands)
     return static_cast<size_t>(bands) * 2 <= BCOUNT_WORDS ? reinterpret_cast<uint32_t*>(base + OFF_BCOUNT) : nullptr;
 }
 
-
 constexpr int64_t DECODE_MAX_M = 32;   // the mma.sync weight stream wins up to here (measured)
 constexpr int64_t STREAM_MAX_M = 128;  // then the tensor-core weight stream, then the engine (measured);
                                        // up to 256 rows while its window layer 1 applies
