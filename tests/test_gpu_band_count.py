@@ -104,6 +104,26 @@ def test_counts_zero_after_a_launch_that_timed_out(fused):
         ws.close()
 
 
+def test_counts_zero_after_gated_launches(fused):
+    # gated layer-1 tiles hold 128 hidden columns (their W1 and W3 halves):
+    # a band has O / 128 of them, each counted by its eight epilogue warps
+    M, N, O, P = 1280, 512, 1536, 512
+    g = synth.glu_inputs(M, N, O, P, seed=9, device="cuda")
+    ws = _Workspace(fused, fused.workspace_bytes(M, N, O, P))
+    try:
+        u = synth.to_u16
+        host = (u(g.X), u(g.W1), u(g.W3), u(g.W2))
+        rows = parity.band_rows(M)
+        want = parity.oracle_rows(lambda r: oracle.glu_ffn(*host, oracle.ACT_SILU, rows=r), rows)
+        for rep in range(2):
+            Y = fused.ffn_glu_forward(g.X, g.W1, g.W3, g.W2, "silu")
+            fused.check()
+            assert not ws.counts().any(), f"gated launch {rep}"
+            parity.assert_close(Y[rows].float().cpu().numpy(), want, f"gated launch {rep}")
+    finally:
+        ws.close()
+
+
 def test_counts_zero_after_moe_launches(cuda_lib):
     T, N, O, P, E, k = 1500, 256, 768, 256, 4, 2
     inp = synth.moe_inputs(T, N, O, P, E, seed=5, device="cuda")
